@@ -1,0 +1,58 @@
+"""Planted mistakes in copies of the oracle must each fail at least one pin.
+
+Every mutant is a one-place textual edit of nsv_oracle.c (a dropped term, a
+wrong sign, a wrong or transposed index, an off-by-one mask, the wrong
+operand), compiled into a temporary library on the CPU.  If some plausible
+mistake could slip past every pin, the pins would not be pinning the oracle.
+"""
+
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+MUTANTS = {
+    "drop_scale": ("s[t] = scale * acc;", "s[t] = acc;"),
+    "mask_off_by_one": ("s[t] = (t < c) ? s[t] : -INFINITY;",
+                        "s[t] = (t <= c && t < W) ? s[t] : -INFINITY;"),
+    "kv_head_modulo": ("int64_t g = h / group;", "int64_t g = h % Hkv;"),
+    "pool_layout_transposed": ("int64_t base = ((b * Hkv + g) * B + t % B) * D;",
+                               "int64_t base = ((b * B + t % B) * Hkv + g) * D;"),
+    "token_offset_shifted": ("int64_t base = ((b * Hkv + g) * B + t % B) * D;",
+                             "int64_t base = ((b * Hkv + g) * B + (t + 1) % B) * D;"),
+    "softmax_sign": ("s[t] = exp(s[t] - m);", "s[t] = exp(m - s[t]);"),
+    "no_normalisation": ("s[t] /= z;", "s[t] /= 1.0;"),
+    "pv_uses_keys": ("o[d] += s[t] * Vrect[t * D + d];", "o[d] += s[t] * Krect[t * D + d];"),
+    "query_transposed": ("qv[d] = widen(q, dtype, (r * H + h) * D + d);",
+                         "qv[d] = widen(q, dtype, (h * R + r) * D + d);"),
+    "no_negative_wrap": ("b += pool_blocks;", "b = 0;"),
+    "kv_write_swaps_k_v": ("memcpy((char *)k_pool + dst, (const char *)k_new + src,",
+                           "memcpy((char *)k_pool + dst, (const char *)v_new + src,"),
+    "kv_write_offset_dropped": ("int64_t blk = write_slots[r] / B, off = write_slots[r] % B;",
+                                "int64_t blk = write_slots[r] / B, off = 0;"),
+    "walk_floor_not_ceil": ("n += (context_lens[r] + tile - 1) / tile;",
+                            "n += context_lens[r] / tile;"),
+    "rect_bytes_fp16": ("return R * H * width * 4;", "return R * H * width * 2;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    with open(oracle.SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, "mutation site for %s must occur exactly once" % name
+    path = os.path.join(str(tmp_path), "mutant_%s.c" % name)
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    lib = oracle.compile_source(path, os.path.join(str(tmp_path), "libmutant_%s.so" % name))
+    mutant = oracle.Oracle(lib)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(mutant)
+        except Exception as e:  # an assertion or a refusal both count as caught
+            caught.append((pin.__name__, type(e).__name__))
+    assert caught, "mutant %s passed every pin" % name
