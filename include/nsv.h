@@ -1,0 +1,234 @@
+/*
+ * nsv.h -- C ABI of the GB300 (sm_103a) batched paged-attention decode read
+ * and KV append.
+ *
+ * The operation, as the nanoserve daily log defines it:
+ *
+ *   KV append (nanoserve Day 55, "the capture list moved to startup, and the
+ *   dummy batch was all padding", section "Why it matters"): the step's new
+ *   key and value of every row land at the row's write slot, as one indexed
+ *   write over the padded batch.  A padded row's write slot is the sink slot,
+ *   "one past the pool the allocator hands out": a legal address that no
+ *   block table can name.
+ *
+ *   Decode read (nanoserve Day 59, "the rectangle the read builds, and the
+ *   tile that replaces it", sections "What I added today" and "What I
+ *   learned" items 3-4): one query token per row and per query head attends
+ *   over that row's own context_lens[row] keys and values.  Position t of a
+ *   row lives in pool block block_tables[row][t / block_size] at offset
+ *   t % block_size (block-id addressing, Day 51, "the read rectangle stopped
+ *   being built", section "Why it matters").  The read walks
+ *   cdiv(ctx, block_size) blocks of the row, never the rest of the table,
+ *   and folds them with an online softmax (running max, running denominator,
+ *   running weighted sum of V).  Output = softmax(scale * q.K^T) V over the
+ *   row's positions; a row with context length 0 attends over nothing and
+ *   its output is 0.
+ *
+ * Ownership: every pointer passed in is owned by the caller; the library
+ * never frees, retains or reallocates caller memory.  Device pointers must
+ * be device memory of the current CUDA device.  All calls are asynchronous
+ * on the given stream unless stated otherwise.
+ *
+ * Layouts (all C-contiguous, no strides; element type from nsv_shape.dtype):
+ *   q, out          [rows][num_heads][head_dim]
+ *   k_pool, v_pool  [num_blocks + 1][num_kv_heads][block_size][head_dim]
+ *                   the last block (index num_blocks) is the sink block;
+ *                   flat slot s is (block s / block_size, offset
+ *                   s % block_size); the sink slot is num_blocks*block_size.
+ *   k_new, v_new    [rows][num_kv_heads][head_dim]
+ *   write_slots     [rows] int64
+ *   block_tables    [rows][max_blocks] int32; entries at or past
+ *                   cdiv(context_lens[r], block_size) are never read and may
+ *                   hold anything (-1 by convention)
+ *   context_lens    [rows] int32
+ * Query head h reads KV head h / (num_heads / num_kv_heads).
+ * Every data pointer must be 16-byte aligned.
+ *
+ * Errors: every entry point returns NSV_OK (0) or a negative NSV_ERR_* code
+ * after checking its host-visible arguments; nothing is launched when an
+ * error is returned.  Values that live in device memory (context lengths,
+ * block ids, write slots) are checked by the kernels themselves: a bad value
+ * never causes an out-of-bounds access; the offending row, block or write is
+ * skipped and a bit is set in the device status word (nsv_device_status).
+ * No kernel traps.
+ */
+#ifndef NSV_H
+#define NSV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define NSV_API __attribute__((visibility("default")))
+#else
+#define NSV_API
+#endif
+
+/* Element types of q, out, pools and new K/V (one type for all of them). */
+enum { NSV_F32 = 0, NSV_BF16 = 1 };
+
+/* Return codes. */
+enum {
+    NSV_OK = 0,
+    NSV_ERR_NULLPTR = -1,     /* a required pointer is NULL */
+    NSV_ERR_DTYPE = -2,       /* dtype is not NSV_F32 or NSV_BF16 */
+    NSV_ERR_SHAPE = -3,       /* a size is out of its documented range */
+    NSV_ERR_ALIGN = -4,       /* a data pointer is not 16-byte aligned */
+    NSV_ERR_RANGE = -5,       /* a plan field is inconsistent with the shape */
+    NSV_ERR_CAPTURE = -6,     /* the library workspace must grow while the
+                                 stream is being captured */
+    NSV_ERR_CUDA = -7,        /* a CUDA runtime call failed */
+    NSV_ERR_WORKSPACE = -8,   /* caller workspace smaller than the plan needs */
+    NSV_ERR_UNSUPPORTED = -10 /* head_dim or block_size the kernels lack */
+};
+
+/* Device status bits, sticky until cleared by nsv_device_status. */
+enum {
+    NSV_DEV_BAD_CTX = 1u,   /* context length outside [0, max_blocks*block_size];
+                               the row was read as empty (output 0) */
+    NSV_DEV_BAD_BLOCK = 2u, /* a walked block id outside [0, num_blocks];
+                               that block was skipped */
+    NSV_DEV_BAD_SLOT = 4u,  /* write slot outside [0, (num_blocks+1)*block_size);
+                               that row's K/V was not written */
+    NSV_DEV_TIMEOUT = 8u    /* an in-kernel wait gave up after its limit and the
+                               kernel returned early; results are invalid */
+};
+
+/* Sizes of one decode batch.  Limits: 0 <= rows <= 8192; num_heads a
+ * multiple of num_kv_heads with num_heads/num_kv_heads <= 16; head_dim 64 or
+ * 128; block_size 16; 1 <= max_blocks with max_blocks*block_size < 2^31;
+ * 1 <= num_blocks < 2^31 - 1. */
+typedef struct nsv_shape {
+    int32_t rows;
+    int32_t num_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    int32_t max_blocks;   /* block-table row length; width = max_blocks*block_size */
+    int64_t num_blocks;   /* blocks the allocator hands out; pools hold one more */
+    int32_t dtype;        /* NSV_F32 or NSV_BF16 */
+    int32_t reserved;     /* must be 0 */
+} nsv_shape;
+
+/* Launch plan of the decode read.  A plan depends on the shape and the SM
+ * count only, never on the values of context_lens, so one plan serves every
+ * step of a given shape (and a captured graph of it). */
+enum { NSV_MODE_SINGLE = 1, NSV_MODE_SPLIT = 2 };
+
+typedef struct nsv_plan {
+    int32_t mode;             /* NSV_MODE_SINGLE: one work item per (row, head
+                                 group); NSV_MODE_SPLIT: a row's blocks are cut
+                                 into chunks whose partial softmax states are
+                                 merged by a combine kernel */
+    int32_t chunk_blocks;     /* blocks per work item */
+    int32_t max_splits;       /* cdiv(max_blocks, chunk_blocks) */
+    int32_t kv_heads_per_cta; /* KV heads one CTA streams together */
+    int32_t stages;           /* shared-memory pipeline depth */
+    int32_t ctas_per_sm;      /* resident CTAs per SM the grid is sized for */
+    int32_t grid;             /* persistent CTAs launched */
+    int32_t threads;          /* threads per CTA */
+    int32_t smem_bytes;       /* dynamic shared memory per CTA */
+    int32_t num_sms;          /* SM count the plan was made for */
+    int64_t workspace_bytes;  /* scratch the split path needs (0 for single) */
+} nsv_plan;
+
+/*
+ * Plan the decode read for `shape` on a GPU with `num_sms` SMs (<= 0: the
+ * current device's count).  Host-only apart from that optional device query;
+ * deterministic; depends on the shape alone.  Returns NSV_OK or
+ * NSV_ERR_{NULLPTR, DTYPE, SHAPE, UNSUPPORTED, CUDA}.
+ */
+NSV_API int nsv_plan_split(const nsv_shape *shape, int num_sms, nsv_plan *plan);
+
+/*
+ * The same planner with some choices fixed (any argument <= 0 is chosen by
+ * the heuristic): chunk_blocks (>= max_blocks gives the single-pass mode),
+ * kv_heads_per_cta (must divide num_kv_heads), stages (2..8), ctas_per_sm
+ * (1..4) and grid (persistent CTAs; default num_sms * ctas_per_sm, capped
+ * by the number of work items).  Returns NSV_ERR_RANGE when a fixed choice
+ * does not fit the shape or the shared-memory limit.
+ */
+NSV_API int nsv_plan_custom(const nsv_shape *shape, int num_sms, int chunk_blocks,
+                            int kv_heads_per_cta, int stages, int ctas_per_sm,
+                            int grid, nsv_plan *plan);
+
+/*
+ * KV append: for every row r, k_pool/v_pool at slot write_slots[r] receive
+ * k_new[r]/v_new[r] (all KV heads), bit for bit.  Real rows' slots must be
+ * distinct; any number of padded rows may name the sink slot, whose contents
+ * are then unspecified.  Pool bytes at every other slot are untouched.
+ * A slot outside [0, (num_blocks+1)*block_size) is skipped and sets
+ * NSV_DEV_BAD_SLOT.  Uses shape.rows, num_kv_heads, head_dim, block_size,
+ * num_blocks, dtype (num_heads and max_blocks must still be valid).
+ */
+NSV_API int nsv_kv_write(const nsv_shape *shape, const void *k_new, const void *v_new,
+                         const int64_t *write_slots, void *k_pool, void *v_pool,
+                         cudaStream_t stream);
+
+/*
+ * Decode read with the default plan and a library-owned workspace (one per
+ * device, grown with cudaMalloc on first need and kept until exit; returns
+ * NSV_ERR_CAPTURE instead of growing it while `stream` is capturing, so make
+ * one uncaptured call of each shape first).  Calls on different streams of
+ * one device must not overlap when they share that workspace.
+ * out[r][h] = softmax over the row's positions of scale * q[r][h].K, times V.
+ */
+NSV_API int nsv_paged_decode(const nsv_shape *shape, const void *q, const void *k_pool,
+                             const void *v_pool, const int32_t *block_tables,
+                             const int32_t *context_lens, float scale, void *out,
+                             cudaStream_t stream);
+
+/*
+ * Decode read with an explicit plan (NULL: the default plan) and a
+ * caller-owned device workspace of at least plan->workspace_bytes bytes
+ * (256-byte aligned; may be NULL when that is 0).  The workspace holds no
+ * state between calls.  Two calls that overlap on the GPU need two
+ * workspaces.  A plan passed in must be one nsv_plan_split/nsv_plan_custom
+ * returned for this shape (NSV_ERR_RANGE otherwise).
+ */
+NSV_API int nsv_paged_decode_ws(const nsv_shape *shape, const nsv_plan *plan,
+                                const void *q, const void *k_pool, const void *v_pool,
+                                const int32_t *block_tables, const int32_t *context_lens,
+                                float scale, void *out, void *workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * One serving step: nsv_kv_write then the decode read on the same stream.
+ * context_lens already count the appended token (its write slot is the
+ * row's last real position).  plan/workspace as in nsv_paged_decode_ws;
+ * workspace NULL with workspace_bytes 0 uses the library-owned workspace.
+ */
+NSV_API int nsv_decode_step(const nsv_shape *shape, const nsv_plan *plan, const void *q,
+                            const void *k_new, const void *v_new,
+                            const int64_t *write_slots, void *k_pool, void *v_pool,
+                            const int32_t *block_tables, const int32_t *context_lens,
+                            float scale, void *out, void *workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronise the current device, then report its status word (NSV_DEV_*
+ * bits raised since the last clear) and the number of (row, block) pairs the
+ * decode kernels walked (each row's cdiv(ctx, block_size) blocks, counted
+ * once per row, not per head).  Either output pointer may be NULL.  clear != 0
+ * resets both.  Not for use inside stream capture.
+ */
+NSV_API int nsv_device_status(uint32_t *status, uint64_t *blocks_walked, int clear);
+
+/* Static description of a return code. */
+NSV_API const char *nsv_strerror(int code);
+
+/* ABI version of this header (major * 100 + minor). */
+NSV_API int nsv_abi_version(void);
+
+#define NSV_ABI_VERSION 100
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NSV_H */

@@ -1,0 +1,395 @@
+// Host side of the C ABI declared in include/nsv.h: argument checks, the
+// shape-only launch planner, per-device state (the device status word and
+// the library-owned workspace) and the entry points.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "nsv_common.cuh"
+
+namespace nsv {
+
+// Sticky device status (NSV_DEV_* bits) and the walked-block counter.
+__device__ uint32_t g_status;
+__device__ unsigned long long g_walked;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kSmemPerSm = 228 * 1024;     // shared memory per SM on sm_103
+constexpr int kSmemPerCta = 227 * 1024;    // opt-in maximum per CTA
+constexpr int kSmemReserved = 1024;        // per-CTA system reservation
+constexpr int kThreadsPerSm = 2048;
+
+struct DeviceState {
+  bool ready = false;
+  uint32_t* status = nullptr;
+  unsigned long long* walked = nullptr;
+  int num_sms = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+};
+
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+int cuda_fail() {
+  (void)cudaGetLastError();  // do not leave a stale error for the next caller
+  return NSV_ERR_CUDA;
+}
+
+// Per-device set-up on first use: symbol addresses of the status words,
+// kernel attributes, SM count.  Needs the device current.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail();
+  if (dev < 0 || dev >= kMaxDevices) return NSV_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status) != cudaSuccess)
+      return cuda_fail();
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.walked), g_walked) != cudaSuccess)
+      return cuda_fail();
+    if (prepare_decode_kernels() != cudaSuccess) return cuda_fail();
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return cuda_fail();
+    d.ready = true;
+  }
+  *out = &d;
+  return NSV_OK;
+}
+
+int elem_bytes(int dtype) { return dtype == NSV_F32 ? 4 : 2; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const nsv_shape* s) {
+  if (!s) return NSV_ERR_NULLPTR;
+  if (s->dtype != NSV_F32 && s->dtype != NSV_BF16) return NSV_ERR_DTYPE;
+  if (s->reserved != 0) return NSV_ERR_SHAPE;
+  if (s->rows < 0 || s->rows > kMaxRows) return NSV_ERR_SHAPE;
+  if (s->num_heads < 1 || s->num_kv_heads < 1 || s->num_heads % s->num_kv_heads != 0)
+    return NSV_ERR_SHAPE;
+  if (s->num_heads / s->num_kv_heads > kMaxConsumerWarps) return NSV_ERR_SHAPE;
+  if (s->head_dim != 64 && s->head_dim != 128) return NSV_ERR_UNSUPPORTED;
+  if (s->block_size != kBlock) return NSV_ERR_UNSUPPORTED;
+  if (s->max_blocks < 1 || (int64_t)s->max_blocks * s->block_size >= (int64_t(1) << 31))
+    return NSV_ERR_SHAPE;
+  if (s->num_blocks < 1 || s->num_blocks > (int64_t(1) << 31) - 2) return NSV_ERR_SHAPE;
+  return NSV_OK;
+}
+
+int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int make_plan(const nsv_shape* s, int num_sms, int chunk, int hg, int stages, int cps, int grid,
+              nsv_plan* p) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (!p) return NSV_ERR_NULLPTR;
+  if (num_sms <= 0) {
+    DeviceState* d = nullptr;
+    if ((rc = device_state(&d)) != NSV_OK) return rc;
+    num_sms = d->num_sms;
+  }
+  const int elem = elem_bytes(s->dtype);
+  const int G = s->num_heads / s->num_kv_heads;
+  const int tile = kBlock * s->head_dim * elem;
+  if (hg <= 0) {
+    // Largest KV-head group whose K+V stage stays within 32 KiB and whose
+    // query heads fill at most 8 consumer warps.
+    hg = 1;
+    const int cands[4] = {8, 4, 2, 1};
+    for (int c : cands) {
+      if (s->num_kv_heads % c == 0 && c * G <= 8 && 2 * c * tile <= 32 * 1024) {
+        hg = c;
+        break;
+      }
+    }
+  } else if (s->num_kv_heads % hg != 0 || hg * G > kMaxConsumerWarps) {
+    return NSV_ERR_RANGE;
+  }
+  const int rows_for_layout = s->rows > 0 ? s->rows : 1;
+  const bool auto_stages = stages <= 0;
+  if (auto_stages) stages = 3;
+  if (stages < 2 || stages > 8) return NSV_ERR_RANGE;
+  SmemLayout L = make_layout(elem, s->head_dim, hg, G, stages, rows_for_layout);
+  while (auto_stages && L.total > (uint32_t)kSmemPerCta && stages > 2) {
+    --stages;
+    L = make_layout(elem, s->head_dim, hg, G, stages, rows_for_layout);
+  }
+  if (L.total > (uint32_t)kSmemPerCta) return NSV_ERR_RANGE;
+  const int threads = (hg * G + 1) * 32;
+  const int fit = kSmemPerSm / (int)(L.total + kSmemReserved);
+  const int fit_threads = kThreadsPerSm / threads;
+  if (cps <= 0) {
+    cps = fit < 2 ? fit : 2;
+    if (cps > fit_threads) cps = fit_threads;
+    if (cps < 1) cps = 1;
+  } else if (cps > 4 || cps > fit || cps > fit_threads) {
+    return NSV_ERR_RANGE;
+  }
+  const int64_t slots = (int64_t)num_sms * cps;
+  const int64_t units = (int64_t)s->rows * (s->num_kv_heads / hg);
+  if (chunk <= 0) {
+    // Longest chunk (in blocks) that still gives the grid >= 32 items per
+    // CTA if every row were full width; short chunks bound the tail.
+    chunk = 8;
+    const int cands[3] = {32, 16, 8};
+    for (int c : cands) {
+      if (units * cdiv64(s->max_blocks, c) >= 32 * slots) {
+        chunk = c;
+        break;
+      }
+    }
+  }
+  int mode, splits;
+  if (chunk >= s->max_blocks) {
+    mode = NSV_MODE_SINGLE;
+    chunk = s->max_blocks;
+    splits = 1;
+  } else {
+    mode = NSV_MODE_SPLIT;
+    splits = (int)cdiv64(s->max_blocks, chunk);
+  }
+  const int64_t items = units * splits;
+  if (grid <= 0) {
+    int64_t g = slots < items ? slots : items;
+    grid = (int)(g > 0 ? g : 1);
+  } else if (grid > (1 << 20)) {
+    return NSV_ERR_RANGE;
+  }
+  int64_t ws = 0;
+  if (splits > 1) {
+    const int64_t n = (int64_t)s->rows * s->num_heads * splits;
+    ws = cdiv64(n * 8, 256) * 256 + n * s->head_dim * 4;
+  }
+  memset(p, 0, sizeof(*p));
+  p->mode = mode;
+  p->chunk_blocks = chunk;
+  p->max_splits = splits;
+  p->kv_heads_per_cta = hg;
+  p->stages = stages;
+  p->ctas_per_sm = cps;
+  p->grid = grid;
+  p->threads = threads;
+  p->smem_bytes = (int)L.total;
+  p->num_sms = num_sms;
+  p->workspace_bytes = ws;
+  return NSV_OK;
+}
+
+// A caller's plan must be exactly what the planner makes from its choices.
+int check_plan(const nsv_shape* s, const nsv_plan* given, nsv_plan* use) {
+  int rc = make_plan(s, given->num_sms, given->chunk_blocks, given->kv_heads_per_cta,
+                     given->stages, given->ctas_per_sm, given->grid, use);
+  if (rc) return rc;
+  if (memcmp(use, given, sizeof(nsv_plan)) != 0) return NSV_ERR_RANGE;
+  return NSV_OK;
+}
+
+int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, const void* k_pool,
+                const void* v_pool, const int32_t* block_tables, const int32_t* context_lens,
+                float scale, void* out, void* ws, size_t ws_bytes, bool library_ws,
+                cudaStream_t stream) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return NSV_ERR_NULLPTR;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return NSV_ERR_ALIGN;
+  nsv_plan plan;
+  if (plan_in) {
+    if ((rc = check_plan(s, plan_in, &plan)) != NSV_OK) return rc;
+  }
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d)) != NSV_OK) return rc;
+  if (!plan_in) {
+    if ((rc = make_plan(s, d->num_sms, 0, 0, 0, 0, 0, &plan)) != NSV_OK) return rc;
+  }
+  if (s->rows == 0) return NSV_OK;
+  if (library_ws && plan.workspace_bytes > 0) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((size_t)plan.workspace_bytes > d->ws_bytes) {
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return cuda_fail();
+      if (cs != cudaStreamCaptureStatusNone) return NSV_ERR_CAPTURE;
+      if (d->ws) {
+        if (cudaFree(d->ws) != cudaSuccess) return cuda_fail();
+        d->ws = nullptr;
+        d->ws_bytes = 0;
+      }
+      if (cudaMalloc(&d->ws, (size_t)plan.workspace_bytes) != cudaSuccess) return cuda_fail();
+      d->ws_bytes = (size_t)plan.workspace_bytes;
+    }
+    ws = d->ws;
+    ws_bytes = d->ws_bytes;
+  }
+  if (plan.workspace_bytes > 0) {
+    if (!ws || ws_bytes < (size_t)plan.workspace_bytes ||
+        (reinterpret_cast<uintptr_t>(ws) & 255u))
+      return NSV_ERR_WORKSPACE;
+  }
+  const int64_t nslots = (int64_t)s->rows * s->num_heads * plan.max_splits;
+  DecodeParams p;
+  p.q = q;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.ws_ml = plan.workspace_bytes ? static_cast<float2*>(ws) : nullptr;
+  p.ws_acc = plan.workspace_bytes
+                 ? reinterpret_cast<float*>(static_cast<char*>(ws) + cdiv64(nslots * 8, 256) * 256)
+                 : nullptr;
+  p.status = d->status;
+  p.walked = d->walked;
+  p.pool_blocks = s->num_blocks + 1;
+  p.rows = s->rows;
+  p.heads = s->num_heads;
+  p.kv_heads = s->num_kv_heads;
+  p.max_blocks = s->max_blocks;
+  p.chunk_blocks = plan.chunk_blocks;
+  p.max_splits = plan.max_splits;
+  p.heads_per_cta = plan.kv_heads_per_cta;
+  p.group = s->num_heads / s->num_kv_heads;
+  p.stages = plan.stages;
+  p.qscale = scale * 1.4426950408889634f;  // log2(e): the kernels use exp2
+  if (launch_decode(p, s->dtype, s->head_dim, plan.grid, plan.threads, plan.smem_bytes, stream) !=
+      cudaSuccess)
+    return cuda_fail();
+  if (plan.mode == NSV_MODE_SPLIT) {
+    CombineParams c;
+    c.context_lens = context_lens;
+    c.ws_ml = p.ws_ml;
+    c.ws_acc = p.ws_acc;
+    c.out = out;
+    c.rows = s->rows;
+    c.heads = s->num_heads;
+    c.max_blocks = s->max_blocks;
+    c.chunk_blocks = plan.chunk_blocks;
+    c.max_splits = plan.max_splits;
+    if (launch_combine(c, s->dtype, s->head_dim, stream) != cudaSuccess) return cuda_fail();
+  }
+  return NSV_OK;
+}
+
+}  // namespace
+}  // namespace nsv
+
+using namespace nsv;
+
+extern "C" {
+
+NSV_API int nsv_abi_version(void) { return NSV_ABI_VERSION; }
+
+NSV_API const char* nsv_strerror(int code) {
+  switch (code) {
+    case NSV_OK: return "success";
+    case NSV_ERR_NULLPTR: return "a required pointer is NULL";
+    case NSV_ERR_DTYPE: return "dtype must be NSV_F32 or NSV_BF16";
+    case NSV_ERR_SHAPE: return "a size is outside its documented range";
+    case NSV_ERR_ALIGN: return "a data pointer is not 16-byte aligned";
+    case NSV_ERR_RANGE: return "a plan field does not fit the shape";
+    case NSV_ERR_CAPTURE: return "the library workspace would have to grow during stream capture";
+    case NSV_ERR_CUDA: return "a CUDA runtime call failed";
+    case NSV_ERR_WORKSPACE: return "workspace missing, misaligned or smaller than the plan needs";
+    case NSV_ERR_UNSUPPORTED: return "head_dim must be 64 or 128 and block_size 16";
+    default: return "unknown nsv error code";
+  }
+}
+
+NSV_API int nsv_plan_split(const nsv_shape* shape, int num_sms, nsv_plan* plan) {
+  return make_plan(shape, num_sms, 0, 0, 0, 0, 0, plan);
+}
+
+NSV_API int nsv_plan_custom(const nsv_shape* shape, int num_sms, int chunk_blocks,
+                            int kv_heads_per_cta, int stages, int ctas_per_sm, int grid,
+                            nsv_plan* plan) {
+  return make_plan(shape, num_sms, chunk_blocks, kv_heads_per_cta, stages, ctas_per_sm, grid,
+                   plan);
+}
+
+NSV_API int nsv_kv_write(const nsv_shape* s, const void* k_new, const void* v_new,
+                         const int64_t* write_slots, void* k_pool, void* v_pool,
+                         cudaStream_t stream) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (!k_new || !v_new || !write_slots || !k_pool || !v_pool) return NSV_ERR_NULLPTR;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      (reinterpret_cast<uintptr_t>(write_slots) & 7u))
+    return NSV_ERR_ALIGN;
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d)) != NSV_OK) return rc;
+  if (s->rows == 0) return NSV_OK;
+  KvWriteParams p;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.write_slots = write_slots;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.status = d->status;
+  p.pool_slots = (s->num_blocks + 1) * (long long)s->block_size;
+  p.rows = s->rows;
+  p.kv_heads = s->num_kv_heads;
+  p.vec_per_head = s->head_dim * elem_bytes(s->dtype) / 16;
+  p.block_size = s->block_size;
+  if (launch_kv_write(p, stream) != cudaSuccess) return cuda_fail();
+  return NSV_OK;
+}
+
+NSV_API int nsv_paged_decode(const nsv_shape* shape, const void* q, const void* k_pool,
+                             const void* v_pool, const int32_t* block_tables,
+                             const int32_t* context_lens, float scale, void* out,
+                             cudaStream_t stream) {
+  return decode_impl(shape, nullptr, q, k_pool, v_pool, block_tables, context_lens, scale, out,
+                     nullptr, 0, true, stream);
+}
+
+NSV_API int nsv_paged_decode_ws(const nsv_shape* shape, const nsv_plan* plan, const void* q,
+                                const void* k_pool, const void* v_pool,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                float scale, void* out, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
+  return decode_impl(shape, plan, q, k_pool, v_pool, block_tables, context_lens, scale, out,
+                     workspace, workspace_bytes, false, stream);
+}
+
+NSV_API int nsv_decode_step(const nsv_shape* shape, const nsv_plan* plan, const void* q,
+                            const void* k_new, const void* v_new, const int64_t* write_slots,
+                            void* k_pool, void* v_pool, const int32_t* block_tables,
+                            const int32_t* context_lens, float scale, void* out,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int rc = nsv_kv_write(shape, k_new, v_new, write_slots, k_pool, v_pool, stream);
+  if (rc) return rc;
+  const bool lib_ws = workspace == nullptr && workspace_bytes == 0;
+  return decode_impl(shape, plan, q, k_pool, v_pool, block_tables, context_lens, scale, out,
+                     workspace, workspace_bytes, lib_ws, stream);
+}
+
+NSV_API int nsv_device_status(uint32_t* status, uint64_t* blocks_walked, int clear) {
+  DeviceState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail();
+  uint32_t st = 0;
+  unsigned long long w = 0;
+  if (cudaMemcpy(&st, d->status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return cuda_fail();
+  if (cudaMemcpy(&w, d->walked, sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return cuda_fail();
+  if (status) *status = st;
+  if (blocks_walked) *blocks_walked = (uint64_t)w;
+  if (clear) {
+    if (cudaMemset(d->status, 0, sizeof st) != cudaSuccess) return cuda_fail();
+    if (cudaMemset(d->walked, 0, sizeof w) != cudaSuccess) return cuda_fail();
+    if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail();
+  }
+  return NSV_OK;
+}
+
+}  // extern "C"

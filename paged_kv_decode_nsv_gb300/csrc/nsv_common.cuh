@@ -1,0 +1,124 @@
+// Internal declarations shared by the library's translation units: kernel
+// parameter blocks, the shared-memory layout of the decode kernel (computed
+// identically on host and device), and the launchers each .cu file exports.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "nsv.h"
+
+namespace nsv {
+
+// The kernels are built for this block size (the pages' 16-token blocks).
+constexpr int kBlock = 16;
+// Largest number of consumer warps (query heads) one decode CTA serves.
+constexpr int kMaxConsumerWarps = 16;
+constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
+// Largest batch the decode kernel's per-CTA row tables hold.
+constexpr int kMaxRows = 8192;
+
+// Stage flags written by the producer warp for the consumers.  The low 8
+// bits of a stage's flag word carry the number of valid tokens of its block
+// and bits 16 and up the first KV head of the CTA's head group.
+enum : int {
+  kFirst = 1 << 8,   // first block of a work item: reset the softmax state
+  kLast = 1 << 9,    // last block of a work item: write out or the partial
+  kFinal = 1 << 10,  // the item is the row's only split: write `out`
+  kData = 1 << 11,   // the stage holds a K and a V tile
+  kHasQ = 1 << 12,   // the stage holds the CTA's query vectors
+  kEnd = 1 << 13,    // no more work: consumers exit
+};
+
+struct DecodeParams {
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  void* out;
+  float2* ws_ml;     // [rows][heads][max_splits] (running max, denominator)
+  float* ws_acc;     // [rows][heads][max_splits][head_dim]
+  uint32_t* status;  // device status word
+  unsigned long long* walked;  // (row, block) pairs walked
+  long long pool_blocks;       // num_blocks + 1
+  int rows, heads, kv_heads, max_blocks;
+  int chunk_blocks, max_splits;
+  int heads_per_cta;  // KV heads per CTA
+  int group;          // query heads per KV head
+  int stages;
+  float qscale;       // scale * log2(e)
+};
+
+struct CombineParams {
+  const int32_t* context_lens;
+  const float2* ws_ml;
+  const float* ws_acc;
+  void* out;
+  int rows, heads, max_blocks, chunk_blocks, max_splits;
+};
+
+struct KvWriteParams {
+  const void* k_new;
+  const void* v_new;
+  const int64_t* write_slots;
+  void* k_pool;
+  void* v_pool;
+  uint32_t* status;
+  long long pool_slots;  // (num_blocks + 1) * block_size
+  int rows, kv_heads, vec_per_head;  // 16-byte vectors per (row, head)
+  int block_size;
+};
+
+// Shared-memory carve-up of one decode CTA.
+struct SmemLayout {
+  uint32_t kv_bytes;     // one K (or V) tile set: heads_per_cta * block * D * elem
+  uint32_t q_bytes;      // the CTA's query vectors
+  uint32_t stage_bytes;  // K + V + q, rounded to 128
+  uint32_t off_meta;     // int4 per stage
+  uint32_t off_bars;     // full[stages], empty[stages] mbarriers
+  uint32_t off_pbuf;     // per consumer warp: block-size floats
+  uint32_t off_ctx;      // rows ints (validated context lengths)
+  uint32_t off_prefix;   // rows + 1 ints (work-item prefix sums)
+  uint32_t off_flag;     // abort flag
+  uint32_t total;
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) {
+  return (x + a - 1) / a * a;
+}
+
+__host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int heads_per_cta,
+                                                  int group, int stages, int rows) {
+  SmemLayout L;
+  const int cw = heads_per_cta * group;
+  L.kv_bytes = (uint32_t)(heads_per_cta * kBlock * head_dim * elem);
+  L.q_bytes = (uint32_t)(cw * head_dim * elem);
+  L.stage_bytes = align_up(2 * L.kv_bytes + L.q_bytes, 128);
+  uint32_t off = (uint32_t)stages * L.stage_bytes;
+  L.off_meta = off;
+  off += (uint32_t)stages * 16;
+  L.off_bars = align_up(off, 8);
+  off = L.off_bars + (uint32_t)stages * 16;
+  L.off_pbuf = align_up(off, 16);
+  off = L.off_pbuf + (uint32_t)(cw * kBlock * 4);
+  L.off_ctx = off;
+  off += (uint32_t)rows * 4;
+  L.off_prefix = off;
+  off += (uint32_t)(rows + 1) * 4;
+  L.off_flag = align_up(off, 4);
+  off = L.off_flag + 4;
+  L.total = align_up(off, 128);
+  return L;
+}
+
+// Launchers (return the launch's cudaError_t).
+cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int grid,
+                          int threads, int smem, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, int dtype, int head_dim,
+                           cudaStream_t stream);
+cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
+// One-time per-device attribute set-up of the decode kernels.
+cudaError_t prepare_decode_kernels();
+
+}  // namespace nsv
