@@ -1,0 +1,410 @@
+"""Benchmark of one serving step: KV append + batched paged decode read.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl nsv|reference]
+                    [--workload headline_bf16]
+
+Prints ONE JSON line (rank 0).  A step is the whole hot path over one batch:
+nsv_kv_write then the decode read (decode kernel + combine kernel), on the
+headline workload by default (256 rows, 32 heads, head_dim 128, block 16,
+width 8192, lengths uniform in [512, 8192], bf16, seeded synthetic data).
+
+value     = algorithmic bytes of a step (unique K+V read + q + out + the
+            append's read and write) x ranks / max-over-ranks seconds per
+            step, inputs resident in HBM; the step's inputs (18.8 GB) are far
+            larger than L2, so no flush is needed between steps.
+e2e       = the same metric through the C ABI with the step's inputs in
+            pinned host memory: every step copies q, k_new, v_new,
+            write_slots, block_tables and context_lens host->device and the
+            output device->host inside the timed region (the KV pool is the
+            resident cache and stays on the device).
+roofline  = the decode read alone (its two launches): read bytes (K+V + q +
+            out) / its CUDA-event time, against the measured HBM copy
+            bandwidth in MEASURED_PEAKS.json.
+cpu_baseline = the oracle (plain C, fp64) timed on this host's cores on a
+            time-bounded sample of rows of the same workload.
+
+--impl reference times that oracle as the reference arm (host cores only).
+Under torchrun each rank runs its own batch (weak scaling, no collective on
+the data path; the barrier and the max-over-ranks reduction are timing only).
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attention KV GB/s (% of GB300 HBM peak) and µs/step"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_traffic.json")
+DECODE_SRC = os.path.join(ROOT, "paged_kv_decode_nsv_gb300", "csrc", "decode.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["nsv", "reference"], default="nsv")
+    ap.add_argument("--workload", default="headline_bf16")
+    ap.add_argument("--e2e-steps", type=int, default=0,
+                    help="steps of the host-buffer measurement (default: min(steps, 100))")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="time budget of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic():
+    """DRAM bytes per decode-kernel launch from a committed ncu capture, if
+    it was taken on the kernel source as it is now (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        with open(DECODE_SRC, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if d.get("decode_cu_sha256") != sha:
+            return None
+        return d.get("traffic_bytes_per_launch_full_size")
+    except (OSError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid=None):
+        self.proc = None
+        self.uuid = device_uuid
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [r[0] for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, _, parts in rows:
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
+                "sm_mhz_min": min(sm), "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on host cores (cpu_baseline and the reference arm)
+
+
+_SAMPLE_CACHE = {}
+
+
+def oracle_throughput(wl, budget_s, threads=0, seed=12345):
+    """Run the oracle on consecutive rows of `wl` until `budget_s` passes.
+
+    Inputs: the sampled rows' own blocks as a compact pool drawn on the host
+    (same shapes, lengths and distribution as the workload).  Returns
+    (GB/s of the sample's algorithmic read bytes, rows done, seconds, threads).
+    """
+    import torch
+
+    import oracle
+    from paged_kv_decode_nsv_gb300 import workloads as W
+
+    threads = threads or oracle.max_threads()
+    done, t_total, bytes_total, r0 = 0, 0.0, 0, 0
+    per_call = max(1, threads)
+    while t_total < budget_s and r0 < wl.rows:
+        rows = tuple(range(r0, min(wl.rows, r0 + per_call)))
+        key = (wl.name, rows, seed)
+        if key not in _SAMPLE_CACHE:
+            blocks, tables, _ = W.compact_rows(wl, rows)
+            shape = (len(blocks) + 1, wl.kv_heads, wl.block_size, wl.head_dim)
+            gen = torch.Generator().manual_seed(seed * 100003 + r0)
+
+            def draw(s):
+                x = torch.randn(s, generator=gen, dtype=torch.float32)
+                if wl.dtype == "bf16":
+                    return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+                return x.numpy()
+            _SAMPLE_CACHE[key] = (draw(shape), draw(shape),
+                                  draw((len(rows), wl.heads, wl.head_dim)), tables)
+        kp, vp, q, tables = _SAMPLE_CACHE[key]
+        ctx = wl.context_lens[list(rows)]
+        t0 = time.perf_counter()
+        oracle.paged_decode(q, kp, vp, tables, ctx, wl.scale, threads=threads)
+        t_total += time.perf_counter() - t0
+        kv = int(ctx.astype(np.int64).sum()) * wl.kv_heads * wl.head_dim * 2 * wl.elem_bytes
+        bytes_total += kv + 2 * len(rows) * wl.heads * wl.head_dim * wl.elem_bytes
+        done += len(rows)
+        r0 += len(rows)
+    return bytes_total / t_total / 1e9, done, t_total, threads
+
+
+def run_reference(args, wl):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_throughput(wl, per_step)
+    vals, rows_done, secs = [], 0, 0.0
+    threads = 0
+    for _ in range(args.steps):
+        gbs, n, t, threads = oracle_throughput(wl, per_step)
+        vals.append(gbs)
+        rows_done += n
+        secs += t
+    value = float(np.median(vals))
+    sample = ("%d rows of %s (first rows, each step about %.1f s of oracle time; "
+              "compact host pool of the rows' own blocks)" % (rows_done // max(1, args.steps),
+                                                               wl.name, per_step))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "rows": wl.rows, "heads": wl.heads, "kv_heads": wl.kv_heads,
+            "head_dim": wl.head_dim, "block_size": wl.block_size, "width": wl.width,
+            "total_tokens": wl.total_tokens, "kv_dtype": wl.dtype, "accumulate": "f32",
+            "step": "kv_append + decode_read",
+            "l2": "inputs larger than L2 (no flush)" if wl.step_bytes() > 4 * 129e6
+                  else "L2 flushed between steps"}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+
+
+def run_nsv(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from paged_kv_decode_nsv_gb300 import nsv
+    from paged_kv_decode_nsv_gb300 import workloads as W
+
+    # The oracle sample runs first, on the host, before the GPU work starts.
+    cpu = None
+    if rank == 0 and ws == 1:
+        cpu = oracle_throughput(wl, args.cpu_seconds)
+
+    stream = torch.cuda.current_stream()
+    q, kp, vp, kn, vn = W.device_values(wl, "cuda")
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    ctx = torch.from_numpy(wl.context_lens).cuda()
+    slots = torch.from_numpy(wl.write_slots).cuda()
+    out = torch.empty_like(q)
+    shape = nsv.shape_of(q, kp, bt)
+    plan = nsv.plan_split(shape)
+    wsp = nsv.workspace_for(plan)
+    launches_per_step = 2 + (1 if plan.mode == nsv.MODE_SPLIT else 0)
+    small_l2 = wl.step_bytes() <= 4 * 129e6
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if small_l2 else None
+
+    def step(ev_a=None, ev_b=None):
+        if flush is not None:
+            flush.zero_()
+        nsv.kv_write(kn, vn, slots, kp, vp)
+        if ev_a is not None:
+            ev_a.record(stream)
+        nsv.paged_decode_ws(q, kp, vp, bt, ctx, wl.scale, out, workspace=wsp, plan=plan)
+        if ev_b is not None:
+            ev_b.record(stream)
+
+    nsv.device_status(clear=True)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st, _ = nsv.device_status(clear=True)
+    if st:
+        raise RuntimeError("device status %#x after warm-up" % st)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(local).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    sampler.start()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(K):
+        step(*ev[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    read_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # end to end through the C ABI from pinned host buffers
+    E = args.e2e_steps or min(K, 100)
+    h_q = q.cpu().pin_memory()
+    h_kn, h_vn = kn.cpu().pin_memory(), vn.cpu().pin_memory()
+    h_bt, h_ctx = bt.cpu().pin_memory(), ctx.cpu().pin_memory()
+    h_slots = slots.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_q, d_kn, d_vn = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+    d_bt, d_ctx, d_slots = torch.empty_like(bt), torch.empty_like(ctx), torch.empty_like(slots)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_bt, h_ctx, h_slots))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        if flush is not None:
+            flush.zero_()
+        for d, h in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_bt, h_bt), (d_ctx, h_ctx),
+                     (d_slots, h_slots)):
+            d.copy_(h, non_blocking=True)
+        nsv.decode_step(d_q, d_kn, d_vn, d_slots, kp, vp, d_bt, d_ctx, wl.scale, out,
+                        workspace=wsp, plan=plan)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / E
+    clocks = sampler.stop()
+    st, _ = nsv.device_status(clear=True)
+    if st:
+        raise RuntimeError("device status %#x after the timed steps" % st)
+
+    ms_step = total_ms / K
+    ms_read = float(np.mean(read_ms))
+    if ws > 1:
+        t = torch.tensor([ms_step, e2e_ms, ms_read], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, e2e_ms, ms_read = (float(x) for x in t.tolist())
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    step_bytes = wl.step_bytes()
+    value = step_bytes * ws / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = wl.read_bytes() / (ms_read * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
+        "pct_of_hbm_peak": 100.0 * value / ws / peak,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded N(0,1) values, seeded lengths and block permutation)",
+        "config": dict(workload_config(wl), plan=plan.as_dict()),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback",
+                     "kernel": "decode read (decode_kernel + combine_kernel)",
+                     "bytes_per_launch": wl.read_bytes(), "us_per_launch": ms_read * 1e3,
+                     "traffic": recorded_traffic()},
+        "e2e": {"value": step_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clocks,
+    }
+    if cpu is not None:
+        gbs, nrows, secs, threads = cpu
+        line["cpu_baseline"] = {
+            "value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d rows of %s, %.1f s of oracle time (fp64, full-width rectangle "
+                      "per row)" % (nrows, wl.rows, wl.name, secs)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    from paged_kv_decode_nsv_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]()
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_nsv(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -107,11 +107,15 @@ class Workload:
 
 
 def bf16_bits(x):
-    """fp32 -> bf16 bit patterns (uint16), round to nearest even."""
+    """fp32 -> bf16 bit patterns (uint16), round to nearest even (finite x)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return u.astype(np.uint16)
+    u = x.view(np.uint32)
+    r = u >> 16
+    r &= 1
+    r += 0x7FFF
+    r += u          # finite inputs stay below 2^32 - 2^16, so no wrap-around
+    r >>= 16
+    return r.astype(np.uint16)
 
 
 def bf16_to_f32(bits):

@@ -1,0 +1,151 @@
+"""The C-ABI library on the CPU: it loads, exports exactly what include/nsv.h
+declares, plans deterministically, and refuses bad host-visible arguments
+before touching any device (none of these calls needs a GPU)."""
+
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nsv.h")
+
+
+@pytest.fixture(scope="module")
+def nsv():
+    from paged_kv_decode_nsv_gb300 import build
+    build.build()
+    from paged_kv_decode_nsv_gb300 import nsv as mod
+    return mod
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"NSV_API\s+[\w\s\*]+?\b(nsv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("nsv_kv_write", "nsv_paged_decode", "nsv_plan_split"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(nsv):
+    lib = ctypes.CDLL(nsv.lib_path())
+    for name in declared_functions():
+        assert hasattr(lib, name), "libnsv.so does not export %s" % name
+
+
+def test_library_exports_nothing_else(nsv):
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", nsv.lib_path()], check=True,
+                         capture_output=True, text=True).stdout
+    funcs = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert funcs == set(declared_functions()), funcs ^ set(declared_functions())
+
+
+def test_abi_version_and_strerror(nsv):
+    assert nsv.abi_version() == 100
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8, -10):
+        assert nsv.strerror(code) and "unknown" not in nsv.strerror(code)
+    assert "unknown" in nsv.strerror(-99)
+
+
+def _shape(nsv, **kw):
+    d = dict(rows=256, num_heads=32, num_kv_heads=32, head_dim=128, max_blocks=512,
+             num_blocks=70000, dtype=nsv.BF16)
+    d.update(kw)
+    return nsv.make_shape(**d)
+
+
+def test_plan_headline_shape(nsv):
+    p = nsv.plan_split(_shape(nsv), num_sms=152)
+    assert p.mode == nsv.MODE_SPLIT
+    assert p.chunk_blocks == 32 and p.max_splits == 16
+    assert p.kv_heads_per_cta == 4 and p.threads == 5 * 32
+    assert p.grid == 152 * p.ctas_per_sm and p.ctas_per_sm == 2
+    assert p.smem_bytes <= 227 * 1024
+    n = 256 * 32 * 16
+    assert p.workspace_bytes == -(-n * 8 // 256) * 256 + n * 128 * 4
+    again = nsv.plan_split(_shape(nsv), num_sms=152)
+    assert bytes(again) == bytes(p), "planning must be deterministic"
+
+
+def test_plan_shapes_of_every_workload(nsv):
+    from paged_kv_decode_nsv_gb300 import workloads as W
+    for name, make in W.WORKLOADS.items():
+        wl = make()
+        shape = nsv.make_shape(wl.rows, wl.heads, wl.kv_heads, wl.head_dim, wl.max_blocks,
+                               wl.num_blocks, nsv.F32 if wl.dtype == "f32" else nsv.BF16)
+        p = nsv.plan_split(shape, num_sms=152)
+        assert 1 <= p.grid <= 152 * p.ctas_per_sm
+        assert p.smem_bytes <= 227 * 1024
+        assert (p.workspace_bytes == 0) == (p.mode == nsv.MODE_SINGLE)
+        assert p.max_splits == -(-wl.max_blocks // p.chunk_blocks)
+
+
+def test_plan_single_pass_when_chunk_covers_width(nsv):
+    p = nsv.plan_custom(_shape(nsv, max_blocks=64), num_sms=152, chunk_blocks=64)
+    assert p.mode == nsv.MODE_SINGLE and p.max_splits == 1 and p.workspace_bytes == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=96), -10), (dict(head_dim=256), -10), (dict(dtype=7), -2),
+    (dict(num_heads=30, num_kv_heads=8), -3), (dict(rows=-1), -3), (dict(rows=8193), -3),
+    (dict(max_blocks=0), -3), (dict(num_blocks=0), -3),
+    (dict(num_heads=64, num_kv_heads=2), -3),
+])
+def test_shape_refusals(nsv, kw, code):
+    with pytest.raises(nsv.NsvError) as e:
+        nsv.plan_split(_shape(nsv, **kw), num_sms=152)
+    assert e.value.code == code
+
+
+def test_block_size_refusal(nsv):
+    s = _shape(nsv)
+    s.block_size = 32
+    with pytest.raises(nsv.NsvError) as e:
+        nsv.plan_split(s, num_sms=152)
+    assert e.value.code == -10
+
+
+@pytest.mark.parametrize("kw", [dict(kv_heads_per_cta=3), dict(stages=1), dict(stages=9),
+                                dict(ctas_per_sm=5), dict(kv_heads_per_cta=32, stages=8)])
+def test_plan_custom_refusals(nsv, kw):
+    with pytest.raises(nsv.NsvError) as e:
+        nsv.plan_custom(_shape(nsv), num_sms=152, **kw)
+    assert e.value.code == -5
+
+
+def test_null_and_misaligned_pointers_refused_before_any_device_call(nsv):
+    lib = nsv._lib
+    s = _shape(nsv)
+    fake = ctypes.c_void_p(0x100000)
+    odd = ctypes.c_void_p(0x100008)
+    args = [fake, fake, fake, fake, fake]
+    rc = lib.nsv_paged_decode(ctypes.byref(s), None, *args[:4], 1.0, fake, None)
+    assert rc == -1
+    rc = lib.nsv_paged_decode(ctypes.byref(s), odd, fake, fake, fake, fake, 1.0, fake, None)
+    assert rc == -4
+    rc = lib.nsv_kv_write(ctypes.byref(s), fake, fake, ctypes.c_void_p(0x100004), fake, fake,
+                          None)
+    assert rc == -4
+    rc = lib.nsv_kv_write(None, fake, fake, fake, fake, fake, None)
+    assert rc == -1
+
+
+def test_tampered_plan_refused_before_any_device_call(nsv):
+    lib = nsv._lib
+    s = _shape(nsv)
+    p = nsv.plan_split(s, num_sms=152)
+    p.chunk_blocks = 7          # not what the planner made for these choices
+    p.max_splits = 99
+    fake = ctypes.c_void_p(0x100000)
+    rc = lib.nsv_paged_decode_ws(ctypes.byref(s), ctypes.byref(p), fake, fake, fake, fake, fake,
+                                 1.0, fake, fake, 1 << 30, None)
+    assert rc == -5
