@@ -256,7 +256,7 @@ def run_nsv(args, wl):
 
     # The oracle sample runs first, on the host, before the GPU work starts.
     cpu = None
-    if rank == 0 and ws == 1:
+    if rank == 0 and ws == 1 and args.cpu_seconds > 0:
         cpu = oracle_throughput(wl, args.cpu_seconds)
 
     stream = torch.cuda.current_stream()
