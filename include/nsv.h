@@ -211,6 +211,32 @@ NSV_API int nsv_decode_step(const nsv_shape *shape, const nsv_plan *plan, const 
                             size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Decode read that allocates nothing, for callers that cannot call
+ * cudaMalloc or hand the library scratch memory: engines that own all device
+ * memory through a fixed arena, plugin hooks that only receive pre-bound
+ * buffers, loops that must avoid the device-wide synchronisation an
+ * allocation can cause.  The nanoserve pages have no counterpart; this is a
+ * deployment convenience of this library.
+ *
+ * Same arguments, layouts and result as nsv_paged_decode (default plan).  The
+ * split path's scratch comes from a buffer of NSV_NOALLOC_SCRATCH_BYTES
+ * compiled into the library, which every GPU that loads the library holds
+ * until exit; a shape whose plan needs more (plan.workspace_bytes) is
+ * refused with NSV_ERR_WORKSPACE and nothing is launched.  The first call on
+ * a device looks up the buffer's device address (cudaGetSymbolAddress, no
+ * allocation); make that first call before any stream capture.  Calls share
+ * the buffer: two calls whose kernels overlap on the GPU race on it.  The
+ * buffer needs no clearing between calls.
+ */
+#define NSV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+NSV_API int nsv_paged_decode_noalloc(const nsv_shape *shape, const void *q,
+                                     const void *k_pool, const void *v_pool,
+                                     const int32_t *block_tables,
+                                     const int32_t *context_lens, float scale, void *out,
+                                     cudaStream_t stream);
+
+/*
  * Synchronise the current device, then report its status word (NSV_DEV_*
  * bits raised since the last clear) and the number of (row, block) pairs the
  * decode kernels walked (each row's cdiv(ctx, block_size) blocks, counted

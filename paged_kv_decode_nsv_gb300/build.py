@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libnsv.so")
-SOURCES = ["nsv_api.cu", "decode.cu", "kv_write.cu"]
+SOURCES = ["nsv_api.cu", "decode.cu", "kv_write.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -76,6 +76,8 @@ _lib.nsv_paged_decode_ws.argtypes = [_SP, _PP, _vp, _vp, _vp, _vp, _vp, _f, _vp,
 _lib.nsv_decode_step.restype = _i32
 _lib.nsv_decode_step.argtypes = [_SP, _PP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f, _vp,
                                  _vp, _sz, _vp]
+_lib.nsv_paged_decode_noalloc.restype = _i32
+_lib.nsv_paged_decode_noalloc.argtypes = [_SP, _vp, _vp, _vp, _vp, _vp, _f, _vp, _vp]
 _lib.nsv_device_status.restype = _i32
 _lib.nsv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32),
                                    ctypes.POINTER(ctypes.c_uint64), _i32]
@@ -191,6 +193,20 @@ def paged_decode(q, k_pool, v_pool, block_tables, context_lens, scale, out, stre
                                  _ptr(v_pool, "v_pool"), _ptr(block_tables, "block_tables"),
                                  _ptr(context_lens, "context_lens"), float(scale),
                                  _ptr(out, "out"), _stream(stream)), "nsv_paged_decode")
+    return out
+
+
+def paged_decode_noalloc(q, k_pool, v_pool, block_tables, context_lens, scale, out,
+                         stream=None):
+    """Decode read that allocates no device memory (scratch from the library's
+    fixed buffer; see nsv_paged_decode_noalloc in nsv.h for the size limit)."""
+    shape = shape_of(q, k_pool, block_tables)
+    _check(_lib.nsv_paged_decode_noalloc(ctypes.byref(shape), _ptr(q, "q"),
+                                         _ptr(k_pool, "k_pool"), _ptr(v_pool, "v_pool"),
+                                         _ptr(block_tables, "block_tables"),
+                                         _ptr(context_lens, "context_lens"), float(scale),
+                                         _ptr(out, "out"), _stream(stream)),
+           "nsv_paged_decode_noalloc")
     return out
 
 

@@ -1,0 +1,85 @@
+"""The allocation-free decode entry point, nsv_paged_decode_noalloc.
+
+Some callers may not allocate device memory at all: an engine that owns the
+whole device through its own arena, a plugin hook that only gets pre-bound
+buffers, a serving loop that cannot afford the device-wide synchronisation
+an allocation can bring.  This entry point serves them by taking the split
+path's scratch from a fixed buffer compiled into the library.  These tests
+call it through the C ABI and hold it to the existing entry point
+(nsv_paged_decode_ws with a caller-owned workspace) within the parity
+tolerance, on two calls in a row with different inputs, so that whatever the
+first call leaves in the shared buffer cannot leak into the second.
+
+The file is named to be collected last: a run that stops at its first
+failure has then already run every other test.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+from gpu_common import assert_parity, device_inputs, gpu_out_f64, gpu_read
+from paged_kv_decode_nsv_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_LIMIT = 16 << 20  # NSV_NOALLOC_SCRATCH_BYTES in include/nsv.h
+
+
+@pytest.fixture(scope="module")
+def nsv():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from paged_kv_decode_nsv_gb300 import nsv as mod
+    mod.device_status(clear=True)
+    return mod
+
+
+def _noalloc_call(nsv, wl, inp, out):
+    """One call of the new entry point through the C ABI (ctypes)."""
+    import torch
+    shape = nsv.shape_of(inp["q"], inp["k_pool"], inp["block_tables"])
+    rc = nsv._lib.nsv_paged_decode_noalloc(
+        ctypes.byref(shape), inp["q"].data_ptr(), inp["k_pool"].data_ptr(),
+        inp["v_pool"].data_ptr(), inp["block_tables"].data_ptr(),
+        inp["context_lens"].data_ptr(), ctypes.c_float(wl.scale), out.data_ptr(),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    return rc
+
+
+@pytest.mark.parametrize("make", [
+    W.uniform_f32,
+    lambda: W.custom("noalloc_bf16", 31, rows=10, heads=8, kv_heads=8, head_dim=128,
+                     block_size=16, max_blocks=66, dtype="bf16",
+                     lens=[1, 0, 17, 256, 1000, 333, 16, 15, 1024, 47], free_frac=0.2),
+], ids=["uniform_f32", "ragged_bf16_10rows"])
+def test_noalloc_matches_existing_entry_point_on_two_calls(nsv, make):
+    import torch
+    wl = make()
+    for value_seed in (501, 502):
+        inp = device_inputs(wl, value_seed=value_seed)
+        shape = nsv.shape_of(inp["q"], inp["k_pool"], inp["block_tables"])
+        plan = nsv.plan_split(shape)
+        assert plan.mode == nsv.MODE_SPLIT and 0 < plan.workspace_bytes <= SCRATCH_LIMIT, \
+            "the case must use scratch memory and fit the static buffer"
+        want = gpu_read(wl, inp, plan=plan)          # existing entry point
+        got = torch.full_like(inp["q"], float("nan"))
+        assert _noalloc_call(nsv, wl, inp, got) == 0
+        st, _ = nsv.device_status(clear=True)
+        assert st == 0
+        assert_parity(wl.dtype, gpu_out_f64(got), gpu_out_f64(want))
+
+
+def test_noalloc_refuses_shapes_beyond_its_buffer(nsv):
+    import torch
+    wl = W.headline_bf16()
+    shape = nsv.make_shape(wl.rows, wl.heads, wl.kv_heads, wl.head_dim, wl.max_blocks,
+                           wl.num_blocks, nsv.BF16)
+    assert nsv.plan_split(shape).workspace_bytes > SCRATCH_LIMIT
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: the call refuses first
+    rc = nsv._lib.nsv_paged_decode_noalloc(
+        ctypes.byref(shape), fake, fake, fake, fake, fake, ctypes.c_float(1.0), fake,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == -8, "a shape needing more scratch than the buffer must get NSV_ERR_WORKSPACE"
