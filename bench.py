@@ -69,6 +69,21 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, device="cpu"):
+    """Element-wise max of `values` over all ranks (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_gbs(bytes_per_step_per_rank, world, ms_per_step):
+    """Weak scaling: every rank moves its own batch; the slowest rank sets the time."""
+    return bytes_per_step_per_rank * world / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -166,7 +181,7 @@ def oracle_throughput(wl, budget_s, threads=0, seed=12345):
     import oracle
     from paged_kv_decode_nsv_gb300 import workloads as W
 
-    threads = threads or oracle.max_threads()
+    threads = threads or os.cpu_count() or oracle.max_threads()
     done, t_total, bytes_total, r0 = 0, 0.0, 0, 0
     per_call = max(1, threads)
     while t_total < budget_s and r0 < wl.rows:
@@ -174,7 +189,8 @@ def oracle_throughput(wl, budget_s, threads=0, seed=12345):
         key = (wl.name, rows, seed)
         if key not in _SAMPLE_CACHE:
             blocks, tables, _ = W.compact_rows(wl, rows)
-            shape = (len(blocks) + 1, wl.kv_heads, wl.block_size, wl.head_dim)
+            # at least one real block: a sample of empty rows still has a pool
+            shape = (max(len(blocks), 1) + 1, wl.kv_heads, wl.block_size, wl.head_dim)
             gen = torch.Generator().manual_seed(seed * 100003 + r0)
 
             def draw(s):
@@ -357,16 +373,14 @@ def run_nsv(args, wl):
 
     ms_step = total_ms / K
     ms_read = float(np.mean(read_ms))
+    ms_step, e2e_ms, ms_read = max_over_ranks([ms_step, e2e_ms, ms_read], device="cuda")
     if ws > 1:
-        t = torch.tensor([ms_step, e2e_ms, ms_read], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, e2e_ms, ms_read = (float(x) for x in t.tolist())
         dist.destroy_process_group()
     if rank != 0:
         return 0
 
     step_bytes = wl.step_bytes()
-    value = step_bytes * ws / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, ws, ms_step)
     peak, peak_kind = measured_peak()
     achieved = wl.read_bytes() / (ms_read * 1e-3) / 1e9
     line = {
@@ -382,7 +396,7 @@ def run_nsv(args, wl):
                      "kernel": "decode read (decode_kernel + combine_kernel)",
                      "bytes_per_launch": wl.read_bytes(), "us_per_launch": ms_read * 1e3,
                      "traffic": recorded_traffic()},
-        "e2e": {"value": step_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": whole_job_gbs(step_bytes, ws, e2e_ms), "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,

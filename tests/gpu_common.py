@@ -100,8 +100,9 @@ def oracle_step_sampled(wl, inp, rows, threads=0):
     rows = list(rows)
     blocks, tables, slots = W.compact_rows(wl, rows)
     idx = torch.from_numpy(blocks).cuda()
-    sink = torch.zeros((1,) + tuple(inp["k_pool"].shape[1:]), dtype=inp["k_pool"].dtype,
-                       device="cuda")
+    # the sink block (and a spare real block when every sampled row is empty)
+    sink = torch.zeros((1 if len(blocks) else 2,) + tuple(inp["k_pool"].shape[1:]),
+                       dtype=inp["k_pool"].dtype, device="cuda")
     kp = W.to_numpy(torch.cat([inp["k_pool"].index_select(0, idx), sink]))
     vp = W.to_numpy(torch.cat([inp["v_pool"].index_select(0, idx), sink]))
     ridx = torch.tensor(rows, dtype=torch.long, device="cuda")
