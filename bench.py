@@ -284,7 +284,7 @@ def run_nsv(args, wl):
     shape = nsv.shape_of(q, kp, bt)
     plan = nsv.plan_split(shape)
     wsp = nsv.workspace_for(plan)
-    launches_per_step = 2 + (1 if plan.mode == nsv.MODE_SPLIT else 0)
+    launches_per_step = 3  # kv_write, decode_kernel, combine_kernel
     small_l2 = wl.step_bytes() <= 4 * 129e6
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if small_l2 else None
 

@@ -83,7 +83,8 @@ enum {
     NSV_ERR_CAPTURE = -6,     /* the library workspace must grow while the
                                  stream is being captured */
     NSV_ERR_CUDA = -7,        /* a CUDA runtime call failed */
-    NSV_ERR_WORKSPACE = -8,   /* caller workspace smaller than the plan needs */
+    NSV_ERR_WORKSPACE = -8,   /* workspace missing, misaligned or smaller than
+                                 the plan needs */
     NSV_ERR_UNSUPPORTED = -10 /* head_dim or block_size the kernels lack */
 };
 
@@ -117,24 +118,22 @@ typedef struct nsv_shape {
 
 /* Launch plan of the decode read.  A plan depends on the shape and the SM
  * count only, never on the values of context_lens, so one plan serves every
- * step of a given shape (and a captured graph of it). */
-enum { NSV_MODE_SINGLE = 1, NSV_MODE_SPLIT = 2 };
-
+ * step of a given shape (and a captured graph of it).
+ *
+ * The read is split evenly over a persistent grid: the units (KV-head group,
+ * row, block) of all rows are laid end to end and CTA c of `grid` takes the
+ * units [c*U/grid, (c+1)*U/grid).  A row cut by CTA boundaries is finished by
+ * a second kernel that merges the partial softmax states of its pieces. */
 typedef struct nsv_plan {
-    int32_t mode;             /* NSV_MODE_SINGLE: one work item per (row, head
-                                 group); NSV_MODE_SPLIT: a row's blocks are cut
-                                 into chunks whose partial softmax states are
-                                 merged by a combine kernel */
-    int32_t chunk_blocks;     /* blocks per work item */
-    int32_t max_splits;       /* cdiv(max_blocks, chunk_blocks) */
-    int32_t kv_heads_per_cta; /* KV heads one CTA streams together */
+    int32_t kv_heads_per_cta; /* KV heads one CTA streams together (a head group) */
     int32_t stages;           /* shared-memory pipeline depth */
     int32_t ctas_per_sm;      /* resident CTAs per SM the grid is sized for */
     int32_t grid;             /* persistent CTAs launched */
     int32_t threads;          /* threads per CTA */
     int32_t smem_bytes;       /* dynamic shared memory per CTA */
     int32_t num_sms;          /* SM count the plan was made for */
-    int64_t workspace_bytes;  /* scratch the split path needs (0 for single) */
+    int32_t reserved;         /* 0 */
+    int64_t workspace_bytes;  /* device scratch the read needs */
 } nsv_plan;
 
 /*
@@ -147,15 +146,13 @@ NSV_API int nsv_plan_split(const nsv_shape *shape, int num_sms, nsv_plan *plan);
 
 /*
  * The same planner with some choices fixed (any argument <= 0 is chosen by
- * the heuristic): chunk_blocks (>= max_blocks gives the single-pass mode),
- * kv_heads_per_cta (must divide num_kv_heads), stages (2..8), ctas_per_sm
- * (1..4) and grid (persistent CTAs; default num_sms * ctas_per_sm, capped
- * by the number of work items).  Returns NSV_ERR_RANGE when a fixed choice
- * does not fit the shape or the shared-memory limit.
+ * the heuristic): kv_heads_per_cta (must divide num_kv_heads), stages (2..8),
+ * ctas_per_sm (1..4) and grid (persistent CTAs; default num_sms *
+ * ctas_per_sm).  Returns NSV_ERR_RANGE when a fixed choice does not fit the
+ * shape or the shared-memory limit.
  */
-NSV_API int nsv_plan_custom(const nsv_shape *shape, int num_sms, int chunk_blocks,
-                            int kv_heads_per_cta, int stages, int ctas_per_sm,
-                            int grid, nsv_plan *plan);
+NSV_API int nsv_plan_custom(const nsv_shape *shape, int num_sms, int kv_heads_per_cta,
+                            int stages, int ctas_per_sm, int grid, nsv_plan *plan);
 
 /*
  * KV append: for every row r, k_pool/v_pool at slot write_slots[r] receive
@@ -228,7 +225,7 @@ NSV_API int nsv_decode_step(const nsv_shape *shape, const nsv_plan *plan, const 
  * the buffer: two calls whose kernels overlap on the GPU race on it.  The
  * buffer needs no clearing between calls.
  */
-#define NSV_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define NSV_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 NSV_API int nsv_paged_decode_noalloc(const nsv_shape *shape, const void *q,
                                      const void *k_pool, const void *v_pool,

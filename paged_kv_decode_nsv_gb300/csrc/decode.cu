@@ -11,25 +11,28 @@
 // ("Why it matters", the masked-load paragraph).
 //
 // How it runs on GB300 (the design differs from the pages' (row, head) grid):
-//  * A persistent grid of CTAs (SM count x resident CTAs).  Work items are
-//    (row, split, head group): a head group is `heads_per_cta` KV heads with
-//    all their query heads, a split is `chunk_blocks` consecutive blocks of
-//    the row.  Every CTA builds the same compacted item list from
-//    context_lens in shared memory (no host read of the lengths, so the plan
-//    depends on shape alone) and takes items blockIdx.x, +gridDim.x, ...
+//  * A persistent grid of CTAs (SM count x resident CTAs).  The work is the
+//    sequence of units (head group, row, block) -- a head group is
+//    `heads_per_cta` KV heads with all their query heads -- laid end to end
+//    over every row's cdiv(ctx, block) blocks.  CTA c takes the units
+//    [c*U/G, (c+1)*U/G): every CTA streams the same number of blocks (stream-K
+//    style), whatever the length mix.  Every CTA derives the sequence from
+//    context_lens in shared memory, so the launch depends on shape alone.
 //  * Warp 0 is the producer.  Per block it issues two cp.async.bulk copies
 //    (the head group's K tiles and V tiles are each one contiguous run in the
 //    [block][kv_head][token][dim] pool) into a ring of shared-memory stages
-//    guarded by mbarriers, plus the query vectors on an item's first stage.
-//    Block ids of the next window are prefetched a window ahead.
+//    guarded by mbarriers, plus the query vectors at each segment's first
+//    stage.  The block ids of the next 32 units are loaded a window ahead.
 //  * Warps 1..N are consumers, one per query head.  A lane owns 16 bytes of
 //    a key row; the score of each token of the tile is reduced with a
 //    transposing butterfly (one shuffle per token instead of five), the
 //    tile max with a plain butterfly, probabilities go through shared memory
 //    to the lanes that own the value dims, and P.V accumulates in fp32.
-//  * An item that covers its row's whole length writes `out` directly;
-//    otherwise it writes its (m, l, acc) partial and a combine kernel merges
-//    the row's partials (flash-decoding style).
+//  * A segment (a CTA's run of one row) that covers the whole row writes
+//    `out` directly.  A row cut by CTA boundaries leaves one partial (m, l,
+//    acc) per CTA it crosses -- at most two per CTA -- and the combine kernel
+//    merges them (flash-decoding style); it also writes the zero output of
+//    empty rows.
 //  * No tensor cores: one query per head makes each tile a GEMV.
 // Every wait is bounded; a wait that gives up sets NSV_DEV_TIMEOUT and the
 // kernel returns.  Bad lengths and block ids are skipped and flagged.
@@ -177,39 +180,11 @@ __device__ __forceinline__ int checked_ctx(const DecodeParams& p, int r) {
   return c;
 }
 
-// Work items of a row: its splits (at least one, so an empty row still gets
-// an item that writes its zero output).
-__device__ __forceinline__ int row_splits(int ctx, int chunk_blocks) {
-  int nb = cdiv(ctx, kBlock);
-  int s = cdiv(nb, chunk_blocks);
-  return s > 0 ? s : 1;
-}
-
-struct Item {
-  int row, hg, split, ctx, b0, b1;  // blocks [b0, b1) of the row
-  bool final_;                      // the row has one split
-};
-
-__device__ __forceinline__ Item item_at(int it, int nhg, const int* s_prefix, const int* s_ctx,
-                                        int rows, int chunk_blocks) {
-  Item I;
-  const int rs = it / nhg;
-  I.hg = it - rs * nhg;
-  // largest row r with prefix[r] <= rs (prefix is strictly increasing)
-  int lo = 0, hi = rows - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (s_prefix[mid] <= rs) lo = mid; else hi = mid - 1;
-  }
-  I.row = lo;
-  I.split = rs - s_prefix[lo];
-  I.ctx = s_ctx[lo];
-  const int nb = cdiv(I.ctx, kBlock);
-  I.b0 = I.split * chunk_blocks;
-  I.b1 = min(nb, I.b0 + chunk_blocks);
-  if (I.b1 < I.b0) I.b1 = I.b0;
-  I.final_ = (s_prefix[lo + 1] - s_prefix[lo]) == 1;
-  return I;
+// CTA whose unit range [c*U/G, (c+1)*U/G) holds unit u (the last such c
+// when empty ranges share a start).
+__device__ __forceinline__ int cta_of(long long u, long long U, int G) {
+  long long c = ((u + 1) * G + U - 1) / U - 1;
+  return (int)(c < G - 1 ? c : G - 1);
 }
 
 template <typename T, int D>
@@ -247,14 +222,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
     *s_abort = 0;
     fence_mbar_init();
   }
-  // Row table: validated lengths and split counts (prefix computed below).
+  // Row table: validated lengths and block counts (prefix computed below).
   for (int r = tid; r < p.rows; r += blockDim.x) {
     const int c = checked_ctx(p, r);
     s_ctx[r] = c;
-    s_prefix[r + 1] = row_splits(c, p.chunk_blocks);
+    s_prefix[r + 1] = cdiv(c, kBlock);
   }
   __syncthreads();
-  if (warp == 0) {  // inclusive scan of split counts into prefix[1..rows]
+  if (warp == 0) {  // inclusive scan of block counts into prefix[1..rows]
     const int per = (p.rows + 31) / 32;
     const int lo = min(p.rows, lane * per), hi = min(p.rows, lo + per);
     int sum = 0;
@@ -273,9 +248,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
     if (lane == 0) s_prefix[0] = 0;
   }
   __syncthreads();
+  if (blockIdx.x == 0) {  // the combine kernel reads the same prefix
+    for (int r = tid; r <= p.rows; r += blockDim.x) p.ws_prefix[r] = s_prefix[r];
+  }
 
   const int nhg = p.kv_heads / HG;
-  const int total = s_prefix[p.rows] * nhg;
+  const int N = s_prefix[p.rows];                 // blocks per head group
+  const long long U = (long long)N * nhg;         // units
+  const long long beg = (long long)blockIdx.x * U / gridDim.x;
+  const long long end = ((long long)blockIdx.x + 1) * U / gridDim.x;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -285,20 +266,45 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
     const T* kp = static_cast<const T*>(p.k_pool);
     const T* vp = static_cast<const T*>(p.v_pool);
     const T* qp = static_cast<const T*>(p.q);
+    const int slot0 = blockIdx.x * 2;
     unsigned long long walked = 0;
     uint32_t n = 0;  // fills issued (meaningful in lane 0)
     bool ok = true;
 
+    // Unit u (this lane's): its row, its stage flags and its block id.
+    auto unit_at = [&](long long u, int& row, int& flags, int& phys) {
+      const int hg = (int)(u / N);
+      const int rb = (int)(u - (long long)hg * N);
+      int lo = 0, hi = p.rows - 1;  // last row r with prefix[r] <= rb
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_prefix[mid] <= rb) lo = mid; else hi = mid - 1;
+      }
+      const int j = rb - s_prefix[lo];
+      const int nb = s_prefix[lo + 1] - s_prefix[lo];
+      const long long rs = (long long)hg * N + s_prefix[lo];  // the row's first unit
+      int f = min(kBlock, s_ctx[lo] - j * kBlock) | ((hg * HG) << 16);
+      if (u == beg || j == 0) f |= kFirst | kHasQ;
+      if (u == end - 1 || j == nb - 1) f |= kLast;
+      if (rs >= beg && rs + nb <= end) f |= kFinal;
+      if (rs > beg) f |= kSlot1;
+      row = lo;
+      flags = f;
+      phys = p.block_tables[(size_t)lo * p.max_blocks + j];
+    };
+
     // Emit one stage (lane 0 only): wait for it to be free, write its
     // metadata, arm its barrier and start its copies.
-    auto emit = [&](int row, int qh0, int split, int flags, int phys) -> bool {
+    auto emit = [&](int row, int flags, int phys) -> bool {
       const uint32_t s = n % S;
       const uint32_t full = bars + 8 * s, empty = bars + 8 * (S + s);
       if (*s_abort) return false;  // a consumer gave up waiting
       if (n >= (uint32_t)S) {
         if (!mbar_wait(empty, ((n / S) - 1) & 1)) return false;
       }
-      s_meta[s] = make_int4(row, qh0, split, flags);
+      const int kv0 = flags >> 16;
+      const int qh0 = kv0 * G;
+      s_meta[s] = make_int4(row, qh0, slot0 + ((flags & kSlot1) ? 1 : 0), flags);
       uint32_t bytes = 0;
       if (flags & kData) bytes += 2 * L.kv_bytes;
       if (flags & kHasQ) bytes += L.q_bytes;
@@ -308,7 +314,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
         mbar_arrive_tx(full, bytes);
         const uint32_t base = smem_u32(smem + s * L.stage_bytes);
         if (flags & kData) {
-          const size_t off = (size_t)phys * block_elems + (size_t)(flags >> 16) * tile_elems;
+          const size_t off = (size_t)phys * block_elems + (size_t)kv0 * tile_elems;
           bulk_g2s(base, kp + off, L.kv_bytes, full, pol);
           bulk_g2s(base + L.kv_bytes, vp + off, L.kv_bytes, full, pol);
         }
@@ -321,62 +327,35 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
       return true;
     };
 
-    int it = blockIdx.x;
-    Item cur{};
-    int w0 = 0;
-    int cur_id = -1;
-    if (it < total) {
-      cur = item_at(it, nhg, s_prefix, s_ctx, p.rows, p.chunk_blocks);
-      w0 = cur.b0;
-      if (w0 + lane < cur.b1) cur_id = p.block_tables[(size_t)cur.row * p.max_blocks + w0 + lane];
-    }
-    while (it < total && ok) {
-      // Locate the next window (32 blocks) and prefetch its block ids.
-      int nit = it, nw0 = w0 + 32;
-      Item nxt = cur;
-      if (nw0 >= cur.b1) {
-        nit = it + gridDim.x;
-        if (nit < total) {
-          nxt = item_at(nit, nhg, s_prefix, s_ctx, p.rows, p.chunk_blocks);
-          nw0 = nxt.b0;
-        }
-      }
-      int nxt_id = -1;
-      if (nit < total && nw0 + lane < nxt.b1)
-        nxt_id = p.block_tables[(size_t)nxt.row * p.max_blocks + nw0 + lane];
-
-      const int qh0 = cur.hg * HG * G;
-      const int fin = cur.final_ ? kFinal : 0;
-      const int kv0 = cur.hg * HG;
-      const int nwin = min(32, cur.b1 - w0);
-      if (nwin <= 0) {
-        // An empty row: one stage with no data that makes its output zero.
-        if (lane == 0) ok = emit(cur.row, qh0, cur.split, kFirst | kLast | fin, 0);
-        ok = __shfl_sync(kFull, ok, 0);
-      }
+    long long w0 = beg;
+    int c_row = 0, c_flags = 0, c_phys = -1;
+    if (w0 + lane < end) unit_at(w0 + lane, c_row, c_flags, c_phys);
+    while (w0 < end && ok) {
+      // Prefetch the next window's units while this one is issued.
+      const long long nw0 = w0 + 32;
+      int n_row = 0, n_flags = 0, n_phys = -1;
+      if (nw0 + lane < end) unit_at(nw0 + lane, n_row, n_flags, n_phys);
+      const int nwin = (int)min(32ll, end - w0);
       for (int jj = 0; jj < nwin && ok; ++jj) {
-        const int phys = __shfl_sync(kFull, cur_id, jj);
-        const int j = w0 + jj;
-        const int nvalid = min(kBlock, cur.ctx - j * kBlock);
-        int flags = nvalid | fin | (kv0 << 16);
-        if (j == cur.b0) flags |= kFirst | kHasQ;
-        if (j == cur.b1 - 1) flags |= kLast;
+        const int row = __shfl_sync(kFull, c_row, jj);
+        int flags = __shfl_sync(kFull, c_flags, jj);
+        const int phys = __shfl_sync(kFull, c_phys, jj);
         if (phys >= 0 && (long long)phys < p.pool_blocks) {
           flags |= kData;
-          if (cur.hg == 0) ++walked;
+          if ((flags >> 16) == 0) ++walked;
         } else if (lane == 0) {
           atomicOr(p.status, (uint32_t)NSV_DEV_BAD_BLOCK);
         }
-        if (lane == 0) ok = emit(cur.row, qh0, cur.split, flags, phys);
+        if (lane == 0) ok = emit(row, flags, phys);
         ok = __shfl_sync(kFull, ok, 0);
       }
-      it = nit;
       w0 = nw0;
-      cur = nxt;
-      cur_id = nxt_id;
+      c_row = n_row;
+      c_flags = n_flags;
+      c_phys = n_phys;
     }
     if (lane == 0) {
-      if (ok) ok = emit(0, 0, 0, kEnd, 0);
+      if (ok) ok = emit(0, kEnd, 0);
       if (!ok) {
         atomicOr(p.status, (uint32_t)NSV_DEV_TIMEOUT);
         *s_abort = 1;
@@ -510,7 +489,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
 #pragma unroll
         for (int e = 0; e < kDpl; ++e) at[e] += __shfl_xor_sync(kFull, at[e], o);
       }
-      const int row = meta.x, qh = meta.y + cw, split = meta.z;
+      const int row = meta.x, qh = meta.y + cw;
       if (flags & kFinal) {
         if (lane < kLpt) {
           const float inv = lt > 0.f ? 1.f / lt : 0.f;
@@ -520,7 +499,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
           *reinterpret_cast<uint4*>(o) = E::narrow(at);
         }
       } else {
-        const size_t slot = ((size_t)row * p.heads + qh) * p.max_splits + split;
+        const size_t slot = (size_t)meta.z * ncw + cw;
         if (lane < kLpt) {
           float* a = p.ws_acc + slot * D + sub * kDpl;
 #pragma unroll
@@ -535,39 +514,79 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
   }
 }
 
-// Merge the partial softmax states of rows that were split.  One warp per
-// (row, query head); rows with a single split were finished by the decode
-// kernel and are skipped.
+// Finish every row the decode kernel did not: merge the partial softmax
+// states of rows cut by CTA boundaries, and write zeros for empty rows.  One
+// warp per (row, query head).  The partials' (m, l) are loaded by all lanes
+// at once (one partial per lane); the acc slices are then summed with the
+// weights broadcast from the lane that loaded them.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
   constexpr int kPer = D / 32;  // dims per lane
   const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= p.rows * p.heads) return;
-  const int row = gw / p.heads;
-  int c = p.context_lens[row];
-  if (c < 0 || c > p.max_blocks * kBlock) c = 0;  // flagged by the decode kernel
-  const int nsplit = cdiv(cdiv(c, kBlock), p.chunk_blocks);
-  if (nsplit <= 1) return;
-  const size_t base = (size_t)gw * p.max_splits;
-  float M = -INFINITY;
-  for (int i = lane; i < nsplit; i += 32) M = fmaxf(M, p.ws_ml[base + i].x);
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-  float Lsum = 0.f;
+  const int row = gw / p.heads, qh = gw - row * p.heads;
+  const int N = p.ws_prefix[p.rows];
+  const int pr = p.ws_prefix[row];
+  const int nb = p.ws_prefix[row + 1] - pr;
+  T* o = static_cast<T*>(p.out) + (size_t)gw * D + lane * kPer;
   float a[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) a[e] = 0.f;
-  for (int i = 0; i < nsplit; ++i) {
-    const float2 ml = p.ws_ml[base + i];
-    const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-    Lsum = fmaf(w, ml.y, Lsum);
-    const float* src = p.ws_acc + (base + i) * D + lane * kPer;
+  float inv = 0.f;
+  if (nb > 0) {
+    const int nhg = p.kv_heads / p.heads_per_cta;
+    const int ncw = p.heads_per_cta * p.group;
+    const long long U = (long long)N * nhg;
+    const int hg = (qh / p.group) / p.heads_per_cta;
+    const int cw = qh - hg * ncw;
+    const long long u0 = (long long)hg * N + pr, u1 = u0 + nb;
+    const int c0 = cta_of(u0, U, p.grid), c1 = cta_of(u1 - 1, U, p.grid);
+    if (c0 == c1) return;  // one CTA held the whole row and wrote it
+    const int ns = c1 - c0 + 1;
+    // pass 1: the running max over all partials
+    float M = -INFINITY;
+    for (int k = lane; k < ns; k += 32) {
+      const int c = c0 + k;
+      const long long sc = (long long)c * U / p.grid;
+      if ((long long)(c + 1) * U / p.grid == sc) continue;  // CTA with no units
+      const int slot = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
+      M = fmaxf(M, p.ws_ml[(size_t)slot * ncw + cw].x);
+    }
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) a[e] = fmaf(w, src[e], a[e]);
+    for (int o2 = 16; o2 >= 1; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
+    // pass 2: weights per partial (one per lane), then the weighted sums
+    float Lsum = 0.f;
+    for (int base = 0; base < ns; base += 32) {
+      const int c = c0 + base + lane;
+      float w = 0.f;
+      int idx = 0;
+      if (base + lane < ns) {
+        const long long sc = (long long)c * U / p.grid;
+        if ((long long)(c + 1) * U / p.grid != sc) {
+          const int slot = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
+          idx = slot * ncw + cw;
+          const float2 ml = p.ws_ml[idx];
+          w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+          Lsum = fmaf(w, ml.y, Lsum);
+        }
+      }
+      const int cnt = min(32, ns - base);
+#pragma unroll 4
+      for (int k = 0; k < cnt; ++k) {
+        const float wk = __shfl_sync(kFull, w, k);
+        const int ik = __shfl_sync(kFull, idx, k);
+        if (wk != 0.f) {
+          const float* src = p.ws_acc + (size_t)ik * D + lane * kPer;
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) a[e] = fmaf(wk, src[e], a[e]);
+        }
+      }
+    }
+#pragma unroll
+    for (int o2 = 16; o2 >= 1; o2 >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, o2);
+    inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
   }
-  const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-  T* o = static_cast<T*>(p.out) + (size_t)gw * D + lane * kPer;
 #pragma unroll
   for (int e = 0; e < kPer; ++e) {
     if constexpr (sizeof(T) == 4) {

@@ -85,7 +85,7 @@ int check_shape(const nsv_shape* s) {
 
 int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int make_plan(const nsv_shape* s, int num_sms, int chunk, int hg, int stages, int cps, int grid,
+int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int grid,
               nsv_plan* p) {
   int rc = check_shape(s);
   if (rc) return rc;
@@ -99,12 +99,12 @@ int make_plan(const nsv_shape* s, int num_sms, int chunk, int hg, int stages, in
   const int G = s->num_heads / s->num_kv_heads;
   const int tile = kBlock * s->head_dim * elem;
   if (hg <= 0) {
-    // Largest KV-head group whose K+V stage stays within 32 KiB and whose
-    // query heads fill at most 8 consumer warps.
+    // Largest KV-head group whose K+V stage stays within 64 KiB and whose
+    // query heads fill at most 8 consumer warps: big bulk copies, few CTAs.
     hg = 1;
     const int cands[4] = {8, 4, 2, 1};
     for (int c : cands) {
-      if (s->num_kv_heads % c == 0 && c * G <= 8 && 2 * c * tile <= 32 * 1024) {
+      if (s->num_kv_heads % c == 0 && c * G <= 8 && 2 * c * tile <= 64 * 1024) {
         hg = c;
         break;
       }
@@ -132,45 +132,13 @@ int make_plan(const nsv_shape* s, int num_sms, int chunk, int hg, int stages, in
   } else if (cps > 4 || cps > fit || cps > fit_threads) {
     return NSV_ERR_RANGE;
   }
-  const int64_t slots = (int64_t)num_sms * cps;
-  const int64_t units = (int64_t)s->rows * (s->num_kv_heads / hg);
-  if (chunk <= 0) {
-    // Longest chunk (in blocks) that still gives the grid >= 32 items per
-    // CTA if every row were full width; short chunks bound the tail.
-    chunk = 8;
-    const int cands[3] = {32, 16, 8};
-    for (int c : cands) {
-      if (units * cdiv64(s->max_blocks, c) >= 32 * slots) {
-        chunk = c;
-        break;
-      }
-    }
-  }
-  int mode, splits;
-  if (chunk >= s->max_blocks) {
-    mode = NSV_MODE_SINGLE;
-    chunk = s->max_blocks;
-    splits = 1;
-  } else {
-    mode = NSV_MODE_SPLIT;
-    splits = (int)cdiv64(s->max_blocks, chunk);
-  }
-  const int64_t items = units * splits;
   if (grid <= 0) {
-    int64_t g = slots < items ? slots : items;
-    grid = (int)(g > 0 ? g : 1);
-  } else if (grid > (1 << 20)) {
+    grid = num_sms * cps;
+  } else if (grid > (1 << 16)) {
     return NSV_ERR_RANGE;
   }
-  int64_t ws = 0;
-  if (splits > 1) {
-    const int64_t n = (int64_t)s->rows * s->num_heads * splits;
-    ws = cdiv64(n * 8, 256) * 256 + n * s->head_dim * 4;
-  }
+  const WsLayout W = make_ws_layout(rows_for_layout, grid, hg * G, s->head_dim);
   memset(p, 0, sizeof(*p));
-  p->mode = mode;
-  p->chunk_blocks = chunk;
-  p->max_splits = splits;
   p->kv_heads_per_cta = hg;
   p->stages = stages;
   p->ctas_per_sm = cps;
@@ -178,14 +146,14 @@ int make_plan(const nsv_shape* s, int num_sms, int chunk, int hg, int stages, in
   p->threads = threads;
   p->smem_bytes = (int)L.total;
   p->num_sms = num_sms;
-  p->workspace_bytes = ws;
+  p->workspace_bytes = (int64_t)W.total;
   return NSV_OK;
 }
 
 // A caller's plan must be exactly what the planner makes from its choices.
 int check_plan(const nsv_shape* s, const nsv_plan* given, nsv_plan* use) {
-  int rc = make_plan(s, given->num_sms, given->chunk_blocks, given->kv_heads_per_cta,
-                     given->stages, given->ctas_per_sm, given->grid, use);
+  int rc = make_plan(s, given->num_sms, given->kv_heads_per_cta, given->stages,
+                     given->ctas_per_sm, given->grid, use);
   if (rc) return rc;
   if (memcmp(use, given, sizeof(nsv_plan)) != 0) return NSV_ERR_RANGE;
   return NSV_OK;
@@ -209,10 +177,10 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   DeviceState* d = nullptr;
   if ((rc = device_state(&d)) != NSV_OK) return rc;
   if (!plan_in) {
-    if ((rc = make_plan(s, d->num_sms, 0, 0, 0, 0, 0, &plan)) != NSV_OK) return rc;
+    if ((rc = make_plan(s, d->num_sms, 0, 0, 0, 0, &plan)) != NSV_OK) return rc;
   }
   if (s->rows == 0) return NSV_OK;
-  if (library_ws && plan.workspace_bytes > 0) {
+  if (library_ws) {
     std::lock_guard<std::mutex> lk(g_mu);
     if ((size_t)plan.workspace_bytes > d->ws_bytes) {
       cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -229,12 +197,13 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
     ws = d->ws;
     ws_bytes = d->ws_bytes;
   }
-  if (plan.workspace_bytes > 0) {
-    if (!ws || ws_bytes < (size_t)plan.workspace_bytes ||
-        (reinterpret_cast<uintptr_t>(ws) & 255u))
-      return NSV_ERR_WORKSPACE;
-  }
-  const int64_t nslots = (int64_t)s->rows * s->num_heads * plan.max_splits;
+  if (!ws || ws_bytes < (size_t)plan.workspace_bytes ||
+      (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return NSV_ERR_WORKSPACE;
+  const WsLayout W = make_ws_layout(s->rows, plan.grid,
+                                    plan.kv_heads_per_cta * (s->num_heads / s->num_kv_heads),
+                                    s->head_dim);
+  char* wsb = static_cast<char*>(ws);
   DecodeParams p;
   p.q = q;
   p.k_pool = k_pool;
@@ -242,10 +211,9 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   p.block_tables = block_tables;
   p.context_lens = context_lens;
   p.out = out;
-  p.ws_ml = plan.workspace_bytes ? static_cast<float2*>(ws) : nullptr;
-  p.ws_acc = plan.workspace_bytes
-                 ? reinterpret_cast<float*>(static_cast<char*>(ws) + cdiv64(nslots * 8, 256) * 256)
-                 : nullptr;
+  p.ws_prefix = reinterpret_cast<int32_t*>(wsb);
+  p.ws_ml = reinterpret_cast<float2*>(wsb + W.off_ml);
+  p.ws_acc = reinterpret_cast<float*>(wsb + W.off_acc);
   p.status = d->status;
   p.walked = d->walked;
   p.pool_blocks = s->num_blocks + 1;
@@ -253,8 +221,6 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   p.heads = s->num_heads;
   p.kv_heads = s->num_kv_heads;
   p.max_blocks = s->max_blocks;
-  p.chunk_blocks = plan.chunk_blocks;
-  p.max_splits = plan.max_splits;
   p.heads_per_cta = plan.kv_heads_per_cta;
   p.group = s->num_heads / s->num_kv_heads;
   p.stages = plan.stages;
@@ -262,19 +228,18 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   if (launch_decode(p, s->dtype, s->head_dim, plan.grid, plan.threads, plan.smem_bytes, stream) !=
       cudaSuccess)
     return cuda_fail();
-  if (plan.mode == NSV_MODE_SPLIT) {
-    CombineParams c;
-    c.context_lens = context_lens;
-    c.ws_ml = p.ws_ml;
-    c.ws_acc = p.ws_acc;
-    c.out = out;
-    c.rows = s->rows;
-    c.heads = s->num_heads;
-    c.max_blocks = s->max_blocks;
-    c.chunk_blocks = plan.chunk_blocks;
-    c.max_splits = plan.max_splits;
-    if (launch_combine(c, s->dtype, s->head_dim, stream) != cudaSuccess) return cuda_fail();
-  }
+  CombineParams c;
+  c.ws_prefix = p.ws_prefix;
+  c.ws_ml = p.ws_ml;
+  c.ws_acc = p.ws_acc;
+  c.out = out;
+  c.rows = s->rows;
+  c.heads = s->num_heads;
+  c.group = p.group;
+  c.heads_per_cta = plan.kv_heads_per_cta;
+  c.kv_heads = s->num_kv_heads;
+  c.grid = plan.grid;
+  if (launch_combine(c, s->dtype, s->head_dim, stream) != cudaSuccess) return cuda_fail();
   return NSV_OK;
 }
 
@@ -304,14 +269,12 @@ NSV_API const char* nsv_strerror(int code) {
 }
 
 NSV_API int nsv_plan_split(const nsv_shape* shape, int num_sms, nsv_plan* plan) {
-  return make_plan(shape, num_sms, 0, 0, 0, 0, 0, plan);
+  return make_plan(shape, num_sms, 0, 0, 0, 0, plan);
 }
 
-NSV_API int nsv_plan_custom(const nsv_shape* shape, int num_sms, int chunk_blocks,
-                            int kv_heads_per_cta, int stages, int ctas_per_sm, int grid,
-                            nsv_plan* plan) {
-  return make_plan(shape, num_sms, chunk_blocks, kv_heads_per_cta, stages, ctas_per_sm, grid,
-                   plan);
+NSV_API int nsv_plan_custom(const nsv_shape* shape, int num_sms, int kv_heads_per_cta,
+                            int stages, int ctas_per_sm, int grid, nsv_plan* plan) {
+  return make_plan(shape, num_sms, kv_heads_per_cta, stages, ctas_per_sm, grid, plan);
 }
 
 NSV_API int nsv_kv_write(const nsv_shape* s, const void* k_new, const void* v_new,

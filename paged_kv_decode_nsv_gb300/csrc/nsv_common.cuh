@@ -20,15 +20,35 @@ constexpr int kMaxRows = 8192;
 
 // Stage flags written by the producer warp for the consumers.  The low 8
 // bits of a stage's flag word carry the number of valid tokens of its block
-// and bits 16 and up the first KV head of the CTA's head group.
+// and bits 16 and up the first KV head of the head group.
 enum : int {
-  kFirst = 1 << 8,   // first block of a work item: reset the softmax state
-  kLast = 1 << 9,    // last block of a work item: write out or the partial
-  kFinal = 1 << 10,  // the item is the row's only split: write `out`
+  kFirst = 1 << 8,   // first block of a segment: reset the softmax state
+  kLast = 1 << 9,    // last block of a segment: write out or the partial
+  kFinal = 1 << 10,  // the segment is the whole row: write `out`
   kData = 1 << 11,   // the stage holds a K and a V tile
-  kHasQ = 1 << 12,   // the stage holds the CTA's query vectors
+  kHasQ = 1 << 12,   // the stage holds the group's query vectors
   kEnd = 1 << 13,    // no more work: consumers exit
+  kSlot1 = 1 << 14,  // a partial segment that is not the CTA's first one
 };
+
+// Workspace of one decode read (all offsets 256-byte aligned):
+//   prefix  int32 [rows + 1]   blocks before each row (written by CTA 0)
+//   ml      float2 [grid][2][cw]  (running max, denominator) of partials
+//   acc     float [grid][2][cw][head_dim]
+// where cw = query heads per CTA.  Each CTA has at most two partial
+// segments: the row its range starts inside of and the row it ends inside of.
+struct WsLayout {
+  uint64_t off_ml, off_acc, total;
+};
+
+__host__ __device__ inline WsLayout make_ws_layout(int rows, int grid, int cw, int head_dim) {
+  WsLayout W;
+  const uint64_t slots = (uint64_t)grid * 2 * cw;
+  W.off_ml = ((uint64_t)(rows + 1) * 4 + 255) / 256 * 256;
+  W.off_acc = W.off_ml + (slots * 8 + 255) / 256 * 256;
+  W.total = W.off_acc + slots * head_dim * 4;
+  return W;
+}
 
 struct DecodeParams {
   const void* q;
@@ -37,13 +57,13 @@ struct DecodeParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   void* out;
-  float2* ws_ml;     // [rows][heads][max_splits] (running max, denominator)
-  float* ws_acc;     // [rows][heads][max_splits][head_dim]
-  uint32_t* status;  // device status word
+  int32_t* ws_prefix;  // workspace prefix (rows + 1)
+  float2* ws_ml;       // workspace partial (m, l)
+  float* ws_acc;       // workspace partial acc
+  uint32_t* status;    // device status word
   unsigned long long* walked;  // (row, block) pairs walked
   long long pool_blocks;       // num_blocks + 1
   int rows, heads, kv_heads, max_blocks;
-  int chunk_blocks, max_splits;
   int heads_per_cta;  // KV heads per CTA
   int group;          // query heads per KV head
   int stages;
@@ -51,11 +71,11 @@ struct DecodeParams {
 };
 
 struct CombineParams {
-  const int32_t* context_lens;
+  const int32_t* ws_prefix;
   const float2* ws_ml;
   const float* ws_acc;
   void* out;
-  int rows, heads, max_blocks, chunk_blocks, max_splits;
+  int rows, heads, group, heads_per_cta, kv_heads, grid;
 };
 
 struct KvWriteParams {

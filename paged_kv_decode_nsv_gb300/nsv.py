@@ -29,7 +29,6 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 F32, BF16 = 0, 1
-MODE_SINGLE, MODE_SPLIT = 1, 2
 DEV_BAD_CTX, DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_TIMEOUT = 1, 2, 4, 8
 ERRORS = {0: "NSV_OK", -1: "NSV_ERR_NULLPTR", -2: "NSV_ERR_DTYPE", -3: "NSV_ERR_SHAPE",
           -4: "NSV_ERR_ALIGN", -5: "NSV_ERR_RANGE", -6: "NSV_ERR_CAPTURE", -7: "NSV_ERR_CUDA",
@@ -45,11 +44,10 @@ class Shape(ctypes.Structure):
 
 
 class Plan(ctypes.Structure):
-    _fields_ = [("mode", ctypes.c_int32), ("chunk_blocks", ctypes.c_int32),
-                ("max_splits", ctypes.c_int32), ("kv_heads_per_cta", ctypes.c_int32),
-                ("stages", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
-                ("grid", ctypes.c_int32), ("threads", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_int32), ("num_sms", ctypes.c_int32),
+    _fields_ = [("kv_heads_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("ctas_per_sm", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self):
@@ -66,7 +64,7 @@ _lib.nsv_strerror.argtypes = [_i32]
 _lib.nsv_plan_split.restype = _i32
 _lib.nsv_plan_split.argtypes = [_SP, _i32, _PP]
 _lib.nsv_plan_custom.restype = _i32
-_lib.nsv_plan_custom.argtypes = [_SP, _i32, _i32, _i32, _i32, _i32, _i32, _PP]
+_lib.nsv_plan_custom.argtypes = [_SP, _i32, _i32, _i32, _i32, _i32, _PP]
 _lib.nsv_kv_write.restype = _i32
 _lib.nsv_kv_write.argtypes = [_SP, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.nsv_paged_decode.restype = _i32
@@ -158,12 +156,11 @@ def plan_split(shape, num_sms=0):
     return p
 
 
-def plan_custom(shape, num_sms=0, chunk_blocks=0, kv_heads_per_cta=0, stages=0,
-                ctas_per_sm=0, grid=0):
+def plan_custom(shape, num_sms=0, kv_heads_per_cta=0, stages=0, ctas_per_sm=0, grid=0):
     p = Plan()
-    _check(_lib.nsv_plan_custom(ctypes.byref(shape), int(num_sms), int(chunk_blocks),
-                                int(kv_heads_per_cta), int(stages), int(ctas_per_sm),
-                                int(grid), ctypes.byref(p)), "nsv_plan_custom")
+    _check(_lib.nsv_plan_custom(ctypes.byref(shape), int(num_sms), int(kv_heads_per_cta),
+                                int(stages), int(ctas_per_sm), int(grid), ctypes.byref(p)),
+           "nsv_plan_custom")
     return p
 
 

@@ -65,13 +65,12 @@ def _shape(nsv, **kw):
 
 def test_plan_headline_shape(nsv):
     p = nsv.plan_split(_shape(nsv), num_sms=152)
-    assert p.mode == nsv.MODE_SPLIT
-    assert p.chunk_blocks == 32 and p.max_splits == 16
-    assert p.kv_heads_per_cta == 4 and p.threads == 5 * 32
-    assert p.grid == 152 * p.ctas_per_sm and p.ctas_per_sm == 2
+    assert p.kv_heads_per_cta == 8 and p.threads == 9 * 32
+    assert p.stages == 3 and p.ctas_per_sm == 1 and p.grid == 152
     assert p.smem_bytes <= 227 * 1024
-    n = 256 * 32 * 16
-    assert p.workspace_bytes == -(-n * 8 // 256) * 256 + n * 128 * 4
+    slots = 152 * 2 * 8
+    want = -(-257 * 4 // 256) * 256 + -(-slots * 8 // 256) * 256 + slots * 128 * 4
+    assert p.workspace_bytes == want
     again = nsv.plan_split(_shape(nsv), num_sms=152)
     assert bytes(again) == bytes(p), "planning must be deterministic"
 
@@ -83,15 +82,17 @@ def test_plan_shapes_of_every_workload(nsv):
         shape = nsv.make_shape(wl.rows, wl.heads, wl.kv_heads, wl.head_dim, wl.max_blocks,
                                wl.num_blocks, nsv.F32 if wl.dtype == "f32" else nsv.BF16)
         p = nsv.plan_split(shape, num_sms=152)
-        assert 1 <= p.grid <= 152 * p.ctas_per_sm
+        assert p.grid == 152 * p.ctas_per_sm
         assert p.smem_bytes <= 227 * 1024
-        assert (p.workspace_bytes == 0) == (p.mode == nsv.MODE_SINGLE)
-        assert p.max_splits == -(-wl.max_blocks // p.chunk_blocks)
+        assert 0 < p.workspace_bytes < (4 << 20)
+        assert wl.kv_heads % p.kv_heads_per_cta == 0
 
 
-def test_plan_single_pass_when_chunk_covers_width(nsv):
-    p = nsv.plan_custom(_shape(nsv, max_blocks=64), num_sms=152, chunk_blocks=64)
-    assert p.mode == nsv.MODE_SINGLE and p.max_splits == 1 and p.workspace_bytes == 0
+def test_plan_custom_choices(nsv):
+    p = nsv.plan_custom(_shape(nsv), num_sms=152, kv_heads_per_cta=2, stages=5,
+                        ctas_per_sm=2, grid=77)
+    assert (p.kv_heads_per_cta, p.stages, p.ctas_per_sm, p.grid) == (2, 5, 2, 77)
+    assert p.threads == 3 * 32
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -115,7 +116,8 @@ def test_block_size_refusal(nsv):
 
 
 @pytest.mark.parametrize("kw", [dict(kv_heads_per_cta=3), dict(stages=1), dict(stages=9),
-                                dict(ctas_per_sm=5), dict(kv_heads_per_cta=32, stages=8)])
+                                dict(ctas_per_sm=5), dict(kv_heads_per_cta=32, stages=8),
+                                dict(kv_heads_per_cta=8, stages=4), dict(grid=70000)])
 def test_plan_custom_refusals(nsv, kw):
     with pytest.raises(nsv.NsvError) as e:
         nsv.plan_custom(_shape(nsv), num_sms=152, **kw)
@@ -143,8 +145,7 @@ def test_tampered_plan_refused_before_any_device_call(nsv):
     lib = nsv._lib
     s = _shape(nsv)
     p = nsv.plan_split(s, num_sms=152)
-    p.chunk_blocks = 7          # not what the planner made for these choices
-    p.max_splits = 99
+    p.smem_bytes += 16          # not what the planner made for these choices
     fake = ctypes.c_void_p(0x100000)
     rc = lib.nsv_paged_decode_ws(ctypes.byref(s), ctypes.byref(p), fake, fake, fake, fake, fake,
                                  1.0, fake, fake, 1 << 30, None)

@@ -86,10 +86,12 @@ def test_library_workspace_refuses_to_grow_under_capture():
     import ctypes
     import torch
     from paged_kv_decode_nsv_gb300 import nsv
-    rows, heads, head_dim, max_blocks = 512, 32, 128, 1024   # a plan bigger than any earlier one
+    # 16 query heads per KV head: the largest default workspace of any shape
+    # the other tests use, so the library's buffer must grow here
+    rows, heads, kv_heads, head_dim, max_blocks = 512, 128, 8, 128, 1024
     q = torch.zeros((rows, heads, head_dim), dtype=torch.bfloat16, device="cuda")
     out = torch.zeros_like(q)
-    pool = torch.zeros((2, heads, 16, head_dim), dtype=torch.bfloat16, device="cuda")
+    pool = torch.zeros((2, kv_heads, 16, head_dim), dtype=torch.bfloat16, device="cuda")
     tables = torch.full((rows, max_blocks), -1, dtype=torch.int32, device="cuda")
     ctx = torch.zeros((rows,), dtype=torch.int32, device="cuda")
     shape = nsv.shape_of(q, pool, tables)

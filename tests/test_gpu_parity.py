@@ -103,7 +103,6 @@ def test_headline_sampled_in_bench_configuration(nsv):
                    *map(int, rng.choice(wl.rows, 4, replace=False))})
     ref = oracle_step_sampled(wl, inp, rows)
     plan = default_plan(inp)
-    assert plan.mode == nsv.MODE_SPLIT
     out = gpu_step(wl, inp, plan=plan)
     st, walked = status()
     assert st == 0
@@ -119,17 +118,16 @@ MEDIUM_LENS = [1, 0, 17, 256, 1000, 333, 16, 15, 1024, 47]
 
 
 @pytest.mark.parametrize("kw", [
-    dict(chunk_blocks=1000),                 # single pass
-    dict(chunk_blocks=1),
-    dict(chunk_blocks=3),
-    dict(chunk_blocks=40),                   # items longer than one 32-block window
-    dict(chunk_blocks=8, stages=2),
-    dict(chunk_blocks=8, stages=6),
-    dict(chunk_blocks=4, grid=1),            # one CTA walks every item
-    dict(chunk_blocks=4, grid=3),
-    dict(chunk_blocks=16, kv_heads_per_cta=1),
-    dict(chunk_blocks=16, kv_heads_per_cta=2, ctas_per_sm=1),
-    dict(chunk_blocks=1000, kv_heads_per_cta=4),
+    dict(),
+    dict(grid=1),                            # one CTA walks every unit
+    dict(grid=3),
+    dict(grid=7, stages=2),
+    dict(grid=5000),                         # more CTAs than units: empty ranges
+    dict(stages=2),
+    dict(stages=6, kv_heads_per_cta=2),
+    dict(kv_heads_per_cta=1),
+    dict(kv_heads_per_cta=2, ctas_per_sm=2),
+    dict(kv_heads_per_cta=4, ctas_per_sm=1, grid=100),
 ])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_plan_variants(nsv, kw, dtype):
@@ -263,7 +261,7 @@ def test_walk_count_matches_host_accounting(nsv):
     wl = W.WORKLOADS["ragged_bf16"]()
     inp = device_inputs(wl)
     status()
-    for kw in (dict(chunk_blocks=1000), dict(chunk_blocks=5), dict(chunk_blocks=8, grid=7)):
+    for kw in (dict(), dict(grid=5), dict(grid=999, kv_heads_per_cta=1)):
         shape = nsv.shape_of(inp["q"], inp["k_pool"], inp["block_tables"])
         gpu_read(wl, inp, plan=nsv.plan_custom(shape, **kw))
         st, walked = status()
@@ -316,8 +314,8 @@ def test_host_side_refusals(nsv):
     inp = device_inputs(wl)
     out = torch.empty_like(inp["q"])
     shape = nsv.shape_of(inp["q"], inp["k_pool"], inp["block_tables"])
-    plan = nsv.plan_custom(shape, chunk_blocks=2)
-    assert plan.workspace_bytes > 0
+    plan = nsv.plan_custom(shape, grid=40)
+    assert plan.workspace_bytes > 256
     with pytest.raises(nsv.NsvError) as e:
         nsv.paged_decode_ws(inp["q"], inp["k_pool"], inp["v_pool"], inp["block_tables"],
                             inp["context_lens"], wl.scale, out, workspace=None, plan=plan)

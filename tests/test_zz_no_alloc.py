@@ -24,7 +24,7 @@ from paged_kv_decode_nsv_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-SCRATCH_LIMIT = 16 << 20  # NSV_NOALLOC_SCRATCH_BYTES in include/nsv.h
+SCRATCH_LIMIT = 4 << 20  # NSV_NOALLOC_SCRATCH_BYTES in include/nsv.h
 
 
 @pytest.fixture(scope="module")
@@ -62,7 +62,7 @@ def test_noalloc_matches_existing_entry_point_on_two_calls(nsv, make):
         inp = device_inputs(wl, value_seed=value_seed)
         shape = nsv.shape_of(inp["q"], inp["k_pool"], inp["block_tables"])
         plan = nsv.plan_split(shape)
-        assert plan.mode == nsv.MODE_SPLIT and 0 < plan.workspace_bytes <= SCRATCH_LIMIT, \
+        assert 0 < plan.workspace_bytes <= SCRATCH_LIMIT, \
             "the case must use scratch memory and fit the static buffer"
         want = gpu_read(wl, inp, plan=plan)          # existing entry point
         got = torch.full_like(inp["q"], float("nan"))
@@ -77,7 +77,9 @@ def test_noalloc_refuses_shapes_beyond_its_buffer(nsv):
     before anything is launched.  The tensors are real and every row is empty,
     so even a launch could not read or write out of bounds."""
     import torch
-    rows, heads, kv_heads, head_dim, max_blocks = 256, 32, 32, 128, 512
+    # 16 query heads per KV head: one KV head per CTA, 16 consumer warps and two
+    # CTAs per SM make the partial-state scratch larger than the buffer.
+    rows, heads, kv_heads, head_dim, max_blocks = 256, 128, 8, 128, 512
     q = torch.zeros((rows, heads, head_dim), dtype=torch.bfloat16, device="cuda")
     out = torch.zeros_like(q)
     pool = torch.zeros((2, kv_heads, 16, head_dim), dtype=torch.bfloat16, device="cuda")
