@@ -4,7 +4,7 @@
                     [--workload headline_bf16]
 
 Prints ONE JSON line (rank 0).  A step is the whole hot path over one batch:
-nsv_kv_write then the decode read (decode kernel + combine kernel), on the
+nsv_kv_write then the decode read (one kernel), on the
 headline workload by default (256 rows, 32 heads, head_dim 128, block 16,
 width 8192, lengths uniform in [512, 8192], bf16, seeded synthetic data).
 
@@ -17,9 +17,10 @@ e2e       = the same metric through the C ABI with the step's inputs in
             write_slots, block_tables and context_lens host->device and the
             output device->host inside the timed region (the KV pool is the
             resident cache and stays on the device).
-roofline  = the decode read alone (its two launches): read bytes (K+V + q +
-            out) / its CUDA-event time, against the measured HBM copy
-            bandwidth in MEASURED_PEAKS.json.
+roofline  = the decode read alone: read bytes (K+V + q + out) / its
+            CUDA-event time, against the measured HBM copy bandwidth in
+            MEASURED_PEAKS.json.  Workloads smaller than 4x L2 flush L2
+            (a 256 MB write) before every step, outside the timed spans.
 cpu_baseline = the oracle (plain C, fp64) timed on this host's cores on a
             time-bounded sample of rows of the same workload.
 
@@ -284,13 +285,15 @@ def run_nsv(args, wl):
     shape = nsv.shape_of(q, kp, bt)
     plan = nsv.plan_split(shape)
     wsp = nsv.workspace_for(plan)
-    launches_per_step = 3  # kv_write, decode_kernel, combine_kernel
+    launches_per_step = 2  # kv_write_kernel, decode_kernel (plus one counter memset)
     small_l2 = wl.step_bytes() <= 4 * 129e6
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if small_l2 else None
 
-    def step(ev_a=None, ev_b=None):
+    def step(ev_s=None, ev_a=None, ev_b=None):
         if flush is not None:
             flush.zero_()
+        if ev_s is not None:
+            ev_s.record(stream)
         nsv.kv_write(kn, vn, slots, kp, vp)
         if ev_a is not None:
             ev_a.record(stream)
@@ -316,8 +319,7 @@ def run_nsv(args, wl):
     sampler.start()
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         dist.barrier()
@@ -329,8 +331,11 @@ def run_nsv(args, wl):
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
-    total_ms = start.elapsed_time(end)
-    read_ms = [a.elapsed_time(b) for a, b in ev]
+    if flush is None:
+        total_ms = start.elapsed_time(end)
+    else:  # the flushes sit between the timed spans
+        total_ms = sum(s0.elapsed_time(b) for s0, _, b in ev)
+    read_ms = [a.elapsed_time(b) for _, a, b in ev]
 
     # end to end through the C ABI from pinned host buffers
     E = args.e2e_steps or min(K, 100)
@@ -344,28 +349,30 @@ def run_nsv(args, wl):
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_bt, h_ctx, h_slots))
     d2h = h_out.numel() * h_out.element_size()
 
-    def e2e_step():
+    def e2e_step(ev_s=None, ev_e=None):
         if flush is not None:
             flush.zero_()
+        if ev_s is not None:
+            ev_s.record(stream)
         for d, h in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_bt, h_bt), (d_ctx, h_ctx),
                      (d_slots, h_slots)):
             d.copy_(h, non_blocking=True)
         nsv.decode_step(d_q, d_kn, d_vn, d_slots, kp, vp, d_bt, d_ctx, wl.scale, out,
                         workspace=wsp, plan=plan)
         h_out.copy_(out, non_blocking=True)
+        if ev_e is not None:
+            ev_e.record(stream)
 
     for _ in range(3):
         e2e_step()
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(E):
-        e2e_step()
-    e1.record(stream)
+    eev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2)) for _ in range(E)]
+    for k in range(E):
+        e2e_step(*eev[k])
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / E
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / E
     clocks = sampler.stop()
     st, _ = nsv.device_status(clear=True)
     if st:
@@ -393,7 +400,7 @@ def run_nsv(args, wl):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback",
-                     "kernel": "decode read (decode_kernel + combine_kernel)",
+                     "kernel": "decode read (decode_kernel)",
                      "bytes_per_launch": wl.read_bytes(), "us_per_launch": ms_read * 1e3,
                      "traffic": recorded_traffic()},
         "e2e": {"value": whole_job_gbs(step_bytes, ws, e2e_ms), "unit": "GB/s",

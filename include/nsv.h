@@ -123,7 +123,8 @@ typedef struct nsv_shape {
  * The read is split evenly over a persistent grid: the units (KV-head group,
  * row, block) of all rows are laid end to end and CTA c of `grid` takes the
  * units [c*U/grid, (c+1)*U/grid).  A row cut by CTA boundaries is finished by
- * a second kernel that merges the partial softmax states of its pieces. */
+ * the CTA that completes its last piece, which merges the partial softmax
+ * states of all its pieces. */
 typedef struct nsv_plan {
     int32_t kv_heads_per_cta; /* KV heads one CTA streams together (a head group) */
     int32_t stages;           /* shared-memory pipeline depth */
@@ -183,8 +184,9 @@ NSV_API int nsv_paged_decode(const nsv_shape *shape, const void *q, const void *
 /*
  * Decode read with an explicit plan (NULL: the default plan) and a
  * caller-owned device workspace of at least plan->workspace_bytes bytes
- * (256-byte aligned; may be NULL when that is 0).  The workspace holds no
- * state between calls.  Two calls that overlap on the GPU need two
+ * (256-byte aligned).  The workspace holds no state between calls; each
+ * call clears the part that must start at zero with one cudaMemsetAsync on
+ * `stream` before its kernel.  Two calls that overlap on the GPU need two
  * workspaces.  A plan passed in must be one nsv_plan_split/nsv_plan_custom
  * returned for this shape (NSV_ERR_RANGE otherwise).
  */

@@ -30,9 +30,11 @@
 //    to the lanes that own the value dims, and P.V accumulates in fp32.
 //  * A segment (a CTA's run of one row) that covers the whole row writes
 //    `out` directly.  A row cut by CTA boundaries leaves one partial (m, l,
-//    acc) per CTA it crosses -- at most two per CTA -- and the combine kernel
-//    merges them (flash-decoding style); it also writes the zero output of
-//    empty rows.
+//    acc) per CTA it crosses -- at most two per CTA.  Each piece's CTA then
+//    counts itself in the row's arrival counter, and the CTA that arrives
+//    last merges the pieces (flash-decoding style) and writes `out`.  Nobody
+//    waits for anybody: the last arrival finds every partial already
+//    written.  Empty rows get their zero output from the consumers up front.
 //  * No tensor cores: one query per head makes each tile a GEMV.
 // Every wait is bounded; a wait that gives up sets NSV_DEV_TIMEOUT and the
 // kernel returns.  Bad lengths and block ids are skipped and flagged.
@@ -180,6 +182,11 @@ __device__ __forceinline__ int checked_ctx(const DecodeParams& p, int r) {
   return c;
 }
 
+// Barrier over the consumer warps only (the producer never joins it).
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
 // CTA whose unit range [c*U/G, (c+1)*U/G) holds unit u (the last such c
 // when empty ranges share a start).
 __device__ __forceinline__ int cta_of(long long u, long long U, int G) {
@@ -248,9 +255,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
     if (lane == 0) s_prefix[0] = 0;
   }
   __syncthreads();
-  if (blockIdx.x == 0) {  // the combine kernel reads the same prefix
-    for (int r = tid; r <= p.rows; r += blockDim.x) p.ws_prefix[r] = s_prefix[r];
-  }
 
   const int nhg = p.kv_heads / HG;
   const int N = s_prefix[p.rows];                 // blocks per head group
@@ -377,6 +381,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
   const int grp = lane / kLpt;        // which token of a warp-wide load
   const int tok = (sub / kDup) * kTpi + grp;  // token whose score this lane ends with
   float* pbuf = s_pbuf + cw * kBlock;
+
+  volatile int* s_merge = s_abort + 1;
+
+  // Empty rows attend over nothing: their output is zero.  CTA c writes the
+  // empty rows c, c + G, ...; its consumer warps share the heads.
+  for (int r = blockIdx.x; r < p.rows; r += gridDim.x) {
+    if (s_prefix[r + 1] != s_prefix[r]) continue;
+    for (int h = cw; h < p.heads; h += ncw)
+      if (lane < kLpt)
+        *reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)r * p.heads + h) * D +
+                                  sub * kDpl) = make_uint4(0u, 0u, 0u, 0u);
+  }
 
   float qv[kDpl], acc[kDpl];
   float m = -INFINITY, l = 0.f;
@@ -507,93 +523,88 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
             *reinterpret_cast<float4*>(a + e) = make_float4(at[e], at[e + 1], at[e + 2], at[e + 3]);
         }
         if (lane == 0) p.ws_ml[slot] = make_float2(m, lt);
+        // Publish this CTA's piece of the row and count it.
+        __threadfence();
+        consumer_sync(ncw * 32);
+        const int hg = (flags >> 16) / HG;
+        const int pr = s_prefix[row], nb = s_prefix[row + 1] - pr;
+        const long long u0 = (long long)hg * N + pr, u1 = u0 + nb;
+        const int c0 = cta_of(u0, U, gridDim.x), c1 = cta_of(u1 - 1, U, gridDim.x);
+        if (cw == 0 && lane == 0) {
+          int pieces = c1 - c0 + 1;
+          if (U < gridDim.x) {  // some CTAs have no units and wrote nothing
+            pieces = 0;
+            for (int c = c0; c <= c1; ++c)
+              pieces += ((long long)(c + 1) * U / gridDim.x != (long long)c * U / gridDim.x);
+          }
+          int* cnt = p.ws_cnt + (size_t)row * nhg + hg;
+          const int before = atomicAdd(cnt, 1);
+          const bool last = before == pieces - 1;
+          if (last) *cnt = 0;  // every piece has arrived: nobody touches it again
+          *s_merge = last ? 1 : 0;
+        }
+        consumer_sync(ncw * 32);
+        if (*s_merge) {
+          // The last piece to arrive merges all pieces of the row for the
+          // warp's query head.  Lane l owns dims [l*D/32, (l+1)*D/32).
+          __threadfence();
+          constexpr int kPer = D / 32;
+          const int ns = c1 - c0 + 1;
+          float M = -INFINITY;
+          for (int k = lane; k < ns; k += 32) {
+            const int c = c0 + k;
+            const long long sc = (long long)c * U / gridDim.x;
+            if ((long long)(c + 1) * U / gridDim.x == sc) continue;  // CTA with no units
+            const int sl = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
+            M = fmaxf(M, __ldcg(&p.ws_ml[(size_t)sl * ncw + cw]).x);
+          }
+#pragma unroll
+          for (int o2 = 16; o2 >= 1; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
+          float Lsum = 0.f, a[kPer];
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) a[e] = 0.f;
+          for (int base = 0; base < ns; base += 32) {
+            const int c = c0 + base + lane;
+            float w = 0.f;
+            int idx = 0;
+            if (base + lane < ns) {
+              const long long sc = (long long)c * U / gridDim.x;
+              if ((long long)(c + 1) * U / gridDim.x != sc) {
+                const int sl = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
+                idx = sl * ncw + cw;
+                const float2 ml = __ldcg(&p.ws_ml[idx]);
+                w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+                Lsum = fmaf(w, ml.y, Lsum);
+              }
+            }
+            const int cnt = min(32, ns - base);
+            for (int k = 0; k < cnt; ++k) {
+              const float wk = __shfl_sync(kFull, w, k);
+              const int ik = __shfl_sync(kFull, idx, k);
+              if (wk != 0.f) {
+                const float* src = p.ws_acc + (size_t)ik * D + lane * kPer;
+#pragma unroll
+                for (int e = 0; e < kPer; ++e) a[e] = fmaf(wk, __ldcg(src + e), a[e]);
+              }
+            }
+          }
+#pragma unroll
+          for (int o2 = 16; o2 >= 1; o2 >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, o2);
+          const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+          T* o = static_cast<T*>(p.out) + ((size_t)row * p.heads + qh) * D + lane * kPer;
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) {
+            if constexpr (sizeof(T) == 4) {
+              o[e] = a[e] * inv;
+            } else {
+              o[e] = __float2bfloat16_rn(a[e] * inv);
+            }
+          }
+        }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (S + s));
-  }
-}
-
-// Finish every row the decode kernel did not: merge the partial softmax
-// states of rows cut by CTA boundaries, and write zeros for empty rows.  One
-// warp per (row, query head).  The partials' (m, l) are loaded by all lanes
-// at once (one partial per lane); the acc slices are then summed with the
-// weights broadcast from the lane that loaded them.
-template <typename T, int D>
-__global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
-  constexpr int kPer = D / 32;  // dims per lane
-  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (gw >= p.rows * p.heads) return;
-  const int row = gw / p.heads, qh = gw - row * p.heads;
-  const int N = p.ws_prefix[p.rows];
-  const int pr = p.ws_prefix[row];
-  const int nb = p.ws_prefix[row + 1] - pr;
-  T* o = static_cast<T*>(p.out) + (size_t)gw * D + lane * kPer;
-  float a[kPer];
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) a[e] = 0.f;
-  float inv = 0.f;
-  if (nb > 0) {
-    const int nhg = p.kv_heads / p.heads_per_cta;
-    const int ncw = p.heads_per_cta * p.group;
-    const long long U = (long long)N * nhg;
-    const int hg = (qh / p.group) / p.heads_per_cta;
-    const int cw = qh - hg * ncw;
-    const long long u0 = (long long)hg * N + pr, u1 = u0 + nb;
-    const int c0 = cta_of(u0, U, p.grid), c1 = cta_of(u1 - 1, U, p.grid);
-    if (c0 == c1) return;  // one CTA held the whole row and wrote it
-    const int ns = c1 - c0 + 1;
-    // pass 1: the running max over all partials
-    float M = -INFINITY;
-    for (int k = lane; k < ns; k += 32) {
-      const int c = c0 + k;
-      const long long sc = (long long)c * U / p.grid;
-      if ((long long)(c + 1) * U / p.grid == sc) continue;  // CTA with no units
-      const int slot = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
-      M = fmaxf(M, p.ws_ml[(size_t)slot * ncw + cw].x);
-    }
-#pragma unroll
-    for (int o2 = 16; o2 >= 1; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
-    // pass 2: weights per partial (one per lane), then the weighted sums
-    float Lsum = 0.f;
-    for (int base = 0; base < ns; base += 32) {
-      const int c = c0 + base + lane;
-      float w = 0.f;
-      int idx = 0;
-      if (base + lane < ns) {
-        const long long sc = (long long)c * U / p.grid;
-        if ((long long)(c + 1) * U / p.grid != sc) {
-          const int slot = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
-          idx = slot * ncw + cw;
-          const float2 ml = p.ws_ml[idx];
-          w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-          Lsum = fmaf(w, ml.y, Lsum);
-        }
-      }
-      const int cnt = min(32, ns - base);
-#pragma unroll 4
-      for (int k = 0; k < cnt; ++k) {
-        const float wk = __shfl_sync(kFull, w, k);
-        const int ik = __shfl_sync(kFull, idx, k);
-        if (wk != 0.f) {
-          const float* src = p.ws_acc + (size_t)ik * D + lane * kPer;
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) a[e] = fmaf(wk, src[e], a[e]);
-        }
-      }
-    }
-#pragma unroll
-    for (int o2 = 16; o2 >= 1; o2 >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, o2);
-    inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-  }
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    if constexpr (sizeof(T) == 4) {
-      o[e] = a[e] * inv;
-    } else {
-      o[e] = __float2bfloat16_rn(a[e] * inv);
-    }
   }
 }
 
@@ -625,25 +636,6 @@ cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int gr
       decode_kernel<__nv_bfloat16, 64><<<grid, threads, smem, stream>>>(p);
     else
       decode_kernel<__nv_bfloat16, 128><<<grid, threads, smem, stream>>>(p);
-  }
-  return cudaGetLastError();
-}
-
-cudaError_t launch_combine(const CombineParams& p, int dtype, int head_dim, cudaStream_t stream) {
-  const long long warps = (long long)p.rows * p.heads;
-  if (warps == 0) return cudaSuccess;
-  const int wpb = 8;
-  const int grid = (int)((warps + wpb - 1) / wpb);
-  if (dtype == NSV_F32) {
-    if (head_dim == 64)
-      combine_kernel<float, 64><<<grid, wpb * 32, 0, stream>>>(p);
-    else
-      combine_kernel<float, 128><<<grid, wpb * 32, 0, stream>>>(p);
-  } else {
-    if (head_dim == 64)
-      combine_kernel<__nv_bfloat16, 64><<<grid, wpb * 32, 0, stream>>>(p);
-    else
-      combine_kernel<__nv_bfloat16, 128><<<grid, wpb * 32, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }

@@ -83,8 +83,6 @@ int check_shape(const nsv_shape* s) {
   return NSV_OK;
 }
 
-int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
 int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int grid,
               nsv_plan* p) {
   int rc = check_shape(s);
@@ -137,7 +135,8 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   } else if (grid > (1 << 16)) {
     return NSV_ERR_RANGE;
   }
-  const WsLayout W = make_ws_layout(rows_for_layout, grid, hg * G, s->head_dim);
+  const WsLayout W =
+      make_ws_layout(rows_for_layout, s->num_kv_heads / hg, grid, hg * G, s->head_dim);
   memset(p, 0, sizeof(*p));
   p->kv_heads_per_cta = hg;
   p->stages = stages;
@@ -200,10 +199,12 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   if (!ws || ws_bytes < (size_t)plan.workspace_bytes ||
       (reinterpret_cast<uintptr_t>(ws) & 255u))
     return NSV_ERR_WORKSPACE;
-  const WsLayout W = make_ws_layout(s->rows, plan.grid,
+  const WsLayout W = make_ws_layout(s->rows, s->num_kv_heads / plan.kv_heads_per_cta, plan.grid,
                                     plan.kv_heads_per_cta * (s->num_heads / s->num_kv_heads),
                                     s->head_dim);
   char* wsb = static_cast<char*>(ws);
+  // The arrival counters of cut rows start every call at zero.
+  if (cudaMemsetAsync(wsb, 0, W.cnt_bytes, stream) != cudaSuccess) return cuda_fail();
   DecodeParams p;
   p.q = q;
   p.k_pool = k_pool;
@@ -211,7 +212,7 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   p.block_tables = block_tables;
   p.context_lens = context_lens;
   p.out = out;
-  p.ws_prefix = reinterpret_cast<int32_t*>(wsb);
+  p.ws_cnt = reinterpret_cast<int32_t*>(wsb);
   p.ws_ml = reinterpret_cast<float2*>(wsb + W.off_ml);
   p.ws_acc = reinterpret_cast<float*>(wsb + W.off_acc);
   p.status = d->status;
@@ -228,18 +229,6 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   if (launch_decode(p, s->dtype, s->head_dim, plan.grid, plan.threads, plan.smem_bytes, stream) !=
       cudaSuccess)
     return cuda_fail();
-  CombineParams c;
-  c.ws_prefix = p.ws_prefix;
-  c.ws_ml = p.ws_ml;
-  c.ws_acc = p.ws_acc;
-  c.out = out;
-  c.rows = s->rows;
-  c.heads = s->num_heads;
-  c.group = p.group;
-  c.heads_per_cta = plan.kv_heads_per_cta;
-  c.kv_heads = s->num_kv_heads;
-  c.grid = plan.grid;
-  if (launch_combine(c, s->dtype, s->head_dim, stream) != cudaSuccess) return cuda_fail();
   return NSV_OK;
 }
 

@@ -32,19 +32,22 @@ enum : int {
 };
 
 // Workspace of one decode read (all offsets 256-byte aligned):
-//   prefix  int32 [rows + 1]   blocks before each row (written by CTA 0)
+//   cnt     int32 [rows][head groups]  pieces of a cut row that have
+//           finished; zeroed on the stream before every launch
 //   ml      float2 [grid][2][cw]  (running max, denominator) of partials
 //   acc     float [grid][2][cw][head_dim]
 // where cw = query heads per CTA.  Each CTA has at most two partial
 // segments: the row its range starts inside of and the row it ends inside of.
 struct WsLayout {
-  uint64_t off_ml, off_acc, total;
+  uint64_t cnt_bytes, off_ml, off_acc, total;
 };
 
-__host__ __device__ inline WsLayout make_ws_layout(int rows, int grid, int cw, int head_dim) {
+__host__ __device__ inline WsLayout make_ws_layout(int rows, int head_groups, int grid, int cw,
+                                                   int head_dim) {
   WsLayout W;
   const uint64_t slots = (uint64_t)grid * 2 * cw;
-  W.off_ml = ((uint64_t)(rows + 1) * 4 + 255) / 256 * 256;
+  W.cnt_bytes = (uint64_t)rows * head_groups * 4;
+  W.off_ml = (W.cnt_bytes + 255) / 256 * 256;
   W.off_acc = W.off_ml + (slots * 8 + 255) / 256 * 256;
   W.total = W.off_acc + slots * head_dim * 4;
   return W;
@@ -57,7 +60,7 @@ struct DecodeParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   void* out;
-  int32_t* ws_prefix;  // workspace prefix (rows + 1)
+  int32_t* ws_cnt;     // workspace arrival counters (zero at launch)
   float2* ws_ml;       // workspace partial (m, l)
   float* ws_acc;       // workspace partial acc
   uint32_t* status;    // device status word
@@ -68,14 +71,6 @@ struct DecodeParams {
   int group;          // query heads per KV head
   int stages;
   float qscale;       // scale * log2(e)
-};
-
-struct CombineParams {
-  const int32_t* ws_prefix;
-  const float2* ws_ml;
-  const float* ws_acc;
-  void* out;
-  int rows, heads, group, heads_per_cta, kv_heads, grid;
 };
 
 struct KvWriteParams {
@@ -100,7 +95,7 @@ struct SmemLayout {
   uint32_t off_pbuf;     // per consumer warp: block-size floats
   uint32_t off_ctx;      // rows ints (validated context lengths)
   uint32_t off_prefix;   // rows + 1 ints (work-item prefix sums)
-  uint32_t off_flag;     // abort flag
+  uint32_t off_flag;     // abort flag, then the merge flag
   uint32_t total;
 };
 
@@ -127,7 +122,7 @@ __host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int he
   L.off_prefix = off;
   off += (uint32_t)(rows + 1) * 4;
   L.off_flag = align_up(off, 4);
-  off = L.off_flag + 4;
+  off = L.off_flag + 8;
   L.total = align_up(off, 128);
   return L;
 }
@@ -135,8 +130,6 @@ __host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int he
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int grid,
                           int threads, int smem, cudaStream_t stream);
-cudaError_t launch_combine(const CombineParams& p, int dtype, int head_dim,
-                           cudaStream_t stream);
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
 // One-time per-device attribute set-up of the decode kernels.
 cudaError_t prepare_decode_kernels();

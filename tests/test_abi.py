@@ -68,8 +68,9 @@ def test_plan_headline_shape(nsv):
     assert p.kv_heads_per_cta == 8 and p.threads == 9 * 32
     assert p.stages == 3 and p.ctas_per_sm == 1 and p.grid == 152
     assert p.smem_bytes <= 227 * 1024
-    slots = 152 * 2 * 8
-    want = -(-257 * 4 // 256) * 256 + -(-slots * 8 // 256) * 256 + slots * 128 * 4
+    slots = 152 * 2 * 8                      # two partials per CTA, 8 query heads
+    counters = 256 * (32 // 8) * 4           # one per (row, head group)
+    want = -(-counters // 256) * 256 + -(-slots * 8 // 256) * 256 + slots * 128 * 4
     assert p.workspace_bytes == want
     again = nsv.plan_split(_shape(nsv), num_sms=152)
     assert bytes(again) == bytes(p), "planning must be deterministic"
