@@ -287,11 +287,16 @@ def run_nsv(args, wl):
     wsp = nsv.workspace_for(plan)
     launches_per_step = 2  # kv_write_kernel, decode_kernel (plus one counter memset)
     small_l2 = wl.step_bytes() <= 4 * 129e6
+    # L2 flush for small workloads: write a buffer larger than L2, then read
+    # another one, so that L2 holds clean lines and no write-back of the
+    # flush lands inside the next timed span.
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if small_l2 else None
+    flush_rd = torch.ones(32 << 20, dtype=torch.int64, device="cuda") if small_l2 else None
 
     def step(ev_s=None, ev_a=None, ev_b=None):
         if flush is not None:
             flush.zero_()
+            flush_rd.sum()
         if ev_s is not None:
             ev_s.record(stream)
         nsv.kv_write(kn, vn, slots, kp, vp)
@@ -352,6 +357,7 @@ def run_nsv(args, wl):
     def e2e_step(ev_s=None, ev_e=None):
         if flush is not None:
             flush.zero_()
+            flush_rd.sum()
         if ev_s is not None:
             ev_s.record(stream)
         for d, h in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_bt, h_bt), (d_ctx, h_ctx),

@@ -34,6 +34,7 @@ The five named workloads:
                 padded; pool = what the rows need + 10% free.
   headline_bf16 256 rows, 32 heads, head_dim 128, width 8192, lengths
                 uniform integers in [512, 8192]; pool = the sum.
+  headline_gqa4_bf16  the same with 8 KV heads shared by 32 query heads.
 """
 
 from dataclasses import dataclass, field
@@ -204,12 +205,22 @@ def headline_bf16(seed=4):
                  block_size=16, max_blocks=512, dtype="bf16", lens=lens, rng=rng)
 
 
+def headline_gqa4_bf16(seed=4):
+    """The headline batch with grouped-query attention: 32 query heads share
+    8 KV heads (4 per group); same lengths and pool recipe."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(512, 8192, size=256, endpoint=True)
+    return _make("headline_gqa4_bf16", seed, rows=256, heads=32, kv_heads=8, head_dim=128,
+                 block_size=16, max_blocks=512, dtype="bf16", lens=lens, rng=rng)
+
+
 WORKLOADS = {
     "tiny_f32": tiny_f32,
     "uniform_f32": uniform_f32,
     "ragged_bf16": ragged_bf16,
     "manyrow_bf16": manyrow_bf16,
     "headline_bf16": headline_bf16,
+    "headline_gqa4_bf16": headline_gqa4_bf16,
 }
 
 
