@@ -79,7 +79,7 @@ class Oracle:
         lib = ctypes.CDLL(path)
         i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
         lib.oracle_paged_decode.restype = i32
-        lib.oracle_paged_decode.argtypes = [i64, i64, i64, i64, i64, i64, i64, i32,
+        lib.oracle_paged_decode.argtypes = [i64, i64, i64, i64, i64, i64, i64, i64, i32,
                                             vp, vp, vp, vp, vp, dbl, vp, i64, i32, vp]
         lib.oracle_kv_write.restype = i32
         lib.oracle_kv_write.argtypes = [i64, i64, i64, i64, i64, i32, vp, vp, vp, vp, vp]
@@ -101,11 +101,19 @@ class Oracle:
 
     def paged_decode(self, q, k_pool, v_pool, block_tables, context_lens, scale,
                      rows=None, threads=0):
-        """The reference read for the selected rows; returns fp64 [len(rows), H, D]."""
+        """The reference read for the selected rows.
+
+        q is [R, H, D] (one query token per row; returns fp64 [len(rows), H, D])
+        or [R, NQ, H, D] (NQ query tokens per row, causal among themselves;
+        returns fp64 [len(rows), NQ, H, D]).
+        """
         dt = _dtype_code(k_pool)
         if _dtype_code(q) != dt or _dtype_code(v_pool) != dt:
             raise TypeError("q, k_pool and v_pool must share one dtype")
-        R, H, D = q.shape
+        single = q.ndim == 3
+        if single:
+            q = q[:, None]
+        R, NQ, H, D = q.shape
         NB1, Hkv, B, D2 = k_pool.shape
         if D2 != D or v_pool.shape != k_pool.shape:
             raise ValueError("pool shape does not match q")
@@ -120,13 +128,13 @@ class Oracle:
         else:
             rows_arr, rp = _c(np.asarray(rows, dtype=np.int64), np.int64)
             nrows = rows_arr.shape[0]
-        out = np.zeros((nrows, H, D), dtype=np.float64)
-        rc = self.lib.oracle_paged_decode(R, H, Hkv, D, B, MB, NB1 - 1, dt, qp, kp, vpp,
+        out = np.zeros((nrows, NQ, H, D), dtype=np.float64)
+        rc = self.lib.oracle_paged_decode(R, NQ, H, Hkv, D, B, MB, NB1 - 1, dt, qp, kp, vpp,
                                           btp, clp, float(scale), rp, nrows,
                                           int(threads), out.ctypes.data)
         if rc != 0:
             raise OracleRefusal(rc)
-        return out
+        return out[:, 0] if single else out
 
     def kv_write(self, k_new, v_new, write_slots, k_pool, v_pool):
         """The KV append, in place on the numpy pools."""

@@ -30,6 +30,12 @@
  *     fp64.  Because it gathers before it masks, a padding entry must be a
  *     legal index; a negative entry wraps onto the end of the pool array the
  *     way a Python index does (Day 59, "Why it matters").
+ *     With query_len = n > 1 (several query tokens per row, the multi-token
+ *     form of the Day-22 single-sequence loop that Day 59 "What I learned"
+ *     item 3 describes with [n_q, d] accumulators), query token j of a row
+ *     of length ctx sits at position ctx - n + j and sees the positions
+ *     t < ctx - n + 1 + j (causal within the step's new tokens); a query
+ *     that sees no position outputs 0.  query_len 1 is the decode read.
  *   - oracle_kv_write: pool[write_slots[r]] = new[r], one row at a time.
  *   - oracle_walked_tiles / oracle_rect_tiles: the tile accounting of the
  *     streamed read (tiles walked = sum over rows of cdiv(ctx, tile); the
@@ -95,20 +101,22 @@ static int elem_bytes(int dtype)
 /*
  * The reference read over a subset of rows.
  *
+ * NQ: query tokens per row (1 for the decode read).
  * rows / nrows: which rows to compute (rows == NULL means 0..R-1, nrows = R).
- * out: fp64 [nrows][H][D], row i of out belongs to batch row rows[i].
+ * out: fp64 [nrows][NQ][H][D], row i of out belongs to batch row rows[i].
  * threads: OpenMP threads (<= 0 means the runtime default).
  */
-int oracle_paged_decode(int64_t R, int64_t H, int64_t Hkv, int64_t D,
-                        int64_t B, int64_t MB, int64_t NB, int dtype,
-                        const void *q, const void *k_pool, const void *v_pool,
-                        const int32_t *block_tables,
+int oracle_paged_decode(int64_t R, int64_t NQ, int64_t H, int64_t Hkv,
+                        int64_t D, int64_t B, int64_t MB, int64_t NB,
+                        int dtype, const void *q, const void *k_pool,
+                        const void *v_pool, const int32_t *block_tables,
                         const int32_t *context_lens, double scale,
                         const int64_t *rows, int64_t nrows, int threads,
                         double *out)
 {
-    if (R < 0 || H <= 0 || Hkv <= 0 || D <= 0 || B <= 0 || MB <= 0 ||
-        NB <= 0 || H % Hkv != 0 || (dtype != OR_F32 && dtype != OR_BF16))
+    if (R < 0 || NQ <= 0 || H <= 0 || Hkv <= 0 || D <= 0 || B <= 0 ||
+        MB <= 0 || NB <= 0 || H % Hkv != 0 ||
+        (dtype != OR_F32 && dtype != OR_BF16))
         return OR_ERR_SHAPE;
     if (rows == NULL)
         nrows = R;
@@ -132,7 +140,7 @@ int oracle_paged_decode(int64_t R, int64_t H, int64_t Hkv, int64_t D,
     }
 
     int failed = 0;
-    const int64_t items = nrows * H;
+    const int64_t items = nrows * NQ * H;
 #ifdef _OPENMP
     int nt = threads > 0 ? threads : omp_get_max_threads();
 #pragma omp parallel num_threads(nt)
@@ -156,11 +164,15 @@ int oracle_paged_decode(int64_t R, int64_t H, int64_t Hkv, int64_t D,
         for (int64_t it = 0; it < items; ++it) {
             if (failed)
                 continue;
-            int64_t i = it / H, h = it % H;
+            int64_t i = it / (NQ * H), jq = (it / H) % NQ, h = it % H;
             int64_t r = rows ? rows[i] : i;
             int64_t g = h / group;
-            int64_t c = context_lens[r];
-            double *o = out + (i * H + h) * D;
+            /* positions this query sees: all of the row's for the last
+             * query token, one fewer for each token before it */
+            int64_t c = context_lens[r] - (NQ - 1 - jq);
+            if (c < 0)
+                c = 0;
+            double *o = out + ((i * NQ + jq) * H + h) * D;
 
             /* 1. Gather the whole rectangle through the block table.
              *    Position t lives in block table[r][t / B] at offset t % B. */
@@ -175,7 +187,7 @@ int oracle_paged_decode(int64_t R, int64_t H, int64_t Hkv, int64_t D,
                 }
             }
             for (int64_t d = 0; d < D; ++d)
-                qv[d] = widen(q, dtype, (r * H + h) * D + d);
+                qv[d] = widen(q, dtype, ((r * NQ + jq) * H + h) * D + d);
 
             /* 2. Score every position of the rectangle. */
             for (int64_t t = 0; t < W; ++t) {
@@ -189,7 +201,7 @@ int oracle_paged_decode(int64_t R, int64_t H, int64_t Hkv, int64_t D,
             for (int64_t t = 0; t < W; ++t)
                 s[t] = (t < c) ? s[t] : -INFINITY;
 
-            if (c == 0) { /* attends over nothing: output 0 */
+            if (c == 0) { /* sees no position: output 0 */
                 for (int64_t d = 0; d < D; ++d)
                     o[d] = 0.0;
                 continue;

@@ -83,30 +83,37 @@ def small_case(seed, dtype="f32", rows=None, heads=None, kv_heads=None,
 
 
 def brute_force(q, k, v, bt, ctx, scale, B):
-    """Per-key loop over a row's real positions; fp64; no rectangle, no mask."""
+    """Per-key loop over the positions each query sees; fp64; no rectangle,
+    no mask.  q is [R, H, D] (one query per row) or [R, NQ, H, D] (query
+    token j of NQ sees the row's first ctx - NQ + 1 + j positions)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
-    R, H, D = q.shape
+    single = q.ndim == 3
+    if single:
+        q = q[:, None]
+    R, NQ, H, D = q.shape
     Hkv = k.shape[1]
     group = H // Hkv
-    out = np.zeros((R, H, D))
+    out = np.zeros((R, NQ, H, D))
     for r in range(R):
-        c = int(ctx[r])
-        for h in range(H):
-            if c == 0:
-                continue
-            g = h // group
-            keys, vals = [], []
-            for t in range(c):
-                blk = int(bt[r, t // B])
-                keys.append(k[blk, g, t % B])
-                vals.append(v[blk, g, t % B])
-            scores = [scale * math.fsum(q[r, h, d] * kk[d] for d in range(D)) for kk in keys]
-            mx = max(scores)
-            w = [math.exp(s - mx) for s in scores]
-            z = math.fsum(w)
-            for d in range(D):
-                out[r, h, d] = math.fsum(w[t] / z * vals[t][d] for t in range(c))
-    return out
+        for j in range(NQ):
+            c = int(ctx[r]) - (NQ - 1 - j)
+            for h in range(H):
+                if c <= 0:
+                    continue
+                g = h // group
+                keys, vals = [], []
+                for t in range(c):
+                    blk = int(bt[r, t // B])
+                    keys.append(k[blk, g, t % B])
+                    vals.append(v[blk, g, t % B])
+                scores = [scale * math.fsum(q[r, j, h, d] * kk[d] for d in range(D))
+                          for kk in keys]
+                mx = max(scores)
+                w = [math.exp(s - mx) for s in scores]
+                z = math.fsum(w)
+                for d in range(D):
+                    out[r, j, h, d] = math.fsum(w[t] / z * vals[t][d] for t in range(c))
+    return out[:, 0] if single else out
 
 
 def _decode(orc, cs, **over):
@@ -135,6 +142,64 @@ def pin_gqa_brute_force(orc):
     got = _decode(orc, cs)
     ref = brute_force(cs["q"], cs["k"], cs["v"], cs["bt"], cs["ctx"], cs["scale"], cs["B"])
     assert np.max(np.abs(got - ref)) <= 1e-12
+
+
+def _mq_case(seed, nq, dtype="f32", lens=None, heads=2, kv_heads=2):
+    cs = small_case(seed, dtype, heads=heads, kv_heads=kv_heads, head_dim=8, block_size=4,
+                    lens=lens)
+    rng = np.random.default_rng(seed + 7)
+    R, H, D = cs["q"].shape
+    cs["q"] = _values(rng, (R, nq, H, D), dtype)
+    return cs
+
+
+def pin_multiquery_brute_force(orc):
+    for seed, nq, dtype in ((30, 2, "f32"), (31, 3, "bf16"), (32, 4, "f32")):
+        cs = _mq_case(seed, nq, dtype, lens=[1, 2, 5, 11, 0, 17], heads=4, kv_heads=2)
+        got = _decode(orc, cs)
+        ref = brute_force(cs["q"], cs["k"], cs["v"], cs["bt"], cs["ctx"], cs["scale"], cs["B"])
+        assert got.shape == ref.shape
+        assert np.max(np.abs(got - ref)) <= 1e-12, "multi-query oracle vs brute force"
+
+
+def pin_multiquery_last_token_is_the_decode_read(orc):
+    cs = _mq_case(33, 3, "bf16", lens=[7, 3, 20, 9])
+    got = _decode(orc, cs)
+    single = _decode(orc, cs, q=np.ascontiguousarray(cs["q"][:, -1]))
+    assert np.array_equal(got[:, -1], single)
+
+
+def pin_multiquery_first_token_sees_one_key(orc):
+    nq = 3
+    cs = _mq_case(34, nq, "f32", lens=[nq, nq, nq])
+    got = _decode(orc, cs)
+    v = _f64(cs["v"])
+    for r in range(3):
+        blk = int(cs["bt"][r, 0])
+        for h in range(2):
+            assert np.array_equal(got[r, 0, h], v[blk, h, 0]), "query 0 sees position 0 only"
+
+
+def pin_multiquery_is_causal(orc):
+    """Changing the value at position p leaves every query that cannot see p
+    bit-identical and changes the ones that can."""
+    nq = 4
+    cs = _mq_case(35, nq, "f32", lens=[13])
+    base = _decode(orc, cs)
+    p = 13 - 2                     # seen by queries j with 13 - 3 + j > p, i.e. j >= 2
+    v2 = cs["v"].copy()
+    v2[int(cs["bt"][0, p // 4]), :, p % 4, :] += 1.0
+    got = _decode(orc, cs, v=v2)
+    assert np.array_equal(got[0, :2], base[0, :2])
+    assert np.all(np.abs(got[0, 2:] - base[0, 2:]).max(axis=-1) > 0)
+
+
+def pin_multiquery_short_row(orc):
+    nq = 4
+    cs = _mq_case(36, nq, "f32", lens=[2])
+    got = _decode(orc, cs)
+    assert np.all(got[0, :2] == 0.0), "queries that see no position output 0"
+    assert np.any(got[0, 2:] != 0.0)
 
 
 def pin_single_key(orc):
@@ -336,4 +401,6 @@ ALL_PINS = [
     pin_constant_v, pin_scale_zero_is_mean, pin_ctx_zero, pin_permutation_invariance,
     pin_padding_value_irrelevant, pin_rectangle_reads_padding, pin_refusals,
     pin_kv_write, pin_walk_table, pin_walk_counts_tiles_touched, pin_score_bytes,
+    pin_multiquery_brute_force, pin_multiquery_last_token_is_the_decode_read,
+    pin_multiquery_first_token_sees_one_key, pin_multiquery_is_causal, pin_multiquery_short_row,
 ]

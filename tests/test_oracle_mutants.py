@@ -25,8 +25,12 @@ MUTANTS = {
     "softmax_sign": ("s[t] = exp(s[t] - m);", "s[t] = exp(m - s[t]);"),
     "no_normalisation": ("s[t] /= z;", "s[t] /= 1.0;"),
     "pv_uses_keys": ("o[d] += s[t] * Vrect[t * D + d];", "o[d] += s[t] * Krect[t * D + d];"),
-    "query_transposed": ("qv[d] = widen(q, dtype, (r * H + h) * D + d);",
-                         "qv[d] = widen(q, dtype, (h * R + r) * D + d);"),
+    "query_transposed": ("qv[d] = widen(q, dtype, ((r * NQ + jq) * H + h) * D + d);",
+                         "qv[d] = widen(q, dtype, ((h * NQ + jq) * R + r) * D + d);"),
+    "causal_offset_reversed": ("int64_t c = context_lens[r] - (NQ - 1 - jq);",
+                               "int64_t c = context_lens[r] - jq;"),
+    "causal_window_ignored": ("int64_t c = context_lens[r] - (NQ - 1 - jq);",
+                              "int64_t c = context_lens[r];"),
     "no_negative_wrap": ("b += pool_blocks;", "b = 0;"),
     "kv_write_swaps_k_v": ("memcpy((char *)k_pool + dst, (const char *)k_new + src,",
                            "memcpy((char *)k_pool + dst, (const char *)v_new + src,"),
