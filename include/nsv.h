@@ -30,18 +30,27 @@
  * on the given stream unless stated otherwise.
  *
  * Layouts (all C-contiguous, no strides; element type from nsv_shape.dtype):
- *   q, out          [rows][num_heads][head_dim]
+ *   q, out          [rows][query_len][num_heads][head_dim]
  *   k_pool, v_pool  [num_blocks + 1][num_kv_heads][block_size][head_dim]
  *                   the last block (index num_blocks) is the sink block;
  *                   flat slot s is (block s / block_size, offset
  *                   s % block_size); the sink slot is num_blocks*block_size.
- *   k_new, v_new    [rows][num_kv_heads][head_dim]
- *   write_slots     [rows] int64
+ *   k_new, v_new    [rows][query_len][num_kv_heads][head_dim]
+ *   write_slots     [rows][query_len] int64
  *   block_tables    [rows][max_blocks] int32; entries at or past
  *                   cdiv(context_lens[r], block_size) are never read and may
  *                   hold anything (-1 by convention)
  *   context_lens    [rows] int32
  * Query head h reads KV head h / (num_heads / num_kv_heads).
+ *
+ * Several query tokens per row (query_len > 1, e.g. verifying speculative
+ * tokens): the step appends query_len tokens per row and query token j of a
+ * row of length ctx (which counts them) sits at position ctx - query_len + j
+ * and sees the positions t < ctx - query_len + 1 + j.  This is the multi-
+ * token form of the streaming loop that Day 59 "What I learned" item 3
+ * describes (the single-sequence kernel's [n_q, d] accumulators), read as
+ * causal among the step's new tokens; a query that sees no position outputs
+ * 0.  query_len 1 is the decode read.
  * Every data pointer must be 16-byte aligned.
  *
  * Errors: every entry point returns NSV_OK (0) or a negative NSV_ERR_* code
@@ -103,7 +112,9 @@ enum {
 /* Sizes of one decode batch.  Limits: 0 <= rows <= 8192; num_heads a
  * multiple of num_kv_heads with num_heads/num_kv_heads <= 16; head_dim 64 or
  * 128; block_size 16; 1 <= max_blocks with max_blocks*block_size < 2^31;
- * 1 <= num_blocks < 2^31 - 1. */
+ * 1 <= num_blocks < 2^31 - 1; query_len 0 or 1 (one query token per row) up
+ * to 32 with query_len * num_heads/num_kv_heads <= 32, and <= 16 when that
+ * product is not a multiple of 4. */
 typedef struct nsv_shape {
     int32_t rows;
     int32_t num_heads;
@@ -113,7 +124,7 @@ typedef struct nsv_shape {
     int32_t max_blocks;   /* block-table row length; width = max_blocks*block_size */
     int64_t num_blocks;   /* blocks the allocator hands out; pools hold one more */
     int32_t dtype;        /* NSV_F32 or NSV_BF16 */
-    int32_t reserved;     /* must be 0 */
+    int32_t query_len;    /* query tokens per row; 0 means 1 */
 } nsv_shape;
 
 /* Launch plan of the decode read.  A plan depends on the shape and the SM
@@ -133,7 +144,9 @@ typedef struct nsv_plan {
     int32_t threads;          /* threads per CTA */
     int32_t smem_bytes;       /* dynamic shared memory per CTA */
     int32_t num_sms;          /* SM count the plan was made for */
-    int32_t reserved;         /* 0 */
+    int32_t vectors_per_warp; /* query vectors (query heads x query tokens
+                                 that share a KV head) one consumer warp
+                                 serves from each K/V tile: 1, 2 or 4 */
     int64_t workspace_bytes;  /* device scratch the read needs */
 } nsv_plan;
 
@@ -156,13 +169,15 @@ NSV_API int nsv_plan_custom(const nsv_shape *shape, int num_sms, int kv_heads_pe
                             int stages, int ctas_per_sm, int grid, nsv_plan *plan);
 
 /*
- * KV append: for every row r, k_pool/v_pool at slot write_slots[r] receive
- * k_new[r]/v_new[r] (all KV heads), bit for bit.  Real rows' slots must be
+ * KV append: for every row r (and each of its query_len new tokens j),
+ * k_pool/v_pool at slot write_slots[r][j] receive k_new[r][j]/v_new[r][j]
+ * (all KV heads), bit for bit.  Real rows' slots must be
  * distinct; any number of padded rows may name the sink slot, whose contents
  * are then unspecified.  Pool bytes at every other slot are untouched.
  * A slot outside [0, (num_blocks+1)*block_size) is skipped and sets
- * NSV_DEV_BAD_SLOT.  Uses shape.rows, num_kv_heads, head_dim, block_size,
- * num_blocks, dtype (num_heads and max_blocks must still be valid).
+ * NSV_DEV_BAD_SLOT.  Uses shape.rows, query_len, num_kv_heads, head_dim,
+ * block_size, num_blocks, dtype (num_heads and max_blocks must still be
+ * valid).
  */
 NSV_API int nsv_kv_write(const nsv_shape *shape, const void *k_new, const void *v_new,
                          const int64_t *write_slots, void *k_pool, void *v_pool,

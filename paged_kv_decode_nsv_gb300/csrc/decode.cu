@@ -194,8 +194,9 @@ __device__ __forceinline__ int cta_of(long long u, long long U, int G) {
   return (int)(c < G - 1 ? c : G - 1);
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodeParams p) {
+template <typename T, int D, int QW>
+__global__ void __launch_bounds__(QW == 1 ? kMaxThreads : kMaxThreadsMulti, 1)
+    decode_kernel(const DecodeParams p) {
   using E = Elem<T>;
   constexpr int kDpl = E::kDpl;           // dims per lane per 16-byte load
   constexpr int kLpt = D / kDpl;          // lanes per token row
@@ -207,10 +208,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
 
   extern __shared__ __align__(128) unsigned char smem[];
   const int G = p.group;
+  const int NQ = p.query_len;
   const int HG = p.heads_per_cta;
-  const int ncw = HG * G;
+  const int nvec = HG * G * NQ;          // query vectors per CTA
+  const int ncw = nvec / QW;             // consumer warps
   const int S = p.stages;
-  const SmemLayout L = make_layout((int)sizeof(T), D, HG, G, S, p.rows);
+  const SmemLayout L = make_layout((int)sizeof(T), D, HG, nvec, S, p.rows);
 
   int4* s_meta = reinterpret_cast<int4*>(smem + L.off_meta);
   const uint32_t bars = smem_u32(smem + L.off_bars);  // full[s] at +8s, empty[s] at +8(S+s)
@@ -270,6 +273,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
     const T* kp = static_cast<const T*>(p.k_pool);
     const T* vp = static_cast<const T*>(p.v_pool);
     const T* qp = static_cast<const T*>(p.q);
+    const uint32_t q_slice = L.q_bytes / NQ;   // one query token's heads of the group
     const int slot0 = blockIdx.x * 2;
     unsigned long long walked = 0;
     uint32_t n = 0;  // fills issued (meaningful in lane 0)
@@ -287,7 +291,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
       const int j = rb - s_prefix[lo];
       const int nb = s_prefix[lo + 1] - s_prefix[lo];
       const long long rs = (long long)hg * N + s_prefix[lo];  // the row's first unit
-      int f = min(kBlock, s_ctx[lo] - j * kBlock) | ((hg * HG) << 16);
+      // low byte: positions of the row from this block on (clipped at 255)
+      int f = min(255, s_ctx[lo] - j * kBlock) | ((hg * HG) << 16);
       if (u == beg || j == 0) f |= kFirst | kHasQ;
       if (u == end - 1 || j == nb - 1) f |= kLast;
       if (rs >= beg && rs + nb <= end) f |= kFinal;
@@ -323,8 +328,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
           bulk_g2s(base + L.kv_bytes, vp + off, L.kv_bytes, full, pol);
         }
         if (flags & kHasQ) {
-          bulk_g2s(base + 2 * L.kv_bytes, qp + ((size_t)row * p.heads + qh0) * D, L.q_bytes,
-                   full, pol);
+          for (int jq = 0; jq < NQ; ++jq)
+            bulk_g2s(base + 2 * L.kv_bytes + jq * q_slice,
+                     qp + (((size_t)row * NQ + jq) * p.heads + qh0) * D, q_slice, full, pol);
         }
       }
       ++n;
@@ -374,30 +380,48 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
   }
 
   // -------------------------------------------------------------------- consumers
+  // A consumer warp serves QW query vectors that read the same KV head: the
+  // group's query heads of that KV head and the row's query tokens, so each
+  // K/V tile is loaded and widened once for all of them.  Vector v of the CTA
+  // is (KV head v / (G*NQ), query head (v / NQ) % G, query token v % NQ).
   if (warp > ncw) return;
-  const int cw = warp - 1;            // query head within the CTA's group
-  const int kvl = cw / G;             // KV head within the CTA's group
+  const int cw = warp - 1;
+  const int vpk = G * NQ;
+  const int v0 = cw * QW;
+  const int kvl = v0 / vpk;           // KV head within the group
   const int sub = lane % kLpt;        // which 16-byte slice of a token row
   const int grp = lane / kLpt;        // which token of a warp-wide load
   const int tok = (sub / kDup) * kTpi + grp;  // token whose score this lane ends with
-  float* pbuf = s_pbuf + cw * kBlock;
-
+  const int hq = HG * G;              // query heads per group
+  float* pbuf = s_pbuf + (size_t)v0 * kBlock;
   volatile int* s_merge = s_abort + 1;
 
-  // Empty rows attend over nothing: their output is zero.  CTA c writes the
-  // empty rows c, c + G, ...; its consumer warps share the heads.
+  int qhl[QW], jq[QW];                // query head within the group, query token
+#pragma unroll
+  for (int k = 0; k < QW; ++k) {
+    const int rem = v0 + k - kvl * vpk;
+    qhl[k] = kvl * G + rem / NQ;
+    jq[k] = rem % NQ;
+  }
+
+  // Empty rows see nothing: their output is zero.  CTA c writes the empty
+  // rows c, c + G, ...; its consumer warps share the (token, head) vectors.
   for (int r = blockIdx.x; r < p.rows; r += gridDim.x) {
     if (s_prefix[r + 1] != s_prefix[r]) continue;
-    for (int h = cw; h < p.heads; h += ncw)
+    for (int vh = cw; vh < NQ * p.heads; vh += ncw)
       if (lane < kLpt)
-        *reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)r * p.heads + h) * D +
+        *reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)r * NQ * p.heads + vh) * D +
                                   sub * kDpl) = make_uint4(0u, 0u, 0u, 0u);
   }
 
-  float qv[kDpl], acc[kDpl];
-  float m = -INFINITY, l = 0.f;
+  float qv[QW][kDpl], acc[QW][kDpl], m[QW], l[QW];
 #pragma unroll
-  for (int e = 0; e < kDpl; ++e) { qv[e] = 0.f; acc[e] = 0.f; }
+  for (int k = 0; k < QW; ++k) {
+    m[k] = -INFINITY;
+    l[k] = 0.f;
+#pragma unroll
+    for (int e = 0; e < kDpl; ++e) { qv[k][e] = 0.f; acc[k][e] = 0.f; }
+  }
 
   for (uint32_t n = 0;; ++n) {
     const uint32_t s = n % S;
@@ -412,72 +436,89 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
     const unsigned char* st = smem + s * L.stage_bytes;
 
     if (flags & kFirst) {
-      m = -INFINITY;
-      l = 0.f;
 #pragma unroll
-      for (int e = 0; e < kDpl; ++e) acc[e] = 0.f;
-      if (flags & kHasQ) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(st + 2 * L.kv_bytes +
-                                                          ((size_t)cw * D + sub * kDpl) * sizeof(T));
-        E::widen(raw, qv);
+      for (int k = 0; k < QW; ++k) {
+        m[k] = -INFINITY;
+        l[k] = 0.f;
 #pragma unroll
-        for (int e = 0; e < kDpl; ++e) qv[e] *= p.qscale;
+        for (int e = 0; e < kDpl; ++e) acc[k][e] = 0.f;
+        if (flags & kHasQ) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(
+              st + 2 * L.kv_bytes +
+              (((size_t)jq[k] * hq + qhl[k]) * D + sub * kDpl) * sizeof(T));
+          E::widen(raw, qv[k]);
+#pragma unroll
+          for (int e = 0; e < kDpl; ++e) qv[k][e] *= p.qscale;
+        }
       }
     }
 
     if (flags & kData) {
-      const int nvalid = flags & 0xff;
+      const int rem = flags & 0xff;             // the row's positions from this block on
+      const int nvalid = min(kBlock, rem);      // what the last query token sees
       const unsigned char* kt = st + (size_t)kvl * kBlock * D * sizeof(T);
       const unsigned char* vt = kt + L.kv_bytes;
-      // scores: partial dot products of this lane's 16-byte slice
-      float part[kNp];
+      // scores: partial dot products of this lane's 16-byte slice, one
+      // widening of the key slice for all QW vectors
+      float part[QW][kNp];
 #pragma unroll
       for (int i = 0; i < kNp; ++i) {
         const int t = i * kTpi + grp;
         const uint4 raw =
             *reinterpret_cast<const uint4*>(kt + ((size_t)t * D + sub * kDpl) * sizeof(T));
-        float k[kDpl];
-        E::widen(raw, k);
-        float a = 0.f;
+        float kk[kDpl];
+        E::widen(raw, kk);
 #pragma unroll
-        for (int e = 0; e < kDpl; ++e) a = fmaf(qv[e], k[e], a);
-        part[i] = a;
-      }
-      // transposing butterfly: afterwards this lane holds token `tok`'s sum
+        for (int k = 0; k < QW; ++k) {
+          float a = 0.f;
 #pragma unroll
-      for (int stp = 0, cnt = kNp; cnt > 1; ++stp, cnt >>= 1) {
-        const int o = kLpt >> (stp + 1);
-        const bool upper = (sub & o) != 0;
-        const int half = cnt >> 1;
-#pragma unroll
-        for (int j = 0; j < half; ++j) {
-          const float send = upper ? part[j] : part[j + half];
-          const float keep = upper ? part[j + half] : part[j];
-          part[j] = keep + __shfl_xor_sync(kFull, send, o);
+          for (int e = 0; e < kDpl; ++e) a = fmaf(qv[k][e], kk[e], a);
+          part[k][i] = a;
         }
       }
-      float sc = part[0];
 #pragma unroll
-      for (int o = kDup >> 1; o >= 1; o >>= 1) sc += __shfl_xor_sync(kFull, sc, o);
-      sc = (tok < nvalid) ? sc : -INFINITY;
-      float mx = sc;
+      for (int k = 0; k < QW; ++k) {
+        // transposing butterfly: afterwards this lane holds token `tok`'s sum
 #pragma unroll
-      for (int o = kDup; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-      if (mx > m) {  // warp-uniform
-        const float alpha = exp2f(m - mx);
-        l *= alpha;
+        for (int stp = 0, cnt = kNp; cnt > 1; ++stp, cnt >>= 1) {
+          const int o = kLpt >> (stp + 1);
+          const bool upper = (sub & o) != 0;
+          const int half = cnt >> 1;
 #pragma unroll
-        for (int e = 0; e < kDpl; ++e) acc[e] *= alpha;
-        m = mx;
+          for (int j = 0; j < half; ++j) {
+            const float send = upper ? part[k][j] : part[k][j + half];
+            const float keep = upper ? part[k][j + half] : part[k][j];
+            part[k][j] = keep + __shfl_xor_sync(kFull, send, o);
+          }
+        }
+        float sc = part[k][0];
+#pragma unroll
+        for (int o = kDup >> 1; o >= 1; o >>= 1) sc += __shfl_xor_sync(kFull, sc, o);
+        // this vector sees the row's positions before ctx - (NQ - 1 - jq)
+        const int nv = rem - (NQ - 1 - jq[k]);
+        sc = (tok < nv) ? sc : -INFINITY;
+        float mx = sc;
+#pragma unroll
+        for (int o = kDup; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+        if (mx > m[k]) {  // warp-uniform
+          const float alpha = exp2f(m[k] - mx);
+          l[k] *= alpha;
+#pragma unroll
+          for (int e = 0; e < kDpl; ++e) acc[k][e] *= alpha;
+          m[k] = mx;
+        }
+        const float pr = (sc == -INFINITY) ? 0.f : exp2f(sc - m[k]);
+        if ((sub % kDup) == 0) pbuf[k * kBlock + grp * kNp + sub / kDup] = pr;
       }
-      const float pr = exp2f(sc - m);
-      if ((sub % kDup) == 0) pbuf[grp * kNp + sub / kDup] = pr;
       __syncwarp();
-      float pv[kNp];
+      float pv[QW][kNp];
 #pragma unroll
-      for (int i = 0; i < kNp; i += 4) {
-        const float4 f = *reinterpret_cast<const float4*>(pbuf + grp * kNp + i);
-        pv[i] = f.x; pv[i + 1] = f.y; pv[i + 2] = f.z; pv[i + 3] = f.w;
+      for (int k = 0; k < QW; ++k) {
+#pragma unroll
+        for (int i = 0; i < kNp; i += 4) {
+          const float4 f = *reinterpret_cast<const float4*>(pbuf + k * kBlock + grp * kNp + i);
+          pv[k][i] = f.x; pv[k][i + 1] = f.y; pv[k][i + 2] = f.z; pv[k][i + 3] = f.w;
+        }
       }
 #pragma unroll
       for (int i = 0; i < kNp; ++i) {
@@ -488,41 +529,55 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
           float v[kDpl];
           E::widen(raw, v);
 #pragma unroll
-          for (int e = 0; e < kDpl; ++e) acc[e] = fmaf(pv[i], v[e], acc[e]);
-          l += pv[i];
+          for (int k = 0; k < QW; ++k) {
+#pragma unroll
+            for (int e = 0; e < kDpl; ++e) acc[k][e] = fmaf(pv[k][i], v[e], acc[k][e]);
+            l[k] += pv[k][i];
+          }
         }
       }
     }
 
     if (flags & kLast) {
-      float lt = l;
-      float at[kDpl];
+      const int row = meta.x;
+      float lt[QW], at[QW][kDpl];
 #pragma unroll
-      for (int e = 0; e < kDpl; ++e) at[e] = acc[e];
+      for (int k = 0; k < QW; ++k) {
+        lt[k] = l[k];
 #pragma unroll
-      for (int o = kLpt; o < 32; o <<= 1) {
-        lt += __shfl_xor_sync(kFull, lt, o);
+        for (int e = 0; e < kDpl; ++e) at[k][e] = acc[k][e];
 #pragma unroll
-        for (int e = 0; e < kDpl; ++e) at[e] += __shfl_xor_sync(kFull, at[e], o);
+        for (int o = kLpt; o < 32; o <<= 1) {
+          lt[k] += __shfl_xor_sync(kFull, lt[k], o);
+#pragma unroll
+          for (int e = 0; e < kDpl; ++e) at[k][e] += __shfl_xor_sync(kFull, at[k][e], o);
+        }
       }
-      const int row = meta.x, qh = meta.y + cw;
       if (flags & kFinal) {
-        if (lane < kLpt) {
-          const float inv = lt > 0.f ? 1.f / lt : 0.f;
 #pragma unroll
-          for (int e = 0; e < kDpl; ++e) at[e] *= inv;
-          T* o = static_cast<T*>(p.out) + ((size_t)row * p.heads + qh) * D + sub * kDpl;
-          *reinterpret_cast<uint4*>(o) = E::narrow(at);
+        for (int k = 0; k < QW; ++k) {
+          if (lane < kLpt) {
+            const float inv = lt[k] > 0.f ? 1.f / lt[k] : 0.f;
+#pragma unroll
+            for (int e = 0; e < kDpl; ++e) at[k][e] *= inv;
+            T* o = static_cast<T*>(p.out) +
+                   (((size_t)row * NQ + jq[k]) * p.heads + meta.y + qhl[k]) * D + sub * kDpl;
+            *reinterpret_cast<uint4*>(o) = E::narrow(at[k]);
+          }
         }
       } else {
-        const size_t slot = (size_t)meta.z * ncw + cw;
-        if (lane < kLpt) {
-          float* a = p.ws_acc + slot * D + sub * kDpl;
 #pragma unroll
-          for (int e = 0; e < kDpl; e += 4)
-            *reinterpret_cast<float4*>(a + e) = make_float4(at[e], at[e + 1], at[e + 2], at[e + 3]);
+        for (int k = 0; k < QW; ++k) {
+          const size_t slot = (size_t)meta.z * nvec + v0 + k;
+          if (lane < kLpt) {
+            float* a = p.ws_acc + slot * D + sub * kDpl;
+#pragma unroll
+            for (int e = 0; e < kDpl; e += 4)
+              *reinterpret_cast<float4*>(a + e) =
+                  make_float4(at[k][e], at[k][e + 1], at[k][e + 2], at[k][e + 3]);
+          }
+          if (lane == 0) p.ws_ml[slot] = make_float2(m[k], lt[k]);
         }
-        if (lane == 0) p.ws_ml[slot] = make_float2(m, lt);
         // Publish this CTA's piece of the row and count it.
         __threadfence();
         consumer_sync(ncw * 32);
@@ -546,58 +601,62 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
         consumer_sync(ncw * 32);
         if (*s_merge) {
           // The last piece to arrive merges all pieces of the row for the
-          // warp's query head.  Lane l owns dims [l*D/32, (l+1)*D/32).
+          // warp's vectors.  Lane l owns dims [l*D/32, (l+1)*D/32).
           __threadfence();
           constexpr int kPer = D / 32;
           const int ns = c1 - c0 + 1;
-          float M = -INFINITY;
-          for (int k = lane; k < ns; k += 32) {
-            const int c = c0 + k;
-            const long long sc = (long long)c * U / gridDim.x;
-            if ((long long)(c + 1) * U / gridDim.x == sc) continue;  // CTA with no units
-            const int sl = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
-            M = fmaxf(M, __ldcg(&p.ws_ml[(size_t)sl * ncw + cw]).x);
-          }
-#pragma unroll
-          for (int o2 = 16; o2 >= 1; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
-          float Lsum = 0.f, a[kPer];
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) a[e] = 0.f;
-          for (int base = 0; base < ns; base += 32) {
-            const int c = c0 + base + lane;
-            float w = 0.f;
-            int idx = 0;
-            if (base + lane < ns) {
+          for (int k = 0; k < QW; ++k) {
+            const int vv = v0 + k;
+            float M = -INFINITY;
+            for (int kk = lane; kk < ns; kk += 32) {
+              const int c = c0 + kk;
               const long long sc = (long long)c * U / gridDim.x;
-              if ((long long)(c + 1) * U / gridDim.x != sc) {
-                const int sl = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
-                idx = sl * ncw + cw;
-                const float2 ml = __ldcg(&p.ws_ml[idx]);
-                w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-                Lsum = fmaf(w, ml.y, Lsum);
+              if ((long long)(c + 1) * U / gridDim.x == sc) continue;  // CTA with no units
+              const int sl = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
+              M = fmaxf(M, __ldcg(&p.ws_ml[(size_t)sl * nvec + vv]).x);
+            }
+#pragma unroll
+            for (int o2 = 16; o2 >= 1; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
+            float Lsum = 0.f, a[kPer];
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) a[e] = 0.f;
+            for (int base = 0; base < ns; base += 32) {
+              const int c = c0 + base + lane;
+              float w = 0.f;
+              int idx = 0;
+              if (base + lane < ns) {
+                const long long sc = (long long)c * U / gridDim.x;
+                if ((long long)(c + 1) * U / gridDim.x != sc) {
+                  const int sl = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
+                  idx = sl * nvec + vv;
+                  const float2 ml = __ldcg(&p.ws_ml[idx]);
+                  w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+                  Lsum = fmaf(w, ml.y, Lsum);
+                }
+              }
+              const int cnt = min(32, ns - base);
+              for (int kk = 0; kk < cnt; ++kk) {
+                const float wk = __shfl_sync(kFull, w, kk);
+                const int ik = __shfl_sync(kFull, idx, kk);
+                if (wk != 0.f) {
+                  const float* src = p.ws_acc + (size_t)ik * D + lane * kPer;
+#pragma unroll
+                  for (int e = 0; e < kPer; ++e) a[e] = fmaf(wk, __ldcg(src + e), a[e]);
+                }
               }
             }
-            const int cnt = min(32, ns - base);
-            for (int k = 0; k < cnt; ++k) {
-              const float wk = __shfl_sync(kFull, w, k);
-              const int ik = __shfl_sync(kFull, idx, k);
-              if (wk != 0.f) {
-                const float* src = p.ws_acc + (size_t)ik * D + lane * kPer;
 #pragma unroll
-                for (int e = 0; e < kPer; ++e) a[e] = fmaf(wk, __ldcg(src + e), a[e]);
+            for (int o2 = 16; o2 >= 1; o2 >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, o2);
+            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+            T* o = static_cast<T*>(p.out) +
+                   (((size_t)row * NQ + jq[k]) * p.heads + meta.y + qhl[k]) * D + lane * kPer;
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) {
+              if constexpr (sizeof(T) == 4) {
+                o[e] = a[e] * inv;
+              } else {
+                o[e] = __float2bfloat16_rn(a[e] * inv);
               }
-            }
-          }
-#pragma unroll
-          for (int o2 = 16; o2 >= 1; o2 >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, o2);
-          const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-          T* o = static_cast<T*>(p.out) + ((size_t)row * p.heads + qh) * D + lane * kPer;
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) {
-            if constexpr (sizeof(T) == 4) {
-              o[e] = a[e] * inv;
-            } else {
-              o[e] = __float2bfloat16_rn(a[e] * inv);
             }
           }
         }
@@ -608,10 +667,29 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_kernel(const DecodePara
   }
 }
 
+template <typename T, int D, int QW>
+cudaError_t set_attr() {
+  return cudaFuncSetAttribute(decode_kernel<T, D, QW>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+}
+
 template <typename T, int D>
 cudaError_t set_attrs() {
-  return cudaFuncSetAttribute(decode_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              227 * 1024);
+  cudaError_t e;
+  if ((e = set_attr<T, D, 1>()) != cudaSuccess) return e;
+  if ((e = set_attr<T, D, 2>()) != cudaSuccess) return e;
+  return set_attr<T, D, 4>();
+}
+
+template <typename T, int D>
+void launch_typed(const DecodeParams& p, int qw, int grid, int threads, int smem,
+                  cudaStream_t stream) {
+  if (qw == 4)
+    decode_kernel<T, D, 4><<<grid, threads, smem, stream>>>(p);
+  else if (qw == 2)
+    decode_kernel<T, D, 2><<<grid, threads, smem, stream>>>(p);
+  else
+    decode_kernel<T, D, 1><<<grid, threads, smem, stream>>>(p);
 }
 
 }  // namespace
@@ -624,18 +702,18 @@ cudaError_t prepare_decode_kernels() {
   return set_attrs<__nv_bfloat16, 128>();
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int grid, int threads,
-                          int smem, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int qw, int grid,
+                          int threads, int smem, cudaStream_t stream) {
   if (dtype == NSV_F32) {
     if (head_dim == 64)
-      decode_kernel<float, 64><<<grid, threads, smem, stream>>>(p);
+      launch_typed<float, 64>(p, qw, grid, threads, smem, stream);
     else
-      decode_kernel<float, 128><<<grid, threads, smem, stream>>>(p);
+      launch_typed<float, 128>(p, qw, grid, threads, smem, stream);
   } else {
     if (head_dim == 64)
-      decode_kernel<__nv_bfloat16, 64><<<grid, threads, smem, stream>>>(p);
+      launch_typed<__nv_bfloat16, 64>(p, qw, grid, threads, smem, stream);
     else
-      decode_kernel<__nv_bfloat16, 128><<<grid, threads, smem, stream>>>(p);
+      launch_typed<__nv_bfloat16, 128>(p, qw, grid, threads, smem, stream);
   }
   return cudaGetLastError();
 }

@@ -65,16 +65,21 @@ int device_state(DeviceState** out) {
 
 int elem_bytes(int dtype) { return dtype == NSV_F32 ? 4 : 2; }
 
+int query_len(const nsv_shape* s) { return s->query_len > 0 ? s->query_len : 1; }
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_shape(const nsv_shape* s) {
   if (!s) return NSV_ERR_NULLPTR;
   if (s->dtype != NSV_F32 && s->dtype != NSV_BF16) return NSV_ERR_DTYPE;
-  if (s->reserved != 0) return NSV_ERR_SHAPE;
+  if (s->query_len < 0 || s->query_len > kMaxVectorsPerKvHead) return NSV_ERR_SHAPE;
   if (s->rows < 0 || s->rows > kMaxRows) return NSV_ERR_SHAPE;
   if (s->num_heads < 1 || s->num_kv_heads < 1 || s->num_heads % s->num_kv_heads != 0)
     return NSV_ERR_SHAPE;
   if (s->num_heads / s->num_kv_heads > kMaxConsumerWarps) return NSV_ERR_SHAPE;
+  if ((s->num_heads / s->num_kv_heads) * (s->query_len > 0 ? s->query_len : 1) >
+      kMaxVectorsPerKvHead)
+    return NSV_ERR_SHAPE;
   if (s->head_dim != 64 && s->head_dim != 128) return NSV_ERR_UNSUPPORTED;
   if (s->block_size != kBlock) return NSV_ERR_UNSUPPORTED;
   if (s->max_blocks < 1 || (int64_t)s->max_blocks * s->block_size >= (int64_t(1) << 31))
@@ -95,32 +100,38 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   }
   const int elem = elem_bytes(s->dtype);
   const int G = s->num_heads / s->num_kv_heads;
+  const int vpk = G * query_len(s);                // query vectors per KV head
+  const int qw = vpk % 4 == 0 ? 4 : (vpk % 2 == 0 ? 2 : 1);  // vectors per warp
+  const int wpk = vpk / qw;                        // consumer warps per KV head
+  const int max_warps = qw == 1 ? kMaxConsumerWarps : kMaxConsumerWarpsMulti;
+  if (wpk > max_warps) return NSV_ERR_SHAPE;
   const int tile = kBlock * s->head_dim * elem;
   if (hg <= 0) {
     // Largest KV-head group whose K+V stage stays within 64 KiB and whose
-    // query heads fill at most 8 consumer warps: big bulk copies, few CTAs.
+    // query vectors fill at most 8 consumer warps: big bulk copies, few CTAs.
     hg = 1;
     const int cands[4] = {8, 4, 2, 1};
     for (int c : cands) {
-      if (s->num_kv_heads % c == 0 && c * G <= 8 && 2 * c * tile <= 64 * 1024) {
+      if (s->num_kv_heads % c == 0 && c * wpk <= 8 && 2 * c * tile <= 64 * 1024) {
         hg = c;
         break;
       }
     }
-  } else if (s->num_kv_heads % hg != 0 || hg * G > kMaxConsumerWarps) {
+  } else if (s->num_kv_heads % hg != 0 || hg * wpk > max_warps) {
     return NSV_ERR_RANGE;
   }
+  const int nvec = hg * vpk;
   const int rows_for_layout = s->rows > 0 ? s->rows : 1;
   const bool auto_stages = stages <= 0;
   if (auto_stages) stages = 3;
   if (stages < 2 || stages > 8) return NSV_ERR_RANGE;
-  SmemLayout L = make_layout(elem, s->head_dim, hg, G, stages, rows_for_layout);
+  SmemLayout L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout);
   while (auto_stages && L.total > (uint32_t)kSmemPerCta && stages > 2) {
     --stages;
-    L = make_layout(elem, s->head_dim, hg, G, stages, rows_for_layout);
+    L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout);
   }
   if (L.total > (uint32_t)kSmemPerCta) return NSV_ERR_RANGE;
-  const int threads = (hg * G + 1) * 32;
+  const int threads = (hg * wpk + 1) * 32;
   const int fit = kSmemPerSm / (int)(L.total + kSmemReserved);
   const int fit_threads = kThreadsPerSm / threads;
   if (cps <= 0) {
@@ -136,7 +147,7 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
     return NSV_ERR_RANGE;
   }
   const WsLayout W =
-      make_ws_layout(rows_for_layout, s->num_kv_heads / hg, grid, hg * G, s->head_dim);
+      make_ws_layout(rows_for_layout, s->num_kv_heads / hg, grid, nvec, s->head_dim);
   memset(p, 0, sizeof(*p));
   p->kv_heads_per_cta = hg;
   p->stages = stages;
@@ -145,6 +156,7 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   p->threads = threads;
   p->smem_bytes = (int)L.total;
   p->num_sms = num_sms;
+  p->vectors_per_warp = qw;
   p->workspace_bytes = (int64_t)W.total;
   return NSV_OK;
 }
@@ -199,9 +211,9 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   if (!ws || ws_bytes < (size_t)plan.workspace_bytes ||
       (reinterpret_cast<uintptr_t>(ws) & 255u))
     return NSV_ERR_WORKSPACE;
+  const int nvec = plan.kv_heads_per_cta * (s->num_heads / s->num_kv_heads) * query_len(s);
   const WsLayout W = make_ws_layout(s->rows, s->num_kv_heads / plan.kv_heads_per_cta, plan.grid,
-                                    plan.kv_heads_per_cta * (s->num_heads / s->num_kv_heads),
-                                    s->head_dim);
+                                    nvec, s->head_dim);
   char* wsb = static_cast<char*>(ws);
   // The arrival counters of cut rows start every call at zero.
   if (cudaMemsetAsync(wsb, 0, W.cnt_bytes, stream) != cudaSuccess) return cuda_fail();
@@ -224,10 +236,11 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   p.max_blocks = s->max_blocks;
   p.heads_per_cta = plan.kv_heads_per_cta;
   p.group = s->num_heads / s->num_kv_heads;
+  p.query_len = query_len(s);
   p.stages = plan.stages;
   p.qscale = scale * 1.4426950408889634f;  // log2(e): the kernels use exp2
-  if (launch_decode(p, s->dtype, s->head_dim, plan.grid, plan.threads, plan.smem_bytes, stream) !=
-      cudaSuccess)
+  if (launch_decode(p, s->dtype, s->head_dim, plan.vectors_per_warp, plan.grid, plan.threads,
+                    plan.smem_bytes, stream) != cudaSuccess)
     return cuda_fail();
   return NSV_OK;
 }
@@ -286,7 +299,7 @@ NSV_API int nsv_kv_write(const nsv_shape* s, const void* k_new, const void* v_ne
   p.v_pool = v_pool;
   p.status = d->status;
   p.pool_slots = (s->num_blocks + 1) * (long long)s->block_size;
-  p.rows = s->rows;
+  p.rows = s->rows * query_len(s);  // every new token of every row
   p.kv_heads = s->num_kv_heads;
   p.vec_per_head = s->head_dim * elem_bytes(s->dtype) / 16;
   p.block_size = s->block_size;

@@ -12,15 +12,21 @@ namespace nsv {
 
 // The kernels are built for this block size (the pages' 16-token blocks).
 constexpr int kBlock = 16;
-// Largest number of consumer warps (query heads) one decode CTA serves.
+// Largest number of consumer warps one decode CTA runs: 16 when each warp
+// serves one query vector, 8 when it serves 2 or 4 (their registers).
 constexpr int kMaxConsumerWarps = 16;
+constexpr int kMaxConsumerWarpsMulti = 8;
+// Largest number of query vectors (query heads x query tokens) that share
+// one KV head.
+constexpr int kMaxVectorsPerKvHead = 32;
 constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
+constexpr int kMaxThreadsMulti = (kMaxConsumerWarpsMulti + 1) * 32;
 // Largest batch the decode kernel's per-CTA row tables hold.
 constexpr int kMaxRows = 8192;
 
 // Stage flags written by the producer warp for the consumers.  The low 8
-// bits of a stage's flag word carry the number of valid tokens of its block
-// and bits 16 and up the first KV head of the head group.
+// bits of a stage's flag word carry the row's positions from the block on
+// (clipped at 255) and bits 16 and up the first KV head of the head group.
 enum : int {
   kFirst = 1 << 8,   // first block of a segment: reset the softmax state
   kLast = 1 << 9,    // last block of a segment: write out or the partial
@@ -34,18 +40,18 @@ enum : int {
 // Workspace of one decode read (all offsets 256-byte aligned):
 //   cnt     int32 [rows][head groups]  pieces of a cut row that have
 //           finished; zeroed on the stream before every launch
-//   ml      float2 [grid][2][cw]  (running max, denominator) of partials
-//   acc     float [grid][2][cw][head_dim]
-// where cw = query heads per CTA.  Each CTA has at most two partial
+//   ml      float2 [grid][2][nvec]  (running max, denominator) of partials
+//   acc     float [grid][2][nvec][head_dim]
+// where nvec = query vectors per CTA.  Each CTA has at most two partial
 // segments: the row its range starts inside of and the row it ends inside of.
 struct WsLayout {
   uint64_t cnt_bytes, off_ml, off_acc, total;
 };
 
-__host__ __device__ inline WsLayout make_ws_layout(int rows, int head_groups, int grid, int cw,
-                                                   int head_dim) {
+__host__ __device__ inline WsLayout make_ws_layout(int rows, int head_groups, int grid,
+                                                   int nvec, int head_dim) {
   WsLayout W;
-  const uint64_t slots = (uint64_t)grid * 2 * cw;
+  const uint64_t slots = (uint64_t)grid * 2 * nvec;
   W.cnt_bytes = (uint64_t)rows * head_groups * 4;
   W.off_ml = (W.cnt_bytes + 255) / 256 * 256;
   W.off_acc = W.off_ml + (slots * 8 + 255) / 256 * 256;
@@ -69,6 +75,7 @@ struct DecodeParams {
   int rows, heads, kv_heads, max_blocks;
   int heads_per_cta;  // KV heads per CTA
   int group;          // query heads per KV head
+  int query_len;      // query tokens per row
   int stages;
   float qscale;       // scale * log2(e)
 };
@@ -92,7 +99,7 @@ struct SmemLayout {
   uint32_t stage_bytes;  // K + V + q, rounded to 128
   uint32_t off_meta;     // int4 per stage
   uint32_t off_bars;     // full[stages], empty[stages] mbarriers
-  uint32_t off_pbuf;     // per consumer warp: block-size floats
+  uint32_t off_pbuf;     // per query vector: block-size floats
   uint32_t off_ctx;      // rows ints (validated context lengths)
   uint32_t off_prefix;   // rows + 1 ints (work-item prefix sums)
   uint32_t off_flag;     // abort flag, then the merge flag
@@ -104,11 +111,10 @@ __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) {
 }
 
 __host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int heads_per_cta,
-                                                  int group, int stages, int rows) {
+                                                  int nvec, int stages, int rows) {
   SmemLayout L;
-  const int cw = heads_per_cta * group;
   L.kv_bytes = (uint32_t)(heads_per_cta * kBlock * head_dim * elem);
-  L.q_bytes = (uint32_t)(cw * head_dim * elem);
+  L.q_bytes = (uint32_t)(nvec * head_dim * elem);
   L.stage_bytes = align_up(2 * L.kv_bytes + L.q_bytes, 128);
   uint32_t off = (uint32_t)stages * L.stage_bytes;
   L.off_meta = off;
@@ -116,7 +122,7 @@ __host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int he
   L.off_bars = align_up(off, 8);
   off = L.off_bars + (uint32_t)stages * 16;
   L.off_pbuf = align_up(off, 16);
-  off = L.off_pbuf + (uint32_t)(cw * kBlock * 4);
+  off = L.off_pbuf + (uint32_t)(nvec * kBlock * 4);
   L.off_ctx = off;
   off += (uint32_t)rows * 4;
   L.off_prefix = off;
@@ -128,7 +134,7 @@ __host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int he
 }
 
 // Launchers (return the launch's cudaError_t).
-cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int grid,
+cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int qw, int grid,
                           int threads, int smem, cudaStream_t stream);
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
 // One-time per-device attribute set-up of the decode kernels.

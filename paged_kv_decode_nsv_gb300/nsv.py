@@ -5,9 +5,11 @@ runs in the library's CUDA kernels.  Tensors are torch tensors on the current
 CUDA device, C-contiguous, in the layouts nsv.h documents:
 
   q, out          [rows, num_heads, head_dim]               float32 | bfloat16
+                  or [rows, query_len, num_heads, head_dim] (several query
+                  tokens per row, causal among themselves)
   k_pool, v_pool  [num_blocks + 1, num_kv_heads, 16, head_dim]  (last = sink)
-  k_new, v_new    [rows, num_kv_heads, head_dim]
-  write_slots     [rows] int64
+  k_new, v_new    [rows, num_kv_heads, head_dim] or [rows, query_len, ...]
+  write_slots     [rows] or [rows, query_len] int64
   block_tables    [rows, max_blocks] int32
   context_lens    [rows] int32
 
@@ -40,14 +42,14 @@ class Shape(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int64), ("dtype", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("query_len", ctypes.c_int32)]
 
 
 class Plan(ctypes.Structure):
     _fields_ = [("kv_heads_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
-                ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("num_sms", ctypes.c_int32), ("vectors_per_warp", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self):
@@ -106,9 +108,9 @@ def strerror(code):
 
 
 def make_shape(rows, num_heads, num_kv_heads, head_dim, max_blocks, num_blocks, dtype,
-               block_size=16):
+               block_size=16, query_len=1):
     return Shape(rows, num_heads, num_kv_heads, head_dim, block_size, max_blocks, num_blocks,
-                 dtype, 0)
+                 dtype, query_len)
 
 
 def _dtype_code(t):
@@ -131,8 +133,11 @@ def _ptr(t, what):
 
 
 def shape_of(q, k_pool, block_tables):
-    """nsv_shape from the read's tensors."""
-    R, H, D = q.shape
+    """nsv_shape from the read's tensors (q is [R, H, D] or [R, NQ, H, D])."""
+    if q.dim() == 4:
+        R, NQ, H, D = q.shape
+    else:
+        (R, H, D), NQ = q.shape, 1
     NB1, Hkv, B, D2 = k_pool.shape
     if D2 != D:
         raise ValueError("q head_dim %d != pool head_dim %d" % (D, D2))
@@ -140,7 +145,8 @@ def shape_of(q, k_pool, block_tables):
         raise ValueError("block_tables rows %d != q rows %d" % (block_tables.shape[0], R))
     if q.dtype != k_pool.dtype:
         raise ValueError("q and the pool must share one dtype")
-    return make_shape(R, H, Hkv, D, block_tables.shape[1], NB1 - 1, _dtype_code(k_pool), B)
+    return make_shape(R, H, Hkv, D, block_tables.shape[1], NB1 - 1, _dtype_code(k_pool), B,
+                      query_len=NQ)
 
 
 def _stream(stream):
@@ -173,6 +179,10 @@ def workspace_for(plan, device=None):
 
 
 def kv_write(k_new, v_new, write_slots, k_pool, v_pool, stream=None):
+    if k_new.dim() == 4:
+        k_new = k_new.reshape(-1, k_new.shape[2], k_new.shape[3])
+        v_new = v_new.reshape(-1, v_new.shape[2], v_new.shape[3])
+        write_slots = write_slots.reshape(-1)
     R, Hkv, D = k_new.shape
     NB1, Hkv2, B, D2 = k_pool.shape
     if (Hkv, D) != (Hkv2, D2) or k_new.dtype != k_pool.dtype or v_new.dtype != k_pool.dtype:

@@ -61,7 +61,8 @@ class Workload:
     seed: int
     context_lens: np.ndarray = field(repr=False)   # [rows] int32
     block_tables: np.ndarray = field(repr=False)   # [rows, max_blocks] int32
-    write_slots: np.ndarray = field(repr=False)    # [rows] int64
+    write_slots: np.ndarray = field(repr=False)    # [rows] (or [rows, query_len]) int64
+    query_len: int = 1                              # query tokens per row
 
     @property
     def width(self):
@@ -92,11 +93,24 @@ class Workload:
         return self.total_tokens * self.kv_heads * self.head_dim * 2 * self.elem_bytes
 
     def q_out_bytes(self):
-        return 2 * self.rows * self.heads * self.head_dim * self.elem_bytes
+        return 2 * self.rows * self.query_len * self.heads * self.head_dim * self.elem_bytes
 
     def append_bytes(self):
         """The append reads k_new, v_new and writes the same bytes into the pool."""
-        return 2 * 2 * self.rows * self.kv_heads * self.head_dim * self.elem_bytes
+        return (2 * 2 * self.rows * self.query_len * self.kv_heads * self.head_dim *
+                self.elem_bytes)
+
+    @property
+    def q_shape(self):
+        if self.query_len == 1:
+            return (self.rows, self.heads, self.head_dim)
+        return (self.rows, self.query_len, self.heads, self.head_dim)
+
+    @property
+    def new_shape(self):
+        if self.query_len == 1:
+            return (self.rows, self.kv_heads, self.head_dim)
+        return (self.rows, self.query_len, self.kv_heads, self.head_dim)
 
     def read_bytes(self):
         """Algorithmic bytes of one decode read (KV + q + out)."""
@@ -124,7 +138,7 @@ def bf16_to_f32(bits):
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def _tables(rng, lens, block_size, num_blocks, max_blocks):
+def _tables(rng, lens, block_size, num_blocks, max_blocks, query_len=1):
     """Deal a seeded permutation of the pool's blocks out to the rows."""
     nb = [(int(c) + block_size - 1) // block_size for c in lens]
     need = sum(nb)
@@ -138,30 +152,32 @@ def _tables(rng, lens, block_size, num_blocks, max_blocks):
             raise ValueError("row %d needs %d blocks > max_blocks %d" % (r, n, max_blocks))
         bt[r, :n] = perm[off:off + n]
         off += n
-    ws = np.empty(len(lens), dtype=np.int64)
+    # the step's new tokens are each row's last query_len positions
+    ws = np.empty((len(lens), query_len), dtype=np.int64)
     for r, c in enumerate(lens):
-        c = int(c)
-        if c == 0:
-            ws[r] = num_blocks * block_size
-        else:
-            ws[r] = int(bt[r, (c - 1) // block_size]) * block_size + (c - 1) % block_size
-    return bt, ws
+        for j in range(query_len):
+            t = int(c) - query_len + j
+            if t < 0:
+                ws[r, j] = num_blocks * block_size
+            else:
+                ws[r, j] = int(bt[r, t // block_size]) * block_size + t % block_size
+    return bt, (ws[:, 0].copy() if query_len == 1 else ws)
 
 
 def _make(name, seed, rows, heads, kv_heads, head_dim, block_size, max_blocks,
-          dtype, lens, num_blocks=None, free_frac=0.0, scale=None, rng=None):
+          dtype, lens, num_blocks=None, free_frac=0.0, scale=None, rng=None, query_len=1):
     rng = rng if rng is not None else np.random.default_rng(seed)
     lens = np.asarray(lens, dtype=np.int32)
     need = int(sum((int(c) + block_size - 1) // block_size for c in lens))
     if num_blocks is None:
         num_blocks = max(1, int(math.ceil(need * (1.0 + free_frac))))
-    bt, ws = _tables(rng, lens, block_size, num_blocks, max_blocks)
+    bt, ws = _tables(rng, lens, block_size, num_blocks, max_blocks, query_len)
     if scale is None:
         scale = 1.0 / math.sqrt(head_dim)
     return Workload(name=name, rows=rows, heads=heads, kv_heads=kv_heads,
                     head_dim=head_dim, block_size=block_size, max_blocks=max_blocks,
                     num_blocks=num_blocks, dtype=dtype, scale=scale, seed=seed,
-                    context_lens=lens, block_tables=bt, write_slots=ws)
+                    context_lens=lens, block_tables=bt, write_slots=ws, query_len=query_len)
 
 
 def _log_uniform(rng, n, lo, hi):
@@ -214,6 +230,16 @@ def headline_gqa4_bf16(seed=4):
                  block_size=16, max_blocks=512, dtype="bf16", lens=lens, rng=rng)
 
 
+def headline_spec4_bf16(seed=4):
+    """The headline batch verifying 4 speculative tokens per row: 4 query
+    tokens per row and head, causal among themselves; same lengths (which
+    count the 4 new tokens) and pool recipe."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(512, 8192, size=256, endpoint=True)
+    return _make("headline_spec4_bf16", seed, rows=256, heads=32, kv_heads=32, head_dim=128,
+                 block_size=16, max_blocks=512, dtype="bf16", lens=lens, rng=rng, query_len=4)
+
+
 WORKLOADS = {
     "tiny_f32": tiny_f32,
     "uniform_f32": uniform_f32,
@@ -221,16 +247,17 @@ WORKLOADS = {
     "manyrow_bf16": manyrow_bf16,
     "headline_bf16": headline_bf16,
     "headline_gqa4_bf16": headline_gqa4_bf16,
+    "headline_spec4_bf16": headline_spec4_bf16,
 }
 
 
 def custom(name, seed, rows, heads, kv_heads, head_dim, block_size, max_blocks,
-           dtype, lens, num_blocks=None, free_frac=0.0, scale=None):
+           dtype, lens, num_blocks=None, free_frac=0.0, scale=None, query_len=1):
     """A workload with given lengths (used for edge cases and small sweeps)."""
     return _make(name, seed, rows=rows, heads=heads, kv_heads=kv_heads,
                  head_dim=head_dim, block_size=block_size, max_blocks=max_blocks,
                  dtype=dtype, lens=lens, num_blocks=num_blocks,
-                 free_frac=free_frac, scale=scale)
+                 free_frac=free_frac, scale=scale, query_len=query_len)
 
 
 def spread_lengths(rows, width, spread):
@@ -261,12 +288,11 @@ def _host_normal(rng, shape, dtype):
 def host_values(wl, value_seed=None):
     """q, k_pool, v_pool, k_new, v_new as numpy arrays (fp32 or bf16 bits)."""
     rng = np.random.default_rng(wl.seed + 1000 if value_seed is None else value_seed)
-    R, H, Hkv, D = wl.rows, wl.heads, wl.kv_heads, wl.head_dim
-    q = _host_normal(rng, (R, H, D), wl.dtype)
+    q = _host_normal(rng, wl.q_shape, wl.dtype)
     k_pool = _host_normal(rng, wl.pool_shape, wl.dtype)
     v_pool = _host_normal(rng, wl.pool_shape, wl.dtype)
-    k_new = _host_normal(rng, (R, Hkv, D), wl.dtype)
-    v_new = _host_normal(rng, (R, Hkv, D), wl.dtype)
+    k_new = _host_normal(rng, wl.new_shape, wl.dtype)
+    v_new = _host_normal(rng, wl.new_shape, wl.dtype)
     return q, k_pool, v_pool, k_new, v_new
 
 
@@ -291,8 +317,6 @@ def device_values(wl, device, value_seed=None):
     seed = wl.seed + 1000 if value_seed is None else value_seed
     g = torch.Generator(device=device)
     g.manual_seed(seed)
-    R, H, Hkv, D = wl.rows, wl.heads, wl.kv_heads, wl.head_dim
-
     def draw(shape):
         t = torch.empty(shape, dtype=tdt, device=device)
         flat = t.view(-1)
@@ -302,11 +326,11 @@ def device_values(wl, device, value_seed=None):
             flat[s:s + n].copy_(torch.randn(n, generator=g, device=device, dtype=torch.float32))
         return t
 
-    q = draw((R, H, D))
+    q = draw(wl.q_shape)
     k_pool = draw(wl.pool_shape)
     v_pool = draw(wl.pool_shape)
-    k_new = draw((R, Hkv, D))
-    v_new = draw((R, Hkv, D))
+    k_new = draw(wl.new_shape)
+    v_new = draw(wl.new_shape)
     return q, k_pool, v_pool, k_new, v_new
 
 
@@ -343,9 +367,10 @@ def compact_rows(wl, rows):
                 order.append(b)
             tables[i, j] = index[b]
     nb = len(order)
-    slots = np.empty(len(rows), dtype=np.int64)
-    for i, r in enumerate(rows):
-        s = int(wl.write_slots[r])
+    src = np.asarray(wl.write_slots)[rows]
+    slots = np.empty(src.shape, dtype=np.int64)
+    for i, s in np.ndenumerate(src):
+        s = int(s)
         if s // B == wl.num_blocks:
             slots[i] = nb * B + s % B
         else:

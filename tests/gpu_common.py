@@ -78,9 +78,15 @@ def oracle_step(wl, host, rows=None, threads=0):
     """The oracle's append then read on host copies; fp64 [rows, H, D]."""
     kp = host["k_pool"].copy()
     vp = host["v_pool"].copy()
-    oracle.kv_write(host["k_new"], host["v_new"], wl.write_slots, kp, vp)
+    oracle.kv_write(_flat(host["k_new"]), _flat(host["v_new"]),
+                    np.asarray(wl.write_slots).reshape(-1), kp, vp)
     return oracle.paged_decode(host["q"], kp, vp, wl.block_tables, wl.context_lens, wl.scale,
                                rows=rows, threads=threads)
+
+
+def _flat(new):
+    """[R, NQ, Hkv, D] new tokens -> [R*NQ, Hkv, D] (the append is per token)."""
+    return new.reshape(-1, new.shape[-2], new.shape[-1])
 
 
 def oracle_read(wl, host, rows=None, threads=0):
@@ -110,7 +116,7 @@ def oracle_step_sampled(wl, inp, rows, threads=0):
     kn = W.to_numpy(inp["k_new"].index_select(0, ridx))
     vn = W.to_numpy(inp["v_new"].index_select(0, ridx))
     ctx = wl.context_lens[rows]
-    oracle.kv_write(kn, vn, slots, kp, vp)
+    oracle.kv_write(_flat(kn), _flat(vn), slots.reshape(-1), kp, vp)
     return oracle.paged_decode(q, kp, vp, tables, ctx, wl.scale, threads=threads)
 
 

@@ -58,7 +58,7 @@ def test_abi_version_and_strerror(nsv):
 
 def _shape(nsv, **kw):
     d = dict(rows=256, num_heads=32, num_kv_heads=32, head_dim=128, max_blocks=512,
-             num_blocks=70000, dtype=nsv.BF16)
+             num_blocks=70000, dtype=nsv.BF16, query_len=1)
     d.update(kw)
     return nsv.make_shape(**d)
 
@@ -81,12 +81,37 @@ def test_plan_shapes_of_every_workload(nsv):
     for name, make in W.WORKLOADS.items():
         wl = make()
         shape = nsv.make_shape(wl.rows, wl.heads, wl.kv_heads, wl.head_dim, wl.max_blocks,
-                               wl.num_blocks, nsv.F32 if wl.dtype == "f32" else nsv.BF16)
+                               wl.num_blocks, nsv.F32 if wl.dtype == "f32" else nsv.BF16,
+                               query_len=wl.query_len)
         p = nsv.plan_split(shape, num_sms=152)
         assert p.grid == 152 * p.ctas_per_sm
         assert p.smem_bytes <= 227 * 1024
-        assert 0 < p.workspace_bytes < (4 << 20)
+        nvec = p.kv_heads_per_cta * (wl.heads // wl.kv_heads) * wl.query_len
+        assert 0 < p.workspace_bytes < 152 * 4 * 2 * nvec * (wl.head_dim * 4 + 8) + (1 << 16)
         assert wl.kv_heads % p.kv_heads_per_cta == 0
+        assert (p.threads // 32 - 1) * p.vectors_per_warp == nvec
+
+
+@pytest.mark.parametrize("heads,kv_heads,qlen,qw,warps", [
+    (32, 32, 1, 1, 8), (32, 8, 1, 4, 8), (32, 32, 4, 4, 8), (32, 32, 2, 2, 8),
+    (32, 32, 3, 1, 6), (16, 1, 1, 4, 4), (32, 8, 8, 4, 8), (8, 8, 5, 1, 5),
+])
+def test_plan_query_vectors(nsv, heads, kv_heads, qlen, qw, warps):
+    """A consumer warp serves the largest of 4, 2, 1 query vectors that
+    divides the vectors per KV head (query heads per KV head x tokens)."""
+    p = nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen),
+                       num_sms=152)
+    assert p.vectors_per_warp == qw
+    assert p.threads == (warps + 1) * 32
+
+
+@pytest.mark.parametrize("heads,kv_heads,qlen", [(32, 8, 9), (32, 32, 33), (32, 32, 18),
+                                                 (64, 4, 3)])
+def test_plan_refuses_too_many_query_vectors(nsv, heads, kv_heads, qlen):
+    with pytest.raises(nsv.NsvError) as e:
+        nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen),
+                       num_sms=152)
+    assert e.value.code == -3
 
 
 def test_plan_custom_choices(nsv):

@@ -338,3 +338,58 @@ def test_host_side_refusals(nsv):
         nsv.paged_decode(inp["q"], inp["k_pool"], inp["v_pool"], inp["block_tables"],
                          inp["context_lens"], wl.scale, odd)
     assert e.value.code == -4
+
+
+# ---------------------------------------------------------------------------
+# several query tokens per row (causal among themselves) and grouped heads:
+# a consumer warp serves up to 4 query vectors from one K/V tile
+
+
+@pytest.mark.parametrize("qlen,heads,kv_heads,dtype,head_dim", [
+    (2, 8, 8, "bf16", 128), (3, 8, 8, "f32", 128), (4, 8, 8, "bf16", 128),
+    (4, 32, 8, "bf16", 128), (2, 16, 4, "f32", 64), (8, 8, 2, "bf16", 64),
+    (5, 4, 4, "bf16", 128), (4, 4, 1, "f32", 128),
+])
+def test_multi_query_step(nsv, qlen, heads, kv_heads, dtype, head_dim):
+    lens = [qlen, 100, 0, 1030, 17, 2 * qlen + 1, 1]   # the last row is shorter than qlen
+    wl = W.custom("mq", 51 + qlen, rows=len(lens), heads=heads, kv_heads=kv_heads,
+                  head_dim=head_dim, block_size=16, max_blocks=70, dtype=dtype, lens=lens,
+                  free_frac=0.2, query_len=qlen)
+    inp = device_inputs(wl)
+    host = host_copy(inp)
+    out = gpu_step(wl, inp)
+    st, walked = status()
+    assert st == 0 and walked == oracle.walked_tiles(wl.context_lens, 16)
+    ref = oracle_step(wl, host)
+    assert ref.shape == (len(lens), qlen, heads, head_dim)
+    assert_parity(dtype, gpu_out_f64(out), ref)
+
+
+@pytest.mark.parametrize("kw", [dict(grid=1), dict(grid=5000), dict(stages=2, grid=9),
+                                dict(kv_heads_per_cta=1)])
+def test_multi_query_plans(nsv, kw):
+    wl = W.custom("mq_plans", 61, rows=5, heads=8, kv_heads=8, head_dim=128, block_size=16,
+                  max_blocks=70, dtype="bf16", lens=[4, 700, 0, 1100, 33], free_frac=0.2,
+                  query_len=4)
+    inp = device_inputs(wl)
+    host = host_copy(inp)
+    shape = nsv.shape_of(inp["q"], inp["k_pool"], inp["block_tables"])
+    plan = nsv.plan_custom(shape, **kw)
+    out = gpu_step(wl, inp, plan=plan)
+    assert status()[0] == 0
+    assert_parity("bf16", gpu_out_f64(out), oracle_step(wl, host))
+
+
+@pytest.mark.parametrize("name", ["headline_spec4_bf16", "headline_gqa4_bf16"])
+def test_headline_variants_sampled(nsv, name):
+    """Full-size headline batches with 4 query tokens per row, and with 4
+    query heads per KV head, in the benchmark's default plan; sampled rows."""
+    wl = W.WORKLOADS[name]()
+    inp = device_inputs(wl)
+    ctx = wl.context_lens
+    rows = sorted({int(np.argmax(ctx)), int(np.argmin(ctx)), 0, wl.rows - 1, 77, 130})
+    ref = oracle_step_sampled(wl, inp, rows)
+    out = gpu_step(wl, inp, plan=default_plan(inp))
+    st, walked = status()
+    assert st == 0 and walked == oracle.walked_tiles(ctx, 16)
+    assert_parity(wl.dtype, gpu_out_f64(out)[rows], ref)
