@@ -81,6 +81,10 @@ class Oracle:
         lib.oracle_paged_decode.restype = i32
         lib.oracle_paged_decode.argtypes = [i64, i64, i64, i64, i64, i64, i64, i64, i32,
                                             vp, vp, vp, vp, vp, dbl, vp, i64, i32, vp]
+        lib.oracle_paged_decode_slots.restype = i32
+        lib.oracle_paged_decode_slots.argtypes = [i64, i64, i64, i64, i64, i64, i64, i64, i64,
+                                                  i32, vp, vp, vp, vp, vp, dbl, vp, i64, i32,
+                                                  vp]
         lib.oracle_kv_write.restype = i32
         lib.oracle_kv_write.argtypes = [i64, i64, i64, i64, i64, i32, vp, vp, vp, vp, vp]
         lib.oracle_walked_tiles.restype = i64
@@ -136,6 +140,39 @@ class Oracle:
             raise OracleRefusal(rc)
         return out[:, 0] if single else out
 
+    def paged_decode_slots(self, q, k_pool, v_pool, slot_table, width, context_lens, scale,
+                           rows=None, threads=0):
+        """The read through a per-token slot table [R, stride] (int64; the
+        first `width` columns are the rectangle).  Shapes as paged_decode."""
+        dt = _dtype_code(k_pool)
+        if _dtype_code(q) != dt or _dtype_code(v_pool) != dt:
+            raise TypeError("q, k_pool and v_pool must share one dtype")
+        single = q.ndim == 3
+        if single:
+            q = q[:, None]
+        R, NQ, H, D = q.shape
+        NB1, Hkv, B, D2 = k_pool.shape
+        if D2 != D or v_pool.shape != k_pool.shape:
+            raise ValueError("pool shape does not match q")
+        q, qp = _c(q, q.dtype)
+        k_pool, kp = _c(k_pool, k_pool.dtype)
+        v_pool, vpp = _c(v_pool, v_pool.dtype)
+        st, stp = _c(slot_table, np.int64)
+        cl, clp = _c(context_lens, np.int32)
+        if rows is None:
+            rp, nrows = None, R
+        else:
+            rows_arr, rp = _c(np.asarray(rows, dtype=np.int64), np.int64)
+            nrows = rows_arr.shape[0]
+        out = np.zeros((nrows, NQ, H, D), dtype=np.float64)
+        rc = self.lib.oracle_paged_decode_slots(R, NQ, H, Hkv, D, B, int(width), st.shape[1],
+                                                NB1 - 1, dt, qp, kp, vpp, stp, clp,
+                                                float(scale), rp, nrows, int(threads),
+                                                out.ctypes.data)
+        if rc != 0:
+            raise OracleRefusal(rc)
+        return out[:, 0] if single else out
+
     def kv_write(self, k_new, v_new, write_slots, k_pool, v_pool):
         """The KV append, in place on the numpy pools."""
         dt = _dtype_code(k_pool)
@@ -184,6 +221,10 @@ def max_threads():
 
 def paged_decode(*args, **kwargs):
     return default().paged_decode(*args, **kwargs)
+
+
+def paged_decode_slots(*args, **kwargs):
+    return default().paged_decode_slots(*args, **kwargs)
 
 
 def kv_write(*args, **kwargs):

@@ -36,6 +36,9 @@
  *     of length ctx sits at position ctx - n + j and sees the positions
  *     t < ctx - n + 1 + j (causal within the step's new tokens); a query
  *     that sees no position outputs 0.  query_len 1 is the decode read.
+ *   - oracle_paged_decode_slots: the same read through a per-token slot
+ *     table instead of a block table (Day 51 "What I added today": the
+ *     SlotTable window the reference read gathers through).
  *   - oracle_kv_write: pool[write_slots[r]] = new[r], one row at a time.
  *   - oracle_walked_tiles / oracle_rect_tiles: the tile accounting of the
  *     streamed read (tiles walked = sum over rows of cdiv(ctx, tile); the
@@ -99,32 +102,40 @@ static int elem_bytes(int dtype)
 }
 
 /*
- * The reference read over a subset of rows.
+ * The reference read over a subset of rows, through either addressing form:
+ * a block table [R][MB] (position t of row r in block table[r][t / B] at
+ * offset t % B; W = MB * B) or a slot table (position t of row r at flat
+ * slot slots[r * stride + t], slot s being block s / B, offset s % B; the
+ * rectangle is the table's first W columns).
  *
  * NQ: query tokens per row (1 for the decode read).
  * rows / nrows: which rows to compute (rows == NULL means 0..R-1, nrows = R).
  * out: fp64 [nrows][NQ][H][D], row i of out belongs to batch row rows[i].
  * threads: OpenMP threads (<= 0 means the runtime default).
  */
-int oracle_paged_decode(int64_t R, int64_t NQ, int64_t H, int64_t Hkv,
-                        int64_t D, int64_t B, int64_t MB, int64_t NB,
-                        int dtype, const void *q, const void *k_pool,
-                        const void *v_pool, const int32_t *block_tables,
-                        const int32_t *context_lens, double scale,
-                        const int64_t *rows, int64_t nrows, int threads,
-                        double *out)
+static int read_rect(int64_t R, int64_t NQ, int64_t H, int64_t Hkv, int64_t D,
+                     int64_t B, int64_t MB, int64_t W, int64_t NB, int dtype,
+                     const void *q, const void *k_pool, const void *v_pool,
+                     const int32_t *block_tables, const int64_t *slots,
+                     int64_t stride, const int32_t *context_lens,
+                     double scale, const int64_t *rows, int64_t nrows,
+                     int threads, double *out)
 {
     if (R < 0 || NQ <= 0 || H <= 0 || Hkv <= 0 || D <= 0 || B <= 0 ||
-        MB <= 0 || NB <= 0 || H % Hkv != 0 ||
+        W <= 0 || NB <= 0 || H % Hkv != 0 ||
         (dtype != OR_F32 && dtype != OR_BF16))
+        return OR_ERR_SHAPE;
+    if (slots == NULL && MB <= 0)
+        return OR_ERR_SHAPE;
+    if (slots != NULL && stride < W)
         return OR_ERR_SHAPE;
     if (rows == NULL)
         nrows = R;
-    const int64_t W = MB * B;          /* rectangle width in tokens */
     const int64_t pool_blocks = NB + 1; /* allocator's blocks + the sink */
     const int64_t group = H / Hkv;
 
-    /* The oracle's own refusals, checked before any arithmetic. */
+    /* The oracle's own refusals, checked before any arithmetic: every entry
+     * of the rectangle it gathers must be a legal (wrapping) index. */
     for (int64_t i = 0; i < nrows; ++i) {
         int64_t r = rows ? rows[i] : i;
         if (r < 0 || r >= R)
@@ -132,10 +143,18 @@ int oracle_paged_decode(int64_t R, int64_t NQ, int64_t H, int64_t Hkv,
         int64_t c = context_lens[r];
         if (c < 0 || c > W)
             return OR_ERR_RANGE;
-        for (int64_t j = 0; j < MB; ++j) {
-            int64_t b = block_tables[r * MB + j];
-            if (b < -pool_blocks || b >= pool_blocks)
-                return OR_ERR_RANGE;
+        if (slots == NULL) {
+            for (int64_t j = 0; j < MB; ++j) {
+                int64_t b = block_tables[r * MB + j];
+                if (b < -pool_blocks || b >= pool_blocks)
+                    return OR_ERR_RANGE;
+            }
+        } else {
+            for (int64_t t = 0; t < W; ++t) {
+                int64_t e = slots[r * stride + t];
+                if (e < -pool_blocks * B || e >= pool_blocks * B)
+                    return OR_ERR_RANGE;
+            }
         }
     }
 
@@ -174,13 +193,22 @@ int oracle_paged_decode(int64_t R, int64_t NQ, int64_t H, int64_t Hkv,
                 c = 0;
             double *o = out + ((i * NQ + jq) * H + h) * D;
 
-            /* 1. Gather the whole rectangle through the block table.
-             *    Position t lives in block table[r][t / B] at offset t % B. */
+            /* 1. Gather the whole rectangle through the addressing. */
             for (int64_t t = 0; t < W; ++t) {
-                int64_t b = block_tables[r * MB + t / B];
-                if (b < 0)
-                    b += pool_blocks; /* a negative index wraps, as in Python */
-                int64_t base = ((b * Hkv + g) * B + t % B) * D;
+                int64_t base;
+                if (slots == NULL) {
+                    /* position t lives in block table[r][t / B], offset t % B */
+                    int64_t b = block_tables[r * MB + t / B];
+                    if (b < 0)
+                        b += pool_blocks; /* a negative index wraps, as in Python */
+                    base = ((b * Hkv + g) * B + t % B) * D;
+                } else {
+                    /* position t lives at flat slot slots[r][t] */
+                    int64_t sl = slots[r * stride + t];
+                    if (sl < 0)
+                        sl += pool_blocks * B; /* wraps, as in Python */
+                    base = (((sl / B) * Hkv + g) * B + sl % B) * D;
+                }
                 for (int64_t d = 0; d < D; ++d) {
                     Krect[t * D + d] = widen(k_pool, dtype, base + d);
                     Vrect[t * D + d] = widen(v_pool, dtype, base + d);
@@ -233,6 +261,39 @@ int oracle_paged_decode(int64_t R, int64_t NQ, int64_t H, int64_t Hkv,
         free(qv);
     }
     return failed ? OR_ERR_NOMEM : OR_OK;
+}
+
+/* The read through block tables (the decode read of the Day-59 page). */
+int oracle_paged_decode(int64_t R, int64_t NQ, int64_t H, int64_t Hkv,
+                        int64_t D, int64_t B, int64_t MB, int64_t NB,
+                        int dtype, const void *q, const void *k_pool,
+                        const void *v_pool, const int32_t *block_tables,
+                        const int32_t *context_lens, double scale,
+                        const int64_t *rows, int64_t nrows, int threads,
+                        double *out)
+{
+    return read_rect(R, NQ, H, Hkv, D, B, MB, MB * B, NB, dtype, q, k_pool,
+                     v_pool, block_tables, NULL, 0, context_lens, scale, rows,
+                     nrows, threads, out);
+}
+
+/* The read through a per-token slot table (nanoserve Day 51, "the read
+ * rectangle stopped being built", "What I added today": the SlotTable's
+ * [rows, width] window of flat slots, row stride `stride`, that the
+ * reference read gathers through). */
+int oracle_paged_decode_slots(int64_t R, int64_t NQ, int64_t H, int64_t Hkv,
+                              int64_t D, int64_t B, int64_t W, int64_t stride,
+                              int64_t NB, int dtype, const void *q,
+                              const void *k_pool, const void *v_pool,
+                              const int64_t *slots, const int32_t *context_lens,
+                              double scale, const int64_t *rows, int64_t nrows,
+                              int threads, double *out)
+{
+    if (slots == NULL)
+        return OR_ERR_SHAPE;
+    return read_rect(R, NQ, H, Hkv, D, B, 0, W, NB, dtype, q, k_pool, v_pool,
+                     NULL, slots, stride, context_lens, scale, rows, nrows,
+                     threads, out);
 }
 
 /*

@@ -202,6 +202,108 @@ def pin_multiquery_short_row(orc):
     assert np.any(got[0, 2:] != 0.0)
 
 
+def _slots_from_tables(bt, B):
+    """The slot table the reference builds from block tables: slot of
+    position t = table[t / B] * B + t % B; padding entries stay negative."""
+    R, MB = bt.shape
+    t = np.arange(MB * B)
+    blk = bt[:, t // B].astype(np.int64)
+    return np.where(blk >= 0, blk * B + t % B, -1).astype(np.int64)
+
+
+def brute_force_slots(q, k, v, slots, ctx, scale, B):
+    """Per-key loop through a slot table; fp64; q [R, H, D]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    R, H, D = q.shape
+    group = H // k.shape[1]
+    out = np.zeros((R, H, D))
+    for r in range(R):
+        c = int(ctx[r])
+        for h in range(H):
+            if c == 0:
+                continue
+            g = h // group
+            kk = [k[int(slots[r, t]) // B, g, int(slots[r, t]) % B] for t in range(c)]
+            vv = [v[int(slots[r, t]) // B, g, int(slots[r, t]) % B] for t in range(c)]
+            sc = [scale * math.fsum(q[r, h, d] * x[d] for d in range(D)) for x in kk]
+            mx = max(sc)
+            w = [math.exp(s - mx) for s in sc]
+            z = math.fsum(w)
+            for d in range(D):
+                out[r, h, d] = math.fsum(w[t] / z * vv[t][d] for t in range(c))
+    return out
+
+
+def pin_slots_equal_block_tables(orc):
+    """A slot table built from the block tables reads what the block tables
+    read, bit for bit (same gathered rectangle, same arithmetic)."""
+    for dtype in ("f32", "bf16"):
+        cs = small_case(40, dtype, rows=4, heads=4, kv_heads=2, head_dim=8, block_size=4,
+                        lens=[3, 0, 14, 8])
+        base = _decode(orc, cs)
+        slots = _slots_from_tables(cs["bt"], cs["B"])
+        got = orc.paged_decode_slots(cs["q"], cs["k"], cs["v"], slots, slots.shape[1],
+                                     cs["ctx"], cs["scale"])
+        assert np.array_equal(got, base)
+
+
+def pin_slots_brute_force(orc):
+    """Arbitrary per-token slots (not grouped into blocks) against a per-key
+    loop; a wider table (row stride > width) is read only up to the width."""
+    rng = np.random.default_rng(41)
+    cs = small_case(41, "f32", rows=3, heads=2, kv_heads=2, head_dim=8, block_size=4,
+                    lens=[5, 9, 1], spare=6)
+    nslots = cs["k"].shape[0] * 4
+    width, stride = 12, 20
+    slots = np.full((3, stride), 10 ** 9, dtype=np.int64)   # past the width: never read
+    for r in range(3):
+        slots[r, :width] = rng.choice(nslots, size=width, replace=False)
+    got = orc.paged_decode_slots(cs["q"], cs["k"], cs["v"], slots, width, cs["ctx"],
+                                 cs["scale"])
+    ref = brute_force_slots(cs["q"], cs["k"], cs["v"], slots, cs["ctx"], cs["scale"], 4)
+    assert np.max(np.abs(got - ref)) <= 1e-12
+
+
+def pin_slots_rectangle_reads_padding(orc):
+    """A -1 slot wraps onto the pool's last slot (the sink block's); NaN there
+    reaches the oracle's output because the rectangle gathers its padding."""
+    cs = small_case(43, "f32", rows=2, heads=2, kv_heads=2, head_dim=8, block_size=4,
+                    lens=[5, 6])
+    slots = _slots_from_tables(cs["bt"], 4)
+    assert np.all(slots[:, -1] == -1)
+    clean = orc.paged_decode_slots(cs["q"], cs["k"], cs["v"], slots, slots.shape[1],
+                                   cs["ctx"], cs["scale"])
+    assert np.all(np.isfinite(clean))
+    v = cs["v"].copy()
+    v[-1, :, -1, :] = np.nan
+    got = orc.paged_decode_slots(cs["q"], cs["k"], v, slots, slots.shape[1], cs["ctx"],
+                                 cs["scale"])
+    assert np.all(np.isnan(got))
+
+
+def pin_slots_refusals(orc):
+    cs = small_case(42, "f32", rows=2, heads=2, kv_heads=2, head_dim=8, block_size=4,
+                    lens=[3, 6])
+    slots = _slots_from_tables(cs["bt"], 4)
+    nslots = cs["k"].shape[0] * 4
+    for bad in (nslots, -nslots - 1):
+        s2 = slots.copy()
+        s2[1, 2] = bad
+        try:
+            orc.paged_decode_slots(cs["q"], cs["k"], cs["v"], s2, s2.shape[1], cs["ctx"], 1.0)
+        except OracleRefusal as e:
+            assert e.code == -5
+        else:
+            raise AssertionError("slot %d must be refused" % bad)
+    try:
+        orc.paged_decode_slots(cs["q"], cs["k"], cs["v"], slots, slots.shape[1] + 1,
+                               cs["ctx"], 1.0)
+    except OracleRefusal as e:
+        assert e.code == -3
+    else:
+        raise AssertionError("a width past the row stride must be refused")
+
+
 def pin_single_key(orc):
     for dtype in ("f32", "bf16"):
         cs = small_case(11, dtype, rows=3, heads=2, kv_heads=2, head_dim=16, block_size=4,
@@ -403,4 +505,6 @@ ALL_PINS = [
     pin_kv_write, pin_walk_table, pin_walk_counts_tiles_touched, pin_score_bytes,
     pin_multiquery_brute_force, pin_multiquery_last_token_is_the_decode_read,
     pin_multiquery_first_token_sees_one_key, pin_multiquery_is_causal, pin_multiquery_short_row,
+    pin_slots_equal_block_tables, pin_slots_brute_force, pin_slots_rectangle_reads_padding,
+    pin_slots_refusals,
 ]
