@@ -101,8 +101,8 @@ enum {
 enum {
     NSV_DEV_BAD_CTX = 1u,   /* context length outside [0, max_blocks*block_size];
                                the row was read as empty (output 0) */
-    NSV_DEV_BAD_BLOCK = 2u, /* a walked block id outside [0, num_blocks];
-                               that block was skipped */
+    NSV_DEV_BAD_BLOCK = 2u, /* a walked block id outside [0, num_blocks], or a
+                               read slot outside the pool; skipped */
     NSV_DEV_BAD_SLOT = 4u,  /* write slot outside [0, (num_blocks+1)*block_size);
                                that row's K/V was not written */
     NSV_DEV_TIMEOUT = 8u    /* an in-kernel wait gave up after its limit and the
@@ -249,6 +249,31 @@ NSV_API int nsv_paged_decode_noalloc(const nsv_shape *shape, const void *q,
                                      const int32_t *block_tables,
                                      const int32_t *context_lens, float scale, void *out,
                                      cudaStream_t stream);
+
+/*
+ * Decode read through a per-token slot table instead of block tables
+ * (nanoserve Day 51, "the read rectangle stopped being built", "What I added
+ * today": the SlotTable, one [max_batch_size, max_model_len] int64 buffer of
+ * flat slots, read as a window [rows, width] with the buffer's row stride).
+ * Position t of row r lives at flat slot slot_table[r * slot_row_stride + t],
+ * i.e. block slot / block_size, offset slot % block_size.  Only positions
+ * t < context_lens[r] are read, and context_lens[r] <= slot_cols <=
+ * min(slot_row_stride, max_blocks * block_size) (a longer row is read as
+ * empty and flagged NSV_DEV_BAD_CTX).
+ *
+ * A block whose slots form one aligned run of consecutive slots (always so
+ * for a table built from block tables) is moved with the same bulk copies as
+ * the block-table read and gives the same bits; any other block is gathered
+ * token by token.  A slot outside [0, (num_blocks+1)*block_size) is skipped
+ * and sets NSV_DEV_BAD_BLOCK.  plan and workspace as in nsv_decode_step
+ * (workspace NULL with workspace_bytes 0: the library-owned workspace).
+ */
+NSV_API int nsv_paged_decode_slots(const nsv_shape *shape, const nsv_plan *plan,
+                                   const void *q, const void *k_pool, const void *v_pool,
+                                   const int64_t *slot_table, int64_t slot_cols,
+                                   int64_t slot_row_stride, const int32_t *context_lens,
+                                   float scale, void *out, void *workspace,
+                                   size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Synchronise the current device, then report its status word (NSV_DEV_*

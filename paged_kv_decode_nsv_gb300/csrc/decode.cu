@@ -175,11 +175,34 @@ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 // Validated context length (a bad one is read as 0 and flagged).
 __device__ __forceinline__ int checked_ctx(const DecodeParams& p, int r) {
   int c = p.context_lens[r];
-  if (c < 0 || c > p.max_blocks * kBlock) {
+  const int limit = p.slots ? min(p.max_blocks * kBlock, p.slot_cols) : p.max_blocks * kBlock;
+  if (c < 0 || c > limit) {
     atomicOr(p.status, (uint32_t)NSV_DEV_BAD_CTX);
     c = 0;
   }
   return c;
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (bulk copy) writes to the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Block id of a unit under slot-table addressing: the block's `nval` slots
+// must be one aligned, contiguous run (as a table built from block tables
+// always is); otherwise kTokenWise, and the block is gathered per token.
+constexpr int kTokenWise = -2;
+
+__device__ __forceinline__ int slot_block(const int64_t* sp, int nval) {
+  const long long s0 = sp[0];
+  bool run = (s0 % kBlock) == 0;
+#pragma unroll 4
+  for (int i = 1; i < kBlock; ++i)
+    if (i < nval) run = run && (sp[i] == s0 + i);
+  if (!run) return kTokenWise;
+  const long long b = s0 / kBlock;  // may be out of range: flagged by the caller
+  return (b < 0 || b > 0x7fffffffll) ? -1 : (int)b;
 }
 
 // Barrier over the consumer warps only (the producer never joins it).
@@ -279,8 +302,9 @@ __global__ void __launch_bounds__(QW == 1 ? kMaxThreads : kMaxThreadsMulti, 1)
     uint32_t n = 0;  // fills issued (meaningful in lane 0)
     bool ok = true;
 
-    // Unit u (this lane's): its row, its stage flags and its block id.
-    auto unit_at = [&](long long u, int& row, int& flags, int& phys) {
+    // Unit u (this lane's): its row, its block within the row, its stage
+    // flags and its block id.
+    auto unit_at = [&](long long u, int& row, int& blk, int& flags, int& phys) {
       const int hg = (int)(u / N);
       const int rb = (int)(u - (long long)hg * N);
       int lo = 0, hi = p.rows - 1;  // last row r with prefix[r] <= rb
@@ -298,31 +322,40 @@ __global__ void __launch_bounds__(QW == 1 ? kMaxThreads : kMaxThreadsMulti, 1)
       if (rs >= beg && rs + nb <= end) f |= kFinal;
       if (rs > beg) f |= kSlot1;
       row = lo;
+      blk = j;
       flags = f;
-      phys = p.block_tables[(size_t)lo * p.max_blocks + j];
+      if (p.slots)
+        phys = slot_block(p.slots + (size_t)lo * p.slot_stride + (size_t)j * kBlock,
+                          min(kBlock, s_ctx[lo] - j * kBlock));
+      else
+        phys = p.block_tables[(size_t)lo * p.max_blocks + j];
     };
 
-    // Emit one stage (lane 0 only): wait for it to be free, write its
-    // metadata, arm its barrier and start its copies.
-    auto emit = [&](int row, int flags, int phys) -> bool {
-      const uint32_t s = n % S;
-      const uint32_t full = bars + 8 * s, empty = bars + 8 * (S + s);
+    // Wait (lane 0) until the next stage is free.
+    auto wait_free = [&]() -> bool {
       if (*s_abort) return false;  // a consumer gave up waiting
-      if (n >= (uint32_t)S) {
-        if (!mbar_wait(empty, ((n / S) - 1) & 1)) return false;
-      }
+      if (n >= (uint32_t)S)
+        return mbar_wait(bars + 8 * (S + n % S), ((n / S) - 1) & 1);
+      return true;
+    };
+    // Publish the next stage (lane 0): write its metadata, arm its barrier
+    // and start its copies (K/V unless the warp gathered them already, q on
+    // a segment's first stage).
+    auto publish = [&](int row, int flags, int phys, int mask) {
+      const uint32_t s = n % S;
+      const uint32_t full = bars + 8 * s;
       const int kv0 = flags >> 16;
       const int qh0 = kv0 * G;
-      s_meta[s] = make_int4(row, qh0, slot0 + ((flags & kSlot1) ? 1 : 0), flags);
+      s_meta[s] = make_int4(row, mask, slot0 + ((flags & kSlot1) ? 1 : 0), flags);
       uint32_t bytes = 0;
-      if (flags & kData) bytes += 2 * L.kv_bytes;
+      if ((flags & kData) && !(flags & kGathered)) bytes += 2 * L.kv_bytes;
       if (flags & kHasQ) bytes += L.q_bytes;
       if (bytes == 0) {
         mbar_arrive(full);
       } else {
         mbar_arrive_tx(full, bytes);
         const uint32_t base = smem_u32(smem + s * L.stage_bytes);
-        if (flags & kData) {
+        if ((flags & kData) && !(flags & kGathered)) {
           const size_t off = (size_t)phys * block_elems + (size_t)kv0 * tile_elems;
           bulk_g2s(base, kp + off, L.kv_bytes, full, pol);
           bulk_g2s(base + L.kv_bytes, vp + off, L.kv_bytes, full, pol);
@@ -334,22 +367,73 @@ __global__ void __launch_bounds__(QW == 1 ? kMaxThreads : kMaxThreadsMulti, 1)
         }
       }
       ++n;
+    };
+    auto emit = [&](int row, int flags, int phys) -> bool {
+      if (!wait_free()) return false;
+      publish(row, flags, phys, 0xffff);
+      return true;
+    };
+    // Slot mode, a block whose slots are not one aligned run: the whole warp
+    // gathers the block's tokens (every head of the group, K and V) into the
+    // next stage with 16-byte loads and stores, then lane 0 publishes it with
+    // the mask of tokens whose slot lies in the pool.
+    const long long pool_slots = p.pool_blocks * kBlock;
+    auto gather = [&](int row, int blk, int flags) -> bool {
+      bool ok2 = true;
+      if (lane == 0) ok2 = wait_free();
+      ok2 = __shfl_sync(kFull, ok2, 0);
+      if (!ok2) return false;
+      const uint32_t s = __shfl_sync(kFull, n, 0) % S;
+      unsigned char* stg = smem + (size_t)s * L.stage_bytes;
+      const int64_t* sp = p.slots + (size_t)row * p.slot_stride + (size_t)blk * kBlock;
+      const int nval = min(kBlock, flags & 0xff);
+      const long long my = lane < nval ? sp[lane] : -1;
+      const bool in_pool = lane < nval && my >= 0 && my < pool_slots;
+      if (lane < nval && !in_pool) atomicOr(p.status, (uint32_t)NSV_DEV_BAD_BLOCK);
+      const int mask = (int)(__ballot_sync(kFull, in_pool) & 0xffffu);
+      const int kv0 = flags >> 16;
+      constexpr int kVpr = D * (int)sizeof(T) / 16;  // 16-byte vectors per token row
+      const int items = kBlock * HG * 2 * kVpr;
+      for (int it = lane; it < items; it += 32) {
+        const int v = it % kVpr;
+        int rest = it / kVpr;
+        const int h = rest % HG;
+        rest /= HG;
+        const int which = rest & 1;  // 0: K, 1: V
+        const int t = rest >> 1;
+        if (!((mask >> t) & 1)) continue;
+        const long long sl = sp[t];
+        const T* src = (which ? vp : kp) +
+                       (((size_t)(sl / kBlock) * p.kv_heads + kv0 + h) * kBlock + sl % kBlock) * D;
+        *reinterpret_cast<uint4*>(stg + which * L.kv_bytes + (((size_t)h * kBlock + t) * D) *
+                                  sizeof(T) + v * 16) =
+            *(reinterpret_cast<const uint4*>(src) + v);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) publish(row, flags | kData | kGathered, 0, mask);
       return true;
     };
 
     long long w0 = beg;
-    int c_row = 0, c_flags = 0, c_phys = -1;
-    if (w0 + lane < end) unit_at(w0 + lane, c_row, c_flags, c_phys);
+    int c_row = 0, c_blk = 0, c_flags = 0, c_phys = -1;
+    if (w0 + lane < end) unit_at(w0 + lane, c_row, c_blk, c_flags, c_phys);
     while (w0 < end && ok) {
       // Prefetch the next window's units while this one is issued.
       const long long nw0 = w0 + 32;
-      int n_row = 0, n_flags = 0, n_phys = -1;
-      if (nw0 + lane < end) unit_at(nw0 + lane, n_row, n_flags, n_phys);
+      int n_row = 0, n_blk = 0, n_flags = 0, n_phys = -1;
+      if (nw0 + lane < end) unit_at(nw0 + lane, n_row, n_blk, n_flags, n_phys);
       const int nwin = (int)min(32ll, end - w0);
       for (int jj = 0; jj < nwin && ok; ++jj) {
         const int row = __shfl_sync(kFull, c_row, jj);
         int flags = __shfl_sync(kFull, c_flags, jj);
         const int phys = __shfl_sync(kFull, c_phys, jj);
+        const int blk = __shfl_sync(kFull, c_blk, jj);
+        if (phys == kTokenWise) {
+          if ((flags >> 16) == 0) ++walked;
+          ok = gather(row, blk, flags);
+          continue;
+        }
         if (phys >= 0 && (long long)phys < p.pool_blocks) {
           flags |= kData;
           if ((flags >> 16) == 0) ++walked;
@@ -361,6 +445,7 @@ __global__ void __launch_bounds__(QW == 1 ? kMaxThreads : kMaxThreadsMulti, 1)
       }
       w0 = nw0;
       c_row = n_row;
+      c_blk = n_blk;
       c_flags = n_flags;
       c_phys = n_phys;
     }
@@ -434,6 +519,8 @@ __global__ void __launch_bounds__(QW == 1 ? kMaxThreads : kMaxThreadsMulti, 1)
     const int flags = meta.w;
     if (flags & kEnd) break;
     const unsigned char* st = smem + s * L.stage_bytes;
+    const int tmask = meta.y;              // tokens of the block that hold data
+    const int qh0 = (flags >> 16) * G;     // the group's first query head
 
     if (flags & kFirst) {
 #pragma unroll
@@ -496,7 +583,7 @@ __global__ void __launch_bounds__(QW == 1 ? kMaxThreads : kMaxThreadsMulti, 1)
         for (int o = kDup >> 1; o >= 1; o >>= 1) sc += __shfl_xor_sync(kFull, sc, o);
         // this vector sees the row's positions before ctx - (NQ - 1 - jq)
         const int nv = rem - (NQ - 1 - jq[k]);
-        sc = (tok < nv) ? sc : -INFINITY;
+        sc = (tok < nv && ((tmask >> tok) & 1)) ? sc : -INFINITY;
         float mx = sc;
 #pragma unroll
         for (int o = kDup; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
@@ -523,7 +610,7 @@ __global__ void __launch_bounds__(QW == 1 ? kMaxThreads : kMaxThreadsMulti, 1)
 #pragma unroll
       for (int i = 0; i < kNp; ++i) {
         const int t = i * kTpi + grp;
-        if (t < nvalid) {  // never touch values past the row's length
+        if (t < nvalid && ((tmask >> t) & 1)) {  // never touch values past the row's length
           const uint4 raw =
               *reinterpret_cast<const uint4*>(vt + ((size_t)t * D + sub * kDpl) * sizeof(T));
           float v[kDpl];
@@ -561,7 +648,7 @@ __global__ void __launch_bounds__(QW == 1 ? kMaxThreads : kMaxThreadsMulti, 1)
 #pragma unroll
             for (int e = 0; e < kDpl; ++e) at[k][e] *= inv;
             T* o = static_cast<T*>(p.out) +
-                   (((size_t)row * NQ + jq[k]) * p.heads + meta.y + qhl[k]) * D + sub * kDpl;
+                   (((size_t)row * NQ + jq[k]) * p.heads + qh0 + qhl[k]) * D + sub * kDpl;
             *reinterpret_cast<uint4*>(o) = E::narrow(at[k]);
           }
         }
@@ -649,7 +736,7 @@ __global__ void __launch_bounds__(QW == 1 ? kMaxThreads : kMaxThreadsMulti, 1)
             for (int o2 = 16; o2 >= 1; o2 >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, o2);
             const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
             T* o = static_cast<T*>(p.out) +
-                   (((size_t)row * NQ + jq[k]) * p.heads + meta.y + qhl[k]) * D + lane * kPer;
+                   (((size_t)row * NQ + jq[k]) * p.heads + qh0 + qhl[k]) * D + lane * kPer;
 #pragma unroll
             for (int e = 0; e < kPer; ++e) {
               if constexpr (sizeof(T) == 4) {

@@ -170,17 +170,26 @@ int check_plan(const nsv_shape* s, const nsv_plan* given, nsv_plan* use) {
   return NSV_OK;
 }
 
+// The read through either addressing form: block_tables (slots null) or a
+// slot table `slots` with `slot_cols` readable columns per row and row
+// stride `slot_stride` (block_tables null).
 int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, const void* k_pool,
-                const void* v_pool, const int32_t* block_tables, const int32_t* context_lens,
+                const void* v_pool, const int32_t* block_tables, const int64_t* slots,
+                int64_t slot_cols, int64_t slot_stride, const int32_t* context_lens,
                 float scale, void* out, void* ws, size_t ws_bytes, bool library_ws,
                 cudaStream_t stream) {
   int rc = check_shape(s);
   if (rc) return rc;
-  if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return NSV_ERR_NULLPTR;
+  if (!q || !k_pool || !v_pool || !(block_tables || slots) || !context_lens || !out)
+    return NSV_ERR_NULLPTR;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(slots) & 7u) ||
       (reinterpret_cast<uintptr_t>(context_lens) & 3u))
     return NSV_ERR_ALIGN;
+  if (slots && (slot_cols < 1 || slot_cols > (int64_t)s->max_blocks * s->block_size ||
+                slot_stride < slot_cols))
+    return NSV_ERR_SHAPE;
   nsv_plan plan;
   if (plan_in) {
     if ((rc = check_plan(s, plan_in, &plan)) != NSV_OK) return rc;
@@ -222,6 +231,9 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   p.k_pool = k_pool;
   p.v_pool = v_pool;
   p.block_tables = block_tables;
+  p.slots = slots;
+  p.slot_stride = slots ? slot_stride : 0;
+  p.slot_cols = slots ? (int)slot_cols : 0;
   p.context_lens = context_lens;
   p.out = out;
   p.ws_cnt = reinterpret_cast<int32_t*>(wsb);
@@ -311,8 +323,8 @@ NSV_API int nsv_paged_decode(const nsv_shape* shape, const void* q, const void* 
                              const void* v_pool, const int32_t* block_tables,
                              const int32_t* context_lens, float scale, void* out,
                              cudaStream_t stream) {
-  return decode_impl(shape, nullptr, q, k_pool, v_pool, block_tables, context_lens, scale, out,
-                     nullptr, 0, true, stream);
+  return decode_impl(shape, nullptr, q, k_pool, v_pool, block_tables, nullptr, 0, 0,
+                     context_lens, scale, out, nullptr, 0, true, stream);
 }
 
 NSV_API int nsv_paged_decode_ws(const nsv_shape* shape, const nsv_plan* plan, const void* q,
@@ -320,8 +332,8 @@ NSV_API int nsv_paged_decode_ws(const nsv_shape* shape, const nsv_plan* plan, co
                                 const int32_t* block_tables, const int32_t* context_lens,
                                 float scale, void* out, void* workspace, size_t workspace_bytes,
                                 cudaStream_t stream) {
-  return decode_impl(shape, plan, q, k_pool, v_pool, block_tables, context_lens, scale, out,
-                     workspace, workspace_bytes, false, stream);
+  return decode_impl(shape, plan, q, k_pool, v_pool, block_tables, nullptr, 0, 0, context_lens,
+                     scale, out, workspace, workspace_bytes, false, stream);
 }
 
 NSV_API int nsv_decode_step(const nsv_shape* shape, const nsv_plan* plan, const void* q,
@@ -332,8 +344,21 @@ NSV_API int nsv_decode_step(const nsv_shape* shape, const nsv_plan* plan, const 
   int rc = nsv_kv_write(shape, k_new, v_new, write_slots, k_pool, v_pool, stream);
   if (rc) return rc;
   const bool lib_ws = workspace == nullptr && workspace_bytes == 0;
-  return decode_impl(shape, plan, q, k_pool, v_pool, block_tables, context_lens, scale, out,
-                     workspace, workspace_bytes, lib_ws, stream);
+  return decode_impl(shape, plan, q, k_pool, v_pool, block_tables, nullptr, 0, 0, context_lens,
+                     scale, out, workspace, workspace_bytes, lib_ws, stream);
+}
+
+NSV_API int nsv_paged_decode_slots(const nsv_shape* shape, const nsv_plan* plan, const void* q,
+                                   const void* k_pool, const void* v_pool,
+                                   const int64_t* slot_table, int64_t slot_cols,
+                                   int64_t slot_row_stride, const int32_t* context_lens,
+                                   float scale, void* out, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream) {
+  if (!slot_table) return NSV_ERR_NULLPTR;
+  const bool lib_ws = workspace == nullptr && workspace_bytes == 0;
+  return decode_impl(shape, plan, q, k_pool, v_pool, nullptr, slot_table, slot_cols,
+                     slot_row_stride, context_lens, scale, out, workspace, workspace_bytes,
+                     lib_ws, stream);
 }
 
 NSV_API int nsv_device_status(uint32_t* status, uint64_t* blocks_walked, int clear) {

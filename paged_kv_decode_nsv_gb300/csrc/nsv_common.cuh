@@ -35,6 +35,8 @@ enum : int {
   kHasQ = 1 << 12,   // the stage holds the group's query vectors
   kEnd = 1 << 13,    // no more work: consumers exit
   kSlot1 = 1 << 14,  // a partial segment that is not the CTA's first one
+  kGathered = 1 << 15,  // the K/V tiles were gathered token by token by the
+                        // producer warp (slot-table addressing)
 };
 
 // Workspace of one decode read (all offsets 256-byte aligned):
@@ -63,7 +65,10 @@ struct DecodeParams {
   const void* q;
   const void* k_pool;
   const void* v_pool;
-  const int32_t* block_tables;
+  const int32_t* block_tables;  // block-table addressing (null in slot mode)
+  const int64_t* slots;         // slot-table addressing (null in block mode)
+  long long slot_stride;        // row stride of the slot table, in entries
+  int slot_cols;                // readable columns of each slot-table row
   const int32_t* context_lens;
   void* out;
   int32_t* ws_cnt;     // workspace arrival counters (zero at launch)

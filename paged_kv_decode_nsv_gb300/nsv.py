@@ -76,6 +76,9 @@ _lib.nsv_paged_decode_ws.argtypes = [_SP, _PP, _vp, _vp, _vp, _vp, _vp, _f, _vp,
 _lib.nsv_decode_step.restype = _i32
 _lib.nsv_decode_step.argtypes = [_SP, _PP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f, _vp,
                                  _vp, _sz, _vp]
+_lib.nsv_paged_decode_slots.restype = _i32
+_lib.nsv_paged_decode_slots.argtypes = [_SP, _PP, _vp, _vp, _vp, _vp, ctypes.c_int64,
+                                        ctypes.c_int64, _vp, _f, _vp, _vp, _sz, _vp]
 _lib.nsv_paged_decode_noalloc.restype = _i32
 _lib.nsv_paged_decode_noalloc.argtypes = [_SP, _vp, _vp, _vp, _vp, _vp, _f, _vp, _vp]
 _lib.nsv_device_status.restype = _i32
@@ -229,6 +232,41 @@ def paged_decode_ws(q, k_pool, v_pool, block_tables, context_lens, scale, out, w
                                     _ptr(context_lens, "context_lens"), float(scale),
                                     _ptr(out, "out"), ws_ptr, ws_bytes, _stream(stream)),
            "nsv_paged_decode_ws")
+    return out
+
+
+def paged_decode_slots(q, k_pool, v_pool, slot_table, context_lens, scale, out, workspace=None,
+                       plan=None, max_blocks=None, stream=None):
+    """Decode read through a per-token slot table.
+
+    slot_table is an int64 [rows, width] tensor whose rows may be strided (a
+    window of a wider table, as slots[:rows, :width] of a persistent buffer);
+    its last dimension must be contiguous.  max_blocks defaults to
+    cdiv(width, 16) and only sizes the plan.
+    """
+    import torch
+    if slot_table.dtype != torch.int64 or slot_table.dim() != 2 or \
+            (slot_table.shape[1] > 1 and slot_table.stride(1) != 1):
+        raise ValueError("slot_table must be an int64 [rows, width] tensor with unit column stride")
+    if not slot_table.is_cuda:
+        raise ValueError("slot_table must be a CUDA tensor")
+    rows, width = slot_table.shape
+    mb = max_blocks or (width + 15) // 16
+    if q.dim() == 4:
+        R, NQ, H, D = q.shape
+    else:
+        (R, H, D), NQ = q.shape, 1
+    NB1, Hkv, B, _ = k_pool.shape
+    shape = make_shape(R, H, Hkv, D, mb, NB1 - 1, _dtype_code(k_pool), B, query_len=NQ)
+    ws_ptr = _ptr(workspace, "workspace")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib.nsv_paged_decode_slots(ctypes.byref(shape), ctypes.byref(plan) if plan else None,
+                                       _ptr(q, "q"), _ptr(k_pool, "k_pool"),
+                                       _ptr(v_pool, "v_pool"), slot_table.data_ptr(), int(width),
+                                       int(slot_table.stride(0)),
+                                       _ptr(context_lens, "context_lens"), float(scale),
+                                       _ptr(out, "out"), ws_ptr, ws_bytes, _stream(stream)),
+           "nsv_paged_decode_slots")
     return out
 
 
