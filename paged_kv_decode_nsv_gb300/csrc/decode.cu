@@ -172,6 +172,20 @@ struct Elem<__nv_bfloat16> {
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
+// Two fp32 fused multiply-adds in one instruction (sm_100+ packed f32x2):
+// (d0, d1) = (a0 * b0 + d0, a1 * b1 + d1), each rounded as fmaf would.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0,
+                                     float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rd, {%0, %1};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Validated context length (a bad one is read as 0 and flagged).
 __device__ __forceinline__ int checked_ctx(const DecodeParams& p, int r) {
   int c = p.context_lens[r];
@@ -557,10 +571,10 @@ __global__ void __launch_bounds__(QW == 1 ? kMaxThreads : kMaxThreadsMulti, 1)
         E::widen(raw, kk);
 #pragma unroll
         for (int k = 0; k < QW; ++k) {
-          float a = 0.f;
+          float a0 = 0.f, a1 = 0.f;  // even and odd dims, two FMAs per instruction
 #pragma unroll
-          for (int e = 0; e < kDpl; ++e) a = fmaf(qv[k][e], kk[e], a);
-          part[k][i] = a;
+          for (int e = 0; e < kDpl; e += 2) fma2(a0, a1, qv[k][e], qv[k][e + 1], kk[e], kk[e + 1]);
+          part[k][i] = a0 + a1;
         }
       }
 #pragma unroll
@@ -618,7 +632,8 @@ __global__ void __launch_bounds__(QW == 1 ? kMaxThreads : kMaxThreadsMulti, 1)
 #pragma unroll
           for (int k = 0; k < QW; ++k) {
 #pragma unroll
-            for (int e = 0; e < kDpl; ++e) acc[k][e] = fmaf(pv[k][i], v[e], acc[k][e]);
+            for (int e = 0; e < kDpl; e += 2)
+              fma2(acc[k][e], acc[k][e + 1], pv[k][i], pv[k][i], v[e], v[e + 1]);
             l[k] += pv[k][i];
           }
         }

@@ -240,6 +240,16 @@ def headline_spec4_bf16(seed=4):
                  block_size=16, max_blocks=512, dtype="bf16", lens=lens, rng=rng, query_len=4)
 
 
+def manyrow_gqa4_bf16(seed=3):
+    """The many-row batch with 8 KV heads shared by 32 query heads: a 0.7 GB
+    grouped-query case small enough for a full ncu capture."""
+    rng = np.random.default_rng(seed)
+    real = np.concatenate([[2048], _log_uniform(rng, 239, 128, 2048)])
+    lens = np.concatenate([real, np.zeros(16, dtype=np.int64)])
+    return _make("manyrow_gqa4_bf16", seed, rows=256, heads=32, kv_heads=8, head_dim=128,
+                 block_size=16, max_blocks=128, dtype="bf16", lens=lens, free_frac=0.10, rng=rng)
+
+
 WORKLOADS = {
     "tiny_f32": tiny_f32,
     "uniform_f32": uniform_f32,
@@ -248,6 +258,7 @@ WORKLOADS = {
     "headline_bf16": headline_bf16,
     "headline_gqa4_bf16": headline_gqa4_bf16,
     "headline_spec4_bf16": headline_spec4_bf16,
+    "manyrow_gqa4_bf16": manyrow_gqa4_bf16,
 }
 
 
