@@ -113,8 +113,8 @@ enum {
  * multiple of num_kv_heads with num_heads/num_kv_heads <= 16; head_dim 64 or
  * 128; block_size 16; 1 <= max_blocks with max_blocks*block_size < 2^31;
  * 1 <= num_blocks < 2^31 - 1; query_len 0 or 1 (one query token per row) up
- * to 32 with query_len * num_heads/num_kv_heads <= 32, and <= 16 when that
- * product is not a multiple of 4. */
+ * to 32 with query_len * num_heads/num_kv_heads <= 32, and <= 15 when that
+ * product is odd. */
 typedef struct nsv_shape {
     int32_t rows;
     int32_t num_heads;
@@ -161,12 +161,14 @@ NSV_API int nsv_plan_split(const nsv_shape *shape, int num_sms, nsv_plan *plan);
 /*
  * The same planner with some choices fixed (any argument <= 0 is chosen by
  * the heuristic): kv_heads_per_cta (must divide num_kv_heads), stages (2..8),
- * ctas_per_sm (1..4) and grid (persistent CTAs; default num_sms *
- * ctas_per_sm).  Returns NSV_ERR_RANGE when a fixed choice does not fit the
- * shape or the shared-memory limit.
+ * ctas_per_sm (1..4), grid (persistent CTAs; default num_sms * ctas_per_sm)
+ * and vectors_per_warp (1, 2 or 4, dividing the query vectors per KV head;
+ * at most 16 consumer warps for 1 or 2, 8 for 4).  Returns NSV_ERR_RANGE when
+ * a fixed choice does not fit the shape or the shared-memory limit.
  */
 NSV_API int nsv_plan_custom(const nsv_shape *shape, int num_sms, int kv_heads_per_cta,
-                            int stages, int ctas_per_sm, int grid, nsv_plan *plan);
+                            int stages, int ctas_per_sm, int grid, int vectors_per_warp,
+                            nsv_plan *plan);
 
 /*
  * KV append: for every row r (and each of its query_len new tokens j),

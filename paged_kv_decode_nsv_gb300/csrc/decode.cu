@@ -232,7 +232,7 @@ __device__ __forceinline__ int cta_of(long long u, long long U, int G) {
 }
 
 template <typename T, int D, int QW>
-__global__ void __launch_bounds__(QW == 1 ? kMaxThreads : kMaxThreadsMulti, 1)
+__global__ void __launch_bounds__(QW <= 2 ? kMaxThreads : kMaxThreadsMulti, 1)
     decode_kernel(const DecodeParams p) {
   using E = Elem<T>;
   constexpr int kDpl = E::kDpl;           // dims per lane per 16-byte load

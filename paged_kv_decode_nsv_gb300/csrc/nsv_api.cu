@@ -88,7 +88,7 @@ int check_shape(const nsv_shape* s) {
   return NSV_OK;
 }
 
-int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int grid,
+int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int grid, int qw,
               nsv_plan* p) {
   int rc = check_shape(s);
   if (rc) return rc;
@@ -101,10 +101,18 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   const int elem = elem_bytes(s->dtype);
   const int G = s->num_heads / s->num_kv_heads;
   const int vpk = G * query_len(s);                // query vectors per KV head
-  const int qw = vpk % 4 == 0 ? 4 : (vpk % 2 == 0 ? 2 : 1);  // vectors per warp
+  if (qw <= 0) {
+    // Two vectors per warp when they pair up: one widening of each tile
+    // serves both, and their registers still let 16 warps run per SM (two
+    // CTAs), which measured faster than four vectors on 8 warps.
+    qw = vpk % 2 == 0 ? 2 : 1;
+    if (vpk / qw > max_consumer_warps(qw)) return NSV_ERR_SHAPE;
+  } else if ((qw != 1 && qw != 2 && qw != 4) || vpk % qw != 0 ||
+             vpk / qw > max_consumer_warps(qw)) {
+    return NSV_ERR_RANGE;
+  }
   const int wpk = vpk / qw;                        // consumer warps per KV head
-  const int max_warps = qw == 1 ? kMaxConsumerWarps : kMaxConsumerWarpsMulti;
-  if (wpk > max_warps) return NSV_ERR_SHAPE;
+  const int max_warps = max_consumer_warps(qw);
   const int tile = kBlock * s->head_dim * elem;
   if (hg <= 0) {
     // Largest KV-head group whose K+V stage stays within 64 KiB and whose
@@ -164,7 +172,7 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
 // A caller's plan must be exactly what the planner makes from its choices.
 int check_plan(const nsv_shape* s, const nsv_plan* given, nsv_plan* use) {
   int rc = make_plan(s, given->num_sms, given->kv_heads_per_cta, given->stages,
-                     given->ctas_per_sm, given->grid, use);
+                     given->ctas_per_sm, given->grid, given->vectors_per_warp, use);
   if (rc) return rc;
   if (memcmp(use, given, sizeof(nsv_plan)) != 0) return NSV_ERR_RANGE;
   return NSV_OK;
@@ -197,7 +205,7 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   DeviceState* d = nullptr;
   if ((rc = device_state(&d)) != NSV_OK) return rc;
   if (!plan_in) {
-    if ((rc = make_plan(s, d->num_sms, 0, 0, 0, 0, &plan)) != NSV_OK) return rc;
+    if ((rc = make_plan(s, d->num_sms, 0, 0, 0, 0, 0, &plan)) != NSV_OK) return rc;
   }
   if (s->rows == 0) return NSV_OK;
   if (library_ws) {
@@ -283,12 +291,14 @@ NSV_API const char* nsv_strerror(int code) {
 }
 
 NSV_API int nsv_plan_split(const nsv_shape* shape, int num_sms, nsv_plan* plan) {
-  return make_plan(shape, num_sms, 0, 0, 0, 0, plan);
+  return make_plan(shape, num_sms, 0, 0, 0, 0, 0, plan);
 }
 
 NSV_API int nsv_plan_custom(const nsv_shape* shape, int num_sms, int kv_heads_per_cta,
-                            int stages, int ctas_per_sm, int grid, nsv_plan* plan) {
-  return make_plan(shape, num_sms, kv_heads_per_cta, stages, ctas_per_sm, grid, plan);
+                            int stages, int ctas_per_sm, int grid, int vectors_per_warp,
+                            nsv_plan* plan) {
+  return make_plan(shape, num_sms, kv_heads_per_cta, stages, ctas_per_sm, grid,
+                   vectors_per_warp, plan);
 }
 
 NSV_API int nsv_kv_write(const nsv_shape* s, const void* k_new, const void* v_new,

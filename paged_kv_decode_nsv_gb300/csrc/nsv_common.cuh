@@ -13,9 +13,12 @@ namespace nsv {
 // The kernels are built for this block size (the pages' 16-token blocks).
 constexpr int kBlock = 16;
 // Largest number of consumer warps one decode CTA runs: 16 when each warp
-// serves one query vector, 8 when it serves 2 or 4 (their registers).
+// serves one or two query vectors, 8 when it serves 4 (their registers).
 constexpr int kMaxConsumerWarps = 16;
 constexpr int kMaxConsumerWarpsMulti = 8;
+__host__ __device__ constexpr int max_consumer_warps(int qw) {
+  return qw <= 2 ? kMaxConsumerWarps : kMaxConsumerWarpsMulti;
+}
 // Largest number of query vectors (query heads x query tokens) that share
 // one KV head.
 constexpr int kMaxVectorsPerKvHead = 32;

@@ -66,7 +66,7 @@ _lib.nsv_strerror.argtypes = [_i32]
 _lib.nsv_plan_split.restype = _i32
 _lib.nsv_plan_split.argtypes = [_SP, _i32, _PP]
 _lib.nsv_plan_custom.restype = _i32
-_lib.nsv_plan_custom.argtypes = [_SP, _i32, _i32, _i32, _i32, _i32, _PP]
+_lib.nsv_plan_custom.argtypes = [_SP, _i32, _i32, _i32, _i32, _i32, _i32, _PP]
 _lib.nsv_kv_write.restype = _i32
 _lib.nsv_kv_write.argtypes = [_SP, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.nsv_paged_decode.restype = _i32
@@ -165,11 +165,12 @@ def plan_split(shape, num_sms=0):
     return p
 
 
-def plan_custom(shape, num_sms=0, kv_heads_per_cta=0, stages=0, ctas_per_sm=0, grid=0):
+def plan_custom(shape, num_sms=0, kv_heads_per_cta=0, stages=0, ctas_per_sm=0, grid=0,
+                vectors_per_warp=0):
     p = Plan()
     _check(_lib.nsv_plan_custom(ctypes.byref(shape), int(num_sms), int(kv_heads_per_cta),
-                                int(stages), int(ctas_per_sm), int(grid), ctypes.byref(p)),
-           "nsv_plan_custom")
+                                int(stages), int(ctas_per_sm), int(grid), int(vectors_per_warp),
+                                ctypes.byref(p)), "nsv_plan_custom")
     return p
 
 

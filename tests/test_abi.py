@@ -93,25 +93,34 @@ def test_plan_shapes_of_every_workload(nsv):
 
 
 @pytest.mark.parametrize("heads,kv_heads,qlen,qw,warps", [
-    (32, 32, 1, 1, 8), (32, 8, 1, 4, 8), (32, 32, 4, 4, 8), (32, 32, 2, 2, 8),
-    (32, 32, 3, 1, 6), (16, 1, 1, 4, 4), (32, 8, 8, 4, 8), (8, 8, 5, 1, 5),
+    (32, 32, 1, 1, 8), (32, 8, 1, 2, 8), (32, 32, 4, 2, 8), (32, 32, 2, 2, 8),
+    (32, 32, 3, 1, 6), (16, 1, 1, 2, 8), (32, 8, 8, 2, 16), (8, 8, 5, 1, 5),
 ])
 def test_plan_query_vectors(nsv, heads, kv_heads, qlen, qw, warps):
-    """A consumer warp serves the largest of 4, 2, 1 query vectors that
-    divides the vectors per KV head (query heads per KV head x tokens)."""
+    """By default a consumer warp serves two query vectors when the vectors
+    per KV head (query heads per KV head x tokens) pair up, else one."""
     p = nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen),
                        num_sms=152)
     assert p.vectors_per_warp == qw
     assert p.threads == (warps + 1) * 32
 
 
-@pytest.mark.parametrize("heads,kv_heads,qlen", [(32, 8, 9), (32, 32, 33), (32, 32, 18),
+@pytest.mark.parametrize("heads,kv_heads,qlen", [(32, 8, 9), (32, 32, 33), (32, 32, 17),
                                                  (64, 4, 3)])
 def test_plan_refuses_too_many_query_vectors(nsv, heads, kv_heads, qlen):
     with pytest.raises(nsv.NsvError) as e:
         nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen),
                        num_sms=152)
     assert e.value.code == -3
+
+
+def test_plan_four_vectors_per_warp_on_request(nsv):
+    p = nsv.plan_custom(_shape(nsv, num_kv_heads=8), num_sms=152, vectors_per_warp=4)
+    assert p.vectors_per_warp == 4 and p.threads == 9 * 32
+    with pytest.raises(nsv.NsvError) as e:
+        nsv.plan_custom(_shape(nsv, num_kv_heads=32, query_len=2), num_sms=152,
+                        vectors_per_warp=4)
+    assert e.value.code == -5
 
 
 def test_plan_custom_choices(nsv):

@@ -152,14 +152,19 @@ def test_head_dims_and_dtypes(nsv, dtype, head_dim):
     assert_parity(dtype, gpu_out_f64(out), oracle_step(wl, host))
 
 
+@pytest.mark.parametrize("qw", [0, 1, 4])
 @pytest.mark.parametrize("heads,kv_heads,dtype", [(32, 8, "bf16"), (16, 1, "bf16"),
                                                    (8, 4, "f32"), (12, 3, "bf16")])
-def test_grouped_kv_heads(nsv, heads, kv_heads, dtype):
+def test_grouped_kv_heads(nsv, heads, kv_heads, dtype, qw):
+    G = heads // kv_heads
+    if qw and (G % qw or G // qw > (16 if qw <= 2 else 8)):
+        pytest.skip("this group size cannot give %d vectors per warp" % qw)
     wl = _custom("gqa", [40, 513, 0, 2048, 77, 1], dtype=dtype, heads=heads,
                  kv_heads=kv_heads, seed=11)
     inp = device_inputs(wl)
     host = host_copy(inp)
-    out = gpu_step(wl, inp)
+    shape = nsv.shape_of(inp["q"], inp["k_pool"], inp["block_tables"])
+    out = gpu_step(wl, inp, plan=nsv.plan_custom(shape, vectors_per_warp=qw))
     assert status()[0] == 0
     assert_parity(dtype, gpu_out_f64(out), oracle_step(wl, host))
 
@@ -366,7 +371,9 @@ def test_multi_query_step(nsv, qlen, heads, kv_heads, dtype, head_dim):
 
 
 @pytest.mark.parametrize("kw", [dict(grid=1), dict(grid=5000), dict(stages=2, grid=9),
-                                dict(kv_heads_per_cta=1)])
+                                dict(kv_heads_per_cta=1), dict(vectors_per_warp=4),
+                                dict(vectors_per_warp=1), dict(vectors_per_warp=4, grid=7),
+                                dict(vectors_per_warp=2, kv_heads_per_cta=8)])
 def test_multi_query_plans(nsv, kw):
     wl = W.custom("mq_plans", 61, rows=5, heads=8, kv_heads=8, head_dim=128, block_size=16,
                   max_blocks=70, dtype="bf16", lens=[4, 700, 0, 1100, 33], free_frac=0.2,
