@@ -55,7 +55,8 @@
  *
  * Errors: every entry point returns NSV_OK (0) or a negative NSV_ERR_* code
  * after checking its host-visible arguments; nothing is launched when an
- * error is returned.  Values that live in device memory (context lengths,
+ * error is returned.  A batch of 0 rows is a valid no-op (its data pointers
+ * may be NULL).  Values that live in device memory (context lengths,
  * block ids, write slots) are checked by the kernels themselves: a bad value
  * never causes an out-of-bounds access; the offending row, block or write is
  * skipped and a bit is set in the device status word (nsv_device_status).

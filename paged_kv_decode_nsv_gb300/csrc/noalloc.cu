@@ -69,6 +69,7 @@ extern "C" NSV_API int nsv_paged_decode_noalloc(const nsv_shape* shape, const vo
   nsv_plan plan;
   int rc = nsv_plan_split(shape, 0, &plan);
   if (rc != NSV_OK) return rc;
+  if (shape->rows == 0) return NSV_OK;  // an empty batch: nothing to read
   if (plan.workspace_bytes > (int64_t)kScratchBytes) return NSV_ERR_WORKSPACE;
   void* scratch = nullptr;
   size_t scratch_bytes = 0;

@@ -188,6 +188,7 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
                 cudaStream_t stream) {
   int rc = check_shape(s);
   if (rc) return rc;
+  if (s->rows == 0) return NSV_OK;  // an empty batch: nothing to read
   if (!q || !k_pool || !v_pool || !(block_tables || slots) || !context_lens || !out)
     return NSV_ERR_NULLPTR;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
@@ -306,6 +307,7 @@ NSV_API int nsv_kv_write(const nsv_shape* s, const void* k_new, const void* v_ne
                          cudaStream_t stream) {
   int rc = check_shape(s);
   if (rc) return rc;
+  if (s->rows == 0) return NSV_OK;  // an empty batch: nothing to write
   if (!k_new || !v_new || !write_slots || !k_pool || !v_pool) return NSV_ERR_NULLPTR;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
       (reinterpret_cast<uintptr_t>(write_slots) & 7u))
