@@ -147,9 +147,28 @@ typedef struct nsv_plan {
     int32_t num_sms;          /* SM count the plan was made for */
     int32_t vectors_per_warp; /* query vectors (query heads x query tokens
                                  that share a KV head) one consumer warp
-                                 serves from each K/V tile: 1, 2 or 4 */
+                                 serves from each K/V tile: 1, 2 or 4
+                                 (CUDA-core consumer; 1 for the tensor one) */
+    int32_t consumer;         /* NSV_CONSUMER_CUDA or NSV_CONSUMER_TENSOR */
+    int32_t reserved;         /* 0 */
     int64_t workspace_bytes;  /* device scratch the read needs */
 } nsv_plan;
+
+/* How a CTA's consumer warps fold a K/V tile into the softmax state.
+ *  NSV_CONSUMER_CUDA:   fp32 FMAs on the CUDA cores; a warp serves
+ *                       vectors_per_warp query vectors of one KV head.  Any
+ *                       dtype and shape.
+ *  NSV_CONSUMER_TENSOR: bf16 only.  One warp per KV head runs all of that KV
+ *                       head's query vectors (query heads of the group x
+ *                       query tokens, 2 to 16 of them) as the rows of 16x8x16
+ *                       bf16 tensor-core MMAs with fp32 accumulation: scores
+ *                       Q.K^T and the weighted sum P.V, with the
+ *                       probabilities P rounded to bf16 for the second
+ *                       product.  K/V tiles arrive by 2-D TMA with a 128-byte
+ *                       swizzle.  Needs (num_blocks+1)*num_kv_heads*16 < 2^31.
+ * The default plan takes the tensor consumer for bf16 shapes with 2 to 16
+ * query vectors per KV head, and the CUDA-core one otherwise. */
+enum { NSV_CONSUMER_AUTO = 0, NSV_CONSUMER_CUDA = 1, NSV_CONSUMER_TENSOR = 2 };
 
 /*
  * Plan the decode read for `shape` on a GPU with `num_sms` SMs (<= 0: the
@@ -163,13 +182,16 @@ NSV_API int nsv_plan_split(const nsv_shape *shape, int num_sms, nsv_plan *plan);
  * The same planner with some choices fixed (any argument <= 0 is chosen by
  * the heuristic): kv_heads_per_cta (must divide num_kv_heads), stages (2..8),
  * ctas_per_sm (1..4), grid (persistent CTAs; default num_sms * ctas_per_sm)
- * and vectors_per_warp (1, 2 or 4, dividing the query vectors per KV head;
- * at most 16 consumer warps for 1 or 2, 8 for 4).  Returns NSV_ERR_RANGE when
- * a fixed choice does not fit the shape or the shared-memory limit.
+ * vectors_per_warp (1, 2 or 4, dividing the query vectors per KV head;
+ * at most 16 consumer warps for 1 or 2, 8 for 4; CUDA-core consumer only)
+ * and consumer (NSV_CONSUMER_*; AUTO picks as the default plan does).
+ * Returns NSV_ERR_RANGE when a fixed choice does not fit the shape or the
+ * shared-memory limit, or asks for the tensor consumer where it does not
+ * apply.
  */
 NSV_API int nsv_plan_custom(const nsv_shape *shape, int num_sms, int kv_heads_per_cta,
                             int stages, int ctas_per_sm, int grid, int vectors_per_warp,
-                            nsv_plan *plan);
+                            int consumer, nsv_plan *plan);
 
 /*
  * KV append: for every row r (and each of its query_len new tokens j),
@@ -293,7 +315,7 @@ NSV_API const char *nsv_strerror(int code);
 /* ABI version of this header (major * 100 + minor). */
 NSV_API int nsv_abi_version(void);
 
-#define NSV_ABI_VERSION 100
+#define NSV_ABI_VERSION 101
 
 #ifdef __cplusplus
 }

@@ -125,6 +125,57 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// One 2-D TMA tile load global -> this CTA's shared memory (the tensor map's
+// box, with its swizzle), completing on `bar`.  x is the innermost coordinate.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
+                                            uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// Four 8x8 bf16 matrices from shared memory (row addresses from lanes 8i..8i+7).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// The same, each matrix transposed.
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D += A(16x16, bf16, row) * B(16x8, bf16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Byte offset of 16-byte chunk `dc` (dims 8*dc .. 8*dc+7) of row r of a K
+// or V tile set staged by 128-byte-swizzled TMA loads: the dims are split in
+// 64-dim halves of half_bytes each, a row of a half is 128 bytes, and chunk c
+// of row r sits at position c ^ (r % 8).
+__device__ __forceinline__ uint32_t swz(int r, int dc, uint32_t half_bytes) {
+  return (uint32_t)(dc >> 3) * half_bytes + (uint32_t)r * 128u +
+         ((uint32_t)((dc & 7) ^ (r & 7)) << 4);
+}
+
 // ---------------------------------------------------------------------------
 // element traits: a lane loads 16 bytes = kDpl elements and widens to fp32
 
@@ -231,9 +282,320 @@ __device__ __forceinline__ int cta_of(long long u, long long U, int G) {
   return (int)(c < G - 1 ? c : G - 1);
 }
 
-template <typename T, int D, int QW>
-__global__ void __launch_bounds__(QW <= 2 ? kMaxThreads : kMaxThreadsMulti, 1)
-    decode_kernel(const DecodeParams p) {
+// A consumer warp has written its partials of a cut row (the row's pieces
+// lie on CTAs c0..c1).  Count this CTA's piece once it is published; the CTA
+// whose piece arrives last merges every piece, each of its warps for its own
+// query vectors [v0, v0 + nv).  Nobody waits for another CTA: the last
+// arrival finds every partial already written.
+template <typename T, int D>
+__device__ __forceinline__ void finish_cut_row(const DecodeParams& p, int row, int kv0,
+                                               const int* s_prefix, int N, long long U, int nhg,
+                                               int nvec, int v0, int nv, int ncw, int cw,
+                                               int lane, volatile int* s_merge) {
+  const int G = p.group, NQ = p.query_len, HG = p.heads_per_cta;
+  const int vpk = G * NQ;
+  __threadfence();
+  consumer_sync(ncw * 32);
+  const int hg = kv0 / HG;
+  const int pr = s_prefix[row], nb = s_prefix[row + 1] - pr;
+  const long long u0 = (long long)hg * N + pr, u1 = u0 + nb;
+  const int c0 = cta_of(u0, U, gridDim.x), c1 = cta_of(u1 - 1, U, gridDim.x);
+  if (cw == 0 && lane == 0) {
+    int pieces = c1 - c0 + 1;
+    if (U < gridDim.x) {  // some CTAs have no units and wrote nothing
+      pieces = 0;
+      for (int c = c0; c <= c1; ++c)
+        pieces += ((long long)(c + 1) * U / gridDim.x != (long long)c * U / gridDim.x);
+    }
+    int* cnt = p.ws_cnt + (size_t)row * nhg + hg;
+    const int before = atomicAdd(cnt, 1);
+    const bool last = before == pieces - 1;
+    if (last) *cnt = 0;  // every piece has arrived: nobody touches it again
+    *s_merge = last ? 1 : 0;
+  }
+  consumer_sync(ncw * 32);
+  if (!*s_merge) return;
+  // Lane l owns dims [l*D/32, (l+1)*D/32).
+  __threadfence();
+  constexpr int kPer = D / 32;
+  const int ns = c1 - c0 + 1;
+  const int qh0 = kv0 * G;
+  for (int k = 0; k < nv; ++k) {
+    const int vv = v0 + k;
+    const int kvl = vv / vpk, rem = vv - kvl * vpk;
+    const int qh = qh0 + kvl * G + rem / NQ, jq = rem % NQ;
+    float M = -INFINITY;
+    for (int kk = lane; kk < ns; kk += 32) {
+      const int c = c0 + kk;
+      const long long sc = (long long)c * U / gridDim.x;
+      if ((long long)(c + 1) * U / gridDim.x == sc) continue;  // CTA with no units
+      const int sl = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
+      M = fmaxf(M, __ldcg(&p.ws_ml[(size_t)sl * nvec + vv]).x);
+    }
+#pragma unroll
+    for (int o2 = 16; o2 >= 1; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
+    float Lsum = 0.f, a[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) a[e] = 0.f;
+    for (int base = 0; base < ns; base += 32) {
+      const int c = c0 + base + lane;
+      float w = 0.f;
+      int idx = 0;
+      if (base + lane < ns) {
+        const long long sc = (long long)c * U / gridDim.x;
+        if ((long long)(c + 1) * U / gridDim.x != sc) {
+          const int sl = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
+          idx = sl * nvec + vv;
+          const float2 ml = __ldcg(&p.ws_ml[idx]);
+          w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+          Lsum = fmaf(w, ml.y, Lsum);
+        }
+      }
+      const int cnt = min(32, ns - base);
+      for (int kk = 0; kk < cnt; ++kk) {
+        const float wk = __shfl_sync(kFull, w, kk);
+        const int ik = __shfl_sync(kFull, idx, kk);
+        if (wk != 0.f) {
+          const float* src = p.ws_acc + (size_t)ik * D + lane * kPer;
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) a[e] = fmaf(wk, __ldcg(src + e), a[e]);
+        }
+      }
+    }
+#pragma unroll
+    for (int o2 = 16; o2 >= 1; o2 >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, o2);
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    T* o = static_cast<T*>(p.out) + (((size_t)row * NQ + jq) * p.heads + qh) * D + lane * kPer;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      if constexpr (sizeof(T) == 4) {
+        o[e] = a[e] * inv;
+      } else {
+        o[e] = __float2bfloat16_rn(a[e] * inv);
+      }
+    }
+  }
+}
+
+// Tensor-core consumer (bf16): one warp per KV head of the group; its query
+// vectors (the group's query heads of that KV head times the query tokens,
+// at most 16) are the rows of mma.sync.m16n8k16 (bf16 inputs, fp32
+// accumulate).  Per 16-token block: S = Q.K^T from the K tile staged by
+// swizzled TMA loads and read with ldmatrix, the online softmax on the score
+// fragments, then O += P.V with P (bf16) taken straight from the score
+// fragments and V read with ldmatrix.trans.  Fragment layout of m16n8k16:
+// lane = 4*g + t4 holds rows g and g+8, columns 2*t4 and 2*t4+1.
+template <int D>
+__device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char* smem,
+                                            const SmemLayout& L, const int4* s_meta,
+                                            uint32_t bars, const int* s_prefix,
+                                            volatile int* s_abort, int N, long long U, int nhg,
+                                            int nvec, int ncw, int warp, int lane) {
+  using T = __nv_bfloat16;
+  constexpr int kKs = D / 16;  // k-steps of the score MMA
+  constexpr int kNd = D / 8;   // n-tiles of the P.V MMA
+  const int G = p.group, NQ = p.query_len, HG = p.heads_per_cta, S = p.stages;
+  if (warp > ncw) return;
+  const int cw = warp - 1;
+  const int kvl = cw;                   // one warp per KV head of the group
+  const int vpk = G * NQ;               // its query vectors (<= 16)
+  const int vbase = kvl * vpk;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int hq = HG * G;
+  const uint32_t half_bytes = (uint32_t)HG * kBlock * 128;
+  volatile int* s_merge = s_abort + 1;
+
+  // rows g and g + 8 of the MMA: their query head within the group and token
+  int rqh[2], rjq[2];
+  bool rok[2];
+#pragma unroll
+  for (int rh = 0; rh < 2; ++rh) {
+    const int r = g + 8 * rh;
+    rok[rh] = r < vpk;
+    const int rr = rok[rh] ? r : 0;
+    rqh[rh] = kvl * G + rr / NQ;
+    rjq[rh] = rr % NQ;
+  }
+
+  // Empty rows see nothing: zeros for all their (token, head) vectors.
+  constexpr int kChunks = D * 2 / 16;
+  for (int r = blockIdx.x; r < p.rows; r += gridDim.x) {
+    if (s_prefix[r + 1] != s_prefix[r]) continue;
+    for (int vh = cw; vh < NQ * p.heads; vh += ncw)
+      for (int c = lane; c < kChunks; c += 32)
+        reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)r * NQ * p.heads + vh) * D)[c] =
+            make_uint4(0u, 0u, 0u, 0u);
+  }
+
+  uint32_t qa[kKs][4];
+  float o[kNd][4], m[2], l[2];
+#pragma unroll
+  for (int ks = 0; ks < kKs; ++ks) qa[ks][0] = qa[ks][1] = qa[ks][2] = qa[ks][3] = 0u;
+#pragma unroll
+  for (int nd = 0; nd < kNd; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+  m[0] = m[1] = -INFINITY;
+  l[0] = l[1] = 0.f;
+
+  for (uint32_t n = 0;; ++n) {
+    const uint32_t s = n % S;
+    if (!mbar_wait(bars + 8 * s, (n / S) & 1)) {
+      if (lane == 0) atomicOr(p.status, (uint32_t)NSV_DEV_TIMEOUT);
+      *s_abort = 1;
+      return;
+    }
+    const int4 meta = s_meta[s];
+    const int flags = meta.w;
+    if (flags & kEnd) break;
+    unsigned char* st = smem + s * L.stage_bytes;
+    const uint32_t kbase = smem_u32(st), vbase_s = kbase + L.kv_bytes;
+    const int tmask = meta.y;
+    const int qh0 = (flags >> 16) * G;
+
+    if (flags & kFirst) {
+      m[0] = m[1] = -INFINITY;
+      l[0] = l[1] = 0.f;
+#pragma unroll
+      for (int nd = 0; nd < kNd; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+      if (flags & kHasQ) {
+        const unsigned char* qs = st + 2 * L.kv_bytes;
+#pragma unroll
+        for (int ks = 0; ks < kKs; ++ks) {
+#pragma unroll
+          for (int rh = 0; rh < 2; ++rh) {
+            const unsigned char* row =
+                qs + ((size_t)(rjq[rh] * hq + rqh[rh]) * D + ks * 16 + t4 * 2) * sizeof(T);
+            qa[ks][rh] = rok[rh] ? *reinterpret_cast<const uint32_t*>(row) : 0u;
+            qa[ks][2 + rh] = rok[rh] ? *reinterpret_cast<const uint32_t*>(row + 16) : 0u;
+          }
+        }
+      }
+    }
+
+    if (flags & kData) {
+      const int rem = flags & 0xff;
+      const int nvalid = min(kBlock, rem);
+      // V rows that hold no data (past the row's length, or tokens the
+      // producer did not gather) become zeros: P is 0 there, but 0 * NaN is not.
+      if (nvalid < kBlock || tmask != 0xffff) {
+        for (int c = lane; c < kBlock * kChunks; c += 32) {
+          const int t = c / kChunks, dc = c - t * kChunks;
+          if (!(t < nvalid && ((tmask >> t) & 1)))
+            *reinterpret_cast<uint4*>(st + L.kv_bytes + swz(kvl * kBlock + t, dc, half_bytes)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      // scores: 2 n-tiles of 8 tokens, kKs k-steps of 16 dims
+      float sc[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+      {
+        const int mi = lane >> 3, i = lane & 7;
+        const int r = kvl * kBlock + (mi >> 1) * 8 + i;
+#pragma unroll
+        for (int ks = 0; ks < kKs; ++ks) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kbase + swz(r, ks * 2 + (mi & 1), half_bytes), b0, b1, b2, b3);
+          mma_bf16(sc[0], qa[ks], b0, b1);
+          mma_bf16(sc[1], qa[ks], b2, b3);
+        }
+      }
+      // online softmax per row (a row's 16 scores sit on 4 lanes)
+      uint32_t pa[4];
+#pragma unroll
+      for (int rh = 0; rh < 2; ++rh) {
+        const int nv = rem - (NQ - 1 - rjq[rh]);  // positions this row's query sees
+        float x[4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int tok = nt * 8 + t4 * 2 + e;
+            const bool ok = rok[rh] && tok < nv && ((tmask >> tok) & 1);
+            x[nt * 2 + e] = ok ? sc[nt][rh * 2 + e] * p.qscale : -INFINITY;
+          }
+        }
+        float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+        const float mn = fmaxf(m[rh], mx);
+        const float alpha = (mn == -INFINITY) ? 1.f : exp2f(m[rh] - mn);
+        m[rh] = mn;
+        l[rh] *= alpha;
+#pragma unroll
+        for (int nd = 0; nd < kNd; ++nd) {
+          o[nd][rh * 2] *= alpha;
+          o[nd][rh * 2 + 1] *= alpha;
+        }
+        float pv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          pv[e] = (x[e] == -INFINITY) ? 0.f : exp2f(x[e] - mn);
+          l[rh] += pv[e];
+        }
+        pa[rh] = pack_bf16(pv[0], pv[1]);      // row rh*8 + g, tokens 2*t4, 2*t4+1
+        pa[2 + rh] = pack_bf16(pv[2], pv[3]);  // the same row, tokens 8 + 2*t4, ...
+      }
+      // O += P.V: n-tiles of 8 dims, V read transposed
+      {
+        const int mi = lane >> 3, i = lane & 7;
+        const int r = kvl * kBlock + (mi & 1) * 8 + i;
+#pragma unroll
+        for (int nd = 0; nd < kNd; nd += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vbase_s + swz(r, nd + (mi >> 1), half_bytes), b0, b1, b2, b3);
+          mma_bf16(o[nd], pa, b0, b1);
+          mma_bf16(o[nd + 1], pa, b2, b3);
+        }
+      }
+    }
+
+    if (flags & kLast) {
+      const int row = meta.x;
+      float lt[2];
+#pragma unroll
+      for (int rh = 0; rh < 2; ++rh) {
+        lt[rh] = l[rh];
+        lt[rh] += __shfl_xor_sync(kFull, lt[rh], 1);
+        lt[rh] += __shfl_xor_sync(kFull, lt[rh], 2);
+      }
+      if (flags & kFinal) {
+#pragma unroll
+        for (int rh = 0; rh < 2; ++rh) {
+          if (!rok[rh]) continue;
+          const float inv = lt[rh] > 0.f ? 1.f / lt[rh] : 0.f;
+          T* out = static_cast<T*>(p.out) +
+                   (((size_t)row * NQ + rjq[rh]) * p.heads + qh0 + rqh[rh]) * D + t4 * 2;
+#pragma unroll
+          for (int nd = 0; nd < kNd; ++nd)
+            *reinterpret_cast<uint32_t*>(out + nd * 8) =
+                pack_bf16(o[nd][rh * 2] * inv, o[nd][rh * 2 + 1] * inv);
+        }
+      } else {
+#pragma unroll
+        for (int rh = 0; rh < 2; ++rh) {
+          if (!rok[rh]) continue;
+          const size_t slot = (size_t)meta.z * nvec + vbase + g + 8 * rh;
+          float* a = p.ws_acc + slot * D + t4 * 2;
+#pragma unroll
+          for (int nd = 0; nd < kNd; ++nd)
+            *reinterpret_cast<float2*>(a + nd * 8) = make_float2(o[nd][rh * 2], o[nd][rh * 2 + 1]);
+          if (t4 == 0) p.ws_ml[slot] = make_float2(m[rh], lt[rh]);
+        }
+        finish_cut_row<T, D>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, vbase, vpk, ncw, cw,
+                             lane, s_merge);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (S + s));
+  }
+}
+
+template <typename T, int D, int QW, bool MMA>
+__global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
+                                      : (QW <= 2 ? kMaxThreads : kMaxThreadsMulti), 1)
+    decode_kernel(const __grid_constant__ DecodeParams p) {
   using E = Elem<T>;
   constexpr int kDpl = E::kDpl;           // dims per lane per 16-byte load
   constexpr int kLpt = D / kDpl;          // lanes per token row
@@ -243,12 +605,15 @@ __global__ void __launch_bounds__(QW <= 2 ? kMaxThreads : kMaxThreadsMulti, 1)
   static_assert(kLpt * kDpl == D && kLpt <= 32 && kNp >= 4 && kNp <= kLpt, "tile shape");
   static_assert(kDup * kNp == kLpt && kNp % 4 == 0, "butterfly shape");
 
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1024-byte aligned base (the layout's total carries the slack)
+  unsigned char* const smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int G = p.group;
   const int NQ = p.query_len;
   const int HG = p.heads_per_cta;
   const int nvec = HG * G * NQ;          // query vectors per CTA
-  const int ncw = nvec / QW;             // consumer warps
+  const int ncw = MMA ? HG : nvec / QW;  // consumer warps
   const int S = p.stages;
   const SmemLayout L = make_layout((int)sizeof(T), D, HG, nvec, S, p.rows);
 
@@ -311,6 +676,7 @@ __global__ void __launch_bounds__(QW <= 2 ? kMaxThreads : kMaxThreadsMulti, 1)
     const T* vp = static_cast<const T*>(p.v_pool);
     const T* qp = static_cast<const T*>(p.q);
     const uint32_t q_slice = L.q_bytes / NQ;   // one query token's heads of the group
+    const uint32_t half_bytes = (uint32_t)HG * kBlock * 128;  // swizzled 64-dim half
     const int slot0 = blockIdx.x * 2;
     unsigned long long walked = 0;
     uint32_t n = 0;  // fills issued (meaningful in lane 0)
@@ -370,9 +736,19 @@ __global__ void __launch_bounds__(QW <= 2 ? kMaxThreads : kMaxThreadsMulti, 1)
         mbar_arrive_tx(full, bytes);
         const uint32_t base = smem_u32(smem + s * L.stage_bytes);
         if ((flags & kData) && !(flags & kGathered)) {
-          const size_t off = (size_t)phys * block_elems + (size_t)kv0 * tile_elems;
-          bulk_g2s(base, kp + off, L.kv_bytes, full, pol);
-          bulk_g2s(base + L.kv_bytes, vp + off, L.kv_bytes, full, pol);
+          if constexpr (MMA) {
+            // 64-dim halves of the group's [HG * block, D] tile rows, swizzled
+            const int y = (phys * p.kv_heads + kv0) * kBlock;
+#pragma unroll
+            for (int h2 = 0; h2 < D / 64; ++h2) {
+              tma_load_2d(base + h2 * half_bytes, &p.tmap_k, h2 * 64, y, full, pol);
+              tma_load_2d(base + L.kv_bytes + h2 * half_bytes, &p.tmap_v, h2 * 64, y, full, pol);
+            }
+          } else {
+            const size_t off = (size_t)phys * block_elems + (size_t)kv0 * tile_elems;
+            bulk_g2s(base, kp + off, L.kv_bytes, full, pol);
+            bulk_g2s(base + L.kv_bytes, vp + off, L.kv_bytes, full, pol);
+          }
         }
         if (flags & kHasQ) {
           for (int jq = 0; jq < NQ; ++jq)
@@ -419,8 +795,9 @@ __global__ void __launch_bounds__(QW <= 2 ? kMaxThreads : kMaxThreadsMulti, 1)
         const long long sl = sp[t];
         const T* src = (which ? vp : kp) +
                        (((size_t)(sl / kBlock) * p.kv_heads + kv0 + h) * kBlock + sl % kBlock) * D;
-        *reinterpret_cast<uint4*>(stg + which * L.kv_bytes + (((size_t)h * kBlock + t) * D) *
-                                  sizeof(T) + v * 16) =
+        const uint32_t dst = MMA ? swz(h * kBlock + t, v, half_bytes)
+                                 : (uint32_t)((((size_t)h * kBlock + t) * D) * sizeof(T) + v * 16);
+        *reinterpret_cast<uint4*>(stg + which * L.kv_bytes + dst) =
             *(reinterpret_cast<const uint4*>(src) + v);
       }
       fence_proxy_async_smem();
@@ -479,6 +856,10 @@ __global__ void __launch_bounds__(QW <= 2 ? kMaxThreads : kMaxThreadsMulti, 1)
   }
 
   // -------------------------------------------------------------------- consumers
+  if constexpr (MMA) {
+    consume_mma<D>(p, smem, L, s_meta, bars, s_prefix, s_abort, N, U, nhg, nvec, ncw, warp, lane);
+    return;
+  } else {
   // A consumer warp serves QW query vectors that read the same KV head: the
   // group's query heads of that KV head and the row's query tokens, so each
   // K/V tile is loaded and widened once for all of them.  Vector v of the CTA
@@ -680,118 +1061,47 @@ __global__ void __launch_bounds__(QW <= 2 ? kMaxThreads : kMaxThreadsMulti, 1)
           }
           if (lane == 0) p.ws_ml[slot] = make_float2(m[k], lt[k]);
         }
-        // Publish this CTA's piece of the row and count it.
-        __threadfence();
-        consumer_sync(ncw * 32);
-        const int hg = (flags >> 16) / HG;
-        const int pr = s_prefix[row], nb = s_prefix[row + 1] - pr;
-        const long long u0 = (long long)hg * N + pr, u1 = u0 + nb;
-        const int c0 = cta_of(u0, U, gridDim.x), c1 = cta_of(u1 - 1, U, gridDim.x);
-        if (cw == 0 && lane == 0) {
-          int pieces = c1 - c0 + 1;
-          if (U < gridDim.x) {  // some CTAs have no units and wrote nothing
-            pieces = 0;
-            for (int c = c0; c <= c1; ++c)
-              pieces += ((long long)(c + 1) * U / gridDim.x != (long long)c * U / gridDim.x);
-          }
-          int* cnt = p.ws_cnt + (size_t)row * nhg + hg;
-          const int before = atomicAdd(cnt, 1);
-          const bool last = before == pieces - 1;
-          if (last) *cnt = 0;  // every piece has arrived: nobody touches it again
-          *s_merge = last ? 1 : 0;
-        }
-        consumer_sync(ncw * 32);
-        if (*s_merge) {
-          // The last piece to arrive merges all pieces of the row for the
-          // warp's vectors.  Lane l owns dims [l*D/32, (l+1)*D/32).
-          __threadfence();
-          constexpr int kPer = D / 32;
-          const int ns = c1 - c0 + 1;
-          for (int k = 0; k < QW; ++k) {
-            const int vv = v0 + k;
-            float M = -INFINITY;
-            for (int kk = lane; kk < ns; kk += 32) {
-              const int c = c0 + kk;
-              const long long sc = (long long)c * U / gridDim.x;
-              if ((long long)(c + 1) * U / gridDim.x == sc) continue;  // CTA with no units
-              const int sl = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
-              M = fmaxf(M, __ldcg(&p.ws_ml[(size_t)sl * nvec + vv]).x);
-            }
-#pragma unroll
-            for (int o2 = 16; o2 >= 1; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
-            float Lsum = 0.f, a[kPer];
-#pragma unroll
-            for (int e = 0; e < kPer; ++e) a[e] = 0.f;
-            for (int base = 0; base < ns; base += 32) {
-              const int c = c0 + base + lane;
-              float w = 0.f;
-              int idx = 0;
-              if (base + lane < ns) {
-                const long long sc = (long long)c * U / gridDim.x;
-                if ((long long)(c + 1) * U / gridDim.x != sc) {
-                  const int sl = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
-                  idx = sl * nvec + vv;
-                  const float2 ml = __ldcg(&p.ws_ml[idx]);
-                  w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-                  Lsum = fmaf(w, ml.y, Lsum);
-                }
-              }
-              const int cnt = min(32, ns - base);
-              for (int kk = 0; kk < cnt; ++kk) {
-                const float wk = __shfl_sync(kFull, w, kk);
-                const int ik = __shfl_sync(kFull, idx, kk);
-                if (wk != 0.f) {
-                  const float* src = p.ws_acc + (size_t)ik * D + lane * kPer;
-#pragma unroll
-                  for (int e = 0; e < kPer; ++e) a[e] = fmaf(wk, __ldcg(src + e), a[e]);
-                }
-              }
-            }
-#pragma unroll
-            for (int o2 = 16; o2 >= 1; o2 >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, o2);
-            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-            T* o = static_cast<T*>(p.out) +
-                   (((size_t)row * NQ + jq[k]) * p.heads + qh0 + qhl[k]) * D + lane * kPer;
-#pragma unroll
-            for (int e = 0; e < kPer; ++e) {
-              if constexpr (sizeof(T) == 4) {
-                o[e] = a[e] * inv;
-              } else {
-                o[e] = __float2bfloat16_rn(a[e] * inv);
-              }
-            }
-          }
-        }
+        finish_cut_row<T, D>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, v0, QW, ncw, cw, lane,
+                             s_merge);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (S + s));
   }
+  }  // CUDA-core consumer
 }
 
-template <typename T, int D, int QW>
+template <typename T, int D, int QW, bool MMA>
 cudaError_t set_attr() {
-  return cudaFuncSetAttribute(decode_kernel<T, D, QW>,
+  return cudaFuncSetAttribute(decode_kernel<T, D, QW, MMA>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
 }
 
 template <typename T, int D>
 cudaError_t set_attrs() {
   cudaError_t e;
-  if ((e = set_attr<T, D, 1>()) != cudaSuccess) return e;
-  if ((e = set_attr<T, D, 2>()) != cudaSuccess) return e;
-  return set_attr<T, D, 4>();
+  if ((e = set_attr<T, D, 1, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<T, D, 2, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<T, D, 4, false>()) != cudaSuccess) return e;
+  if constexpr (sizeof(T) == 2) return set_attr<T, D, 1, true>();
+  return cudaSuccess;
 }
 
 template <typename T, int D>
-void launch_typed(const DecodeParams& p, int qw, int grid, int threads, int smem,
+void launch_typed(const DecodeParams& p, int qw, int consumer, int grid, int threads, int smem,
                   cudaStream_t stream) {
+  if constexpr (sizeof(T) == 2) {
+    if (consumer == kConsumerTensor) {
+      decode_kernel<T, D, 1, true><<<grid, threads, smem, stream>>>(p);
+      return;
+    }
+  }
   if (qw == 4)
-    decode_kernel<T, D, 4><<<grid, threads, smem, stream>>>(p);
+    decode_kernel<T, D, 4, false><<<grid, threads, smem, stream>>>(p);
   else if (qw == 2)
-    decode_kernel<T, D, 2><<<grid, threads, smem, stream>>>(p);
+    decode_kernel<T, D, 2, false><<<grid, threads, smem, stream>>>(p);
   else
-    decode_kernel<T, D, 1><<<grid, threads, smem, stream>>>(p);
+    decode_kernel<T, D, 1, false><<<grid, threads, smem, stream>>>(p);
 }
 
 }  // namespace
@@ -804,18 +1114,18 @@ cudaError_t prepare_decode_kernels() {
   return set_attrs<__nv_bfloat16, 128>();
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int qw, int grid,
-                          int threads, int smem, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int qw, int consumer,
+                          int grid, int threads, int smem, cudaStream_t stream) {
   if (dtype == NSV_F32) {
     if (head_dim == 64)
-      launch_typed<float, 64>(p, qw, grid, threads, smem, stream);
+      launch_typed<float, 64>(p, qw, consumer, grid, threads, smem, stream);
     else
-      launch_typed<float, 128>(p, qw, grid, threads, smem, stream);
+      launch_typed<float, 128>(p, qw, consumer, grid, threads, smem, stream);
   } else {
     if (head_dim == 64)
-      launch_typed<__nv_bfloat16, 64>(p, qw, grid, threads, smem, stream);
+      launch_typed<__nv_bfloat16, 64>(p, qw, consumer, grid, threads, smem, stream);
     else
-      launch_typed<__nv_bfloat16, 128>(p, qw, grid, threads, smem, stream);
+      launch_typed<__nv_bfloat16, 128>(p, qw, consumer, grid, threads, smem, stream);
   }
   return cudaGetLastError();
 }

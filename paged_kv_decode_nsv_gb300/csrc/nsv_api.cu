@@ -2,6 +2,7 @@
 // shape-only launch planner, per-device state (the device status word and
 // the library-owned workspace) and the entry points.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -36,6 +37,14 @@ struct DeviceState {
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point
+// so that the library needs no link against libcuda.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
 int cuda_fail() {
   (void)cudaGetLastError();  // do not leave a stale error for the next caller
   return NSV_ERR_CUDA;
@@ -57,6 +66,15 @@ int device_state(DeviceState** out) {
     if (prepare_decode_kernels() != cudaSuccess) return cuda_fail();
     if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return cuda_fail();
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return cuda_fail();
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
     d.ready = true;
   }
   *out = &d;
@@ -88,8 +106,15 @@ int check_shape(const nsv_shape* s) {
   return NSV_OK;
 }
 
+// Rows of the [block][kv_head][token] pool seen as one 2-D tensor of
+// head_dim-wide rows, the tensor consumer's TMA view; its row coordinate is
+// a signed 32-bit value.
+bool tensor_rows_fit(const nsv_shape* s) {
+  return (s->num_blocks + 1) * (int64_t)s->num_kv_heads * kBlock < (int64_t(1) << 31);
+}
+
 int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int grid, int qw,
-              nsv_plan* p) {
+              int consumer, nsv_plan* p) {
   int rc = check_shape(s);
   if (rc) return rc;
   if (!p) return NSV_ERR_NULLPTR;
@@ -101,7 +126,20 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   const int elem = elem_bytes(s->dtype);
   const int G = s->num_heads / s->num_kv_heads;
   const int vpk = G * query_len(s);                // query vectors per KV head
-  if (qw <= 0) {
+  const bool tensor_ok = s->dtype == NSV_BF16 && vpk >= 2 && vpk <= kMmaRows &&
+                         tensor_rows_fit(s);
+  if (consumer == NSV_CONSUMER_AUTO) {
+    // The tensor cores pay off once several query vectors share a K/V tile:
+    // one MMA row each, where the CUDA cores repeat the work per vector.
+    consumer = (tensor_ok && qw <= 0) ? kConsumerTensor : kConsumerCuda;
+  } else if (consumer == kConsumerTensor) {
+    if (!tensor_ok || qw > 1) return NSV_ERR_RANGE;
+  } else if (consumer != kConsumerCuda) {
+    return NSV_ERR_RANGE;
+  }
+  if (consumer == kConsumerTensor) {
+    qw = 1;  // unused: a warp runs its KV head's vectors as MMA rows
+  } else if (qw <= 0) {
     // Two vectors per warp when they pair up: one widening of each tile
     // serves both, and their registers still let 16 warps run per SM (two
     // CTAs), which measured faster than four vectors on 8 warps.
@@ -111,8 +149,9 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
              vpk / qw > max_consumer_warps(qw)) {
     return NSV_ERR_RANGE;
   }
-  const int wpk = vpk / qw;                        // consumer warps per KV head
-  const int max_warps = max_consumer_warps(qw);
+  const bool tensor = consumer == kConsumerTensor;
+  const int wpk = tensor ? 1 : vpk / qw;           // consumer warps per KV head
+  const int max_warps = tensor ? kMaxConsumerWarpsMulti : max_consumer_warps(qw);
   const int tile = kBlock * s->head_dim * elem;
   if (hg <= 0) {
     // Largest KV-head group whose K+V stage stays within 64 KiB and whose
@@ -165,6 +204,7 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   p->smem_bytes = (int)L.total;
   p->num_sms = num_sms;
   p->vectors_per_warp = qw;
+  p->consumer = consumer;
   p->workspace_bytes = (int64_t)W.total;
   return NSV_OK;
 }
@@ -172,7 +212,8 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
 // A caller's plan must be exactly what the planner makes from its choices.
 int check_plan(const nsv_shape* s, const nsv_plan* given, nsv_plan* use) {
   int rc = make_plan(s, given->num_sms, given->kv_heads_per_cta, given->stages,
-                     given->ctas_per_sm, given->grid, given->vectors_per_warp, use);
+                     given->ctas_per_sm, given->grid, given->vectors_per_warp,
+                     given->consumer, use);
   if (rc) return rc;
   if (memcmp(use, given, sizeof(nsv_plan)) != 0) return NSV_ERR_RANGE;
   return NSV_OK;
@@ -206,7 +247,7 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   DeviceState* d = nullptr;
   if ((rc = device_state(&d)) != NSV_OK) return rc;
   if (!plan_in) {
-    if ((rc = make_plan(s, d->num_sms, 0, 0, 0, 0, 0, &plan)) != NSV_OK) return rc;
+    if ((rc = make_plan(s, d->num_sms, 0, 0, 0, 0, 0, 0, &plan)) != NSV_OK) return rc;
   }
   if (s->rows == 0) return NSV_OK;
   if (library_ws) {
@@ -260,8 +301,27 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   p.query_len = query_len(s);
   p.stages = plan.stages;
   p.qscale = scale * 1.4426950408889634f;  // log2(e): the kernels use exp2
-  if (launch_decode(p, s->dtype, s->head_dim, plan.vectors_per_warp, plan.grid, plan.threads,
-                    plan.smem_bytes, stream) != cudaSuccess)
+  memset(&p.tmap_k, 0, sizeof(p.tmap_k));
+  memset(&p.tmap_v, 0, sizeof(p.tmap_v));
+  if (plan.consumer == kConsumerTensor) {
+    // The pools as [(num_blocks+1)*kv_heads*16 rows][head_dim] bf16; a box is
+    // 64 dims (128 bytes, the swizzle span) by the head group's 16-token tiles.
+    const cuuint64_t dims[2] = {(cuuint64_t)s->head_dim,
+                                (cuuint64_t)(s->num_blocks + 1) * s->num_kv_heads * kBlock};
+    const cuuint64_t strides[1] = {(cuuint64_t)s->head_dim * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)(plan.kv_heads_per_cta * kBlock)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    for (int i = 0; i < 2; ++i) {
+      if (g_encode(i == 0 ? &p.tmap_k : &p.tmap_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(i == 0 ? k_pool : v_pool), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return NSV_ERR_CUDA;
+    }
+  }
+  if (launch_decode(p, s->dtype, s->head_dim, plan.vectors_per_warp, plan.consumer, plan.grid,
+                    plan.threads, plan.smem_bytes, stream) != cudaSuccess)
     return cuda_fail();
   return NSV_OK;
 }
@@ -292,14 +352,14 @@ NSV_API const char* nsv_strerror(int code) {
 }
 
 NSV_API int nsv_plan_split(const nsv_shape* shape, int num_sms, nsv_plan* plan) {
-  return make_plan(shape, num_sms, 0, 0, 0, 0, 0, plan);
+  return make_plan(shape, num_sms, 0, 0, 0, 0, 0, 0, plan);
 }
 
 NSV_API int nsv_plan_custom(const nsv_shape* shape, int num_sms, int kv_heads_per_cta,
                             int stages, int ctas_per_sm, int grid, int vectors_per_warp,
-                            nsv_plan* plan) {
+                            int consumer, nsv_plan* plan) {
   return make_plan(shape, num_sms, kv_heads_per_cta, stages, ctas_per_sm, grid,
-                   vectors_per_warp, plan);
+                   vectors_per_warp, consumer, plan);
 }
 
 NSV_API int nsv_kv_write(const nsv_shape* s, const void* k_new, const void* v_new,

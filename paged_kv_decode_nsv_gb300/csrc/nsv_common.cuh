@@ -3,6 +3,7 @@
 // identically on host and device), and the launchers each .cu file exports.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,6 +23,10 @@ __host__ __device__ constexpr int max_consumer_warps(int qw) {
 // Largest number of query vectors (query heads x query tokens) that share
 // one KV head.
 constexpr int kMaxVectorsPerKvHead = 32;
+// The tensor-core consumer: one warp per KV head, its query vectors are the
+// rows of one 16-row MMA.
+constexpr int kMmaRows = 16;
+enum : int { kConsumerCuda = 1, kConsumerTensor = 2 };
 constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
 constexpr int kMaxThreadsMulti = (kMaxConsumerWarpsMulti + 1) * 32;
 // Largest batch the decode kernel's per-CTA row tables hold.
@@ -65,6 +70,10 @@ __host__ __device__ inline WsLayout make_ws_layout(int rows, int head_groups, in
 }
 
 struct DecodeParams {
+  // K and V pools as 2-D tensors [(num_blocks+1) * kv_heads * block, head_dim]
+  // for the tensor-core consumer's swizzled TMA loads (unused otherwise).
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
   const void* q;
   const void* k_pool;
   const void* v_pool;
@@ -123,7 +132,9 @@ __host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int he
   SmemLayout L;
   L.kv_bytes = (uint32_t)(heads_per_cta * kBlock * head_dim * elem);
   L.q_bytes = (uint32_t)(nvec * head_dim * elem);
-  L.stage_bytes = align_up(2 * L.kv_bytes + L.q_bytes, 128);
+  // Stages start on 1024-byte boundaries: 128-byte-swizzled TMA writes
+  // need it (the kernel aligns the dynamic shared memory base itself).
+  L.stage_bytes = align_up(2 * L.kv_bytes + L.q_bytes, 1024);
   uint32_t off = (uint32_t)stages * L.stage_bytes;
   L.off_meta = off;
   off += (uint32_t)stages * 16;
@@ -137,13 +148,13 @@ __host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int he
   off += (uint32_t)(rows + 1) * 4;
   L.off_flag = align_up(off, 4);
   off = L.off_flag + 8;
-  L.total = align_up(off, 128);
+  L.total = align_up(off, 128) + 1024;  // + slack to align the base to 1024
   return L;
 }
 
 // Launchers (return the launch's cudaError_t).
-cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int qw, int grid,
-                          int threads, int smem, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int qw, int consumer,
+                          int grid, int threads, int smem, cudaStream_t stream);
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
 // One-time per-device attribute set-up of the decode kernels.
 cudaError_t prepare_decode_kernels();

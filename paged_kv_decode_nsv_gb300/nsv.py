@@ -30,7 +30,9 @@ if not os.path.exists(LIB_PATH):
 
 _lib = ctypes.CDLL(LIB_PATH)
 
+ABI_VERSION = 101  # the layout of Shape and Plan below
 F32, BF16 = 0, 1
+CONSUMER_AUTO, CONSUMER_CUDA, CONSUMER_TENSOR = 0, 1, 2
 DEV_BAD_CTX, DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_TIMEOUT = 1, 2, 4, 8
 ERRORS = {0: "NSV_OK", -1: "NSV_ERR_NULLPTR", -2: "NSV_ERR_DTYPE", -3: "NSV_ERR_SHAPE",
           -4: "NSV_ERR_ALIGN", -5: "NSV_ERR_RANGE", -6: "NSV_ERR_CAPTURE", -7: "NSV_ERR_CUDA",
@@ -50,6 +52,7 @@ class Plan(ctypes.Structure):
                 ("ctas_per_sm", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("num_sms", ctypes.c_int32), ("vectors_per_warp", ctypes.c_int32),
+                ("consumer", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self):
@@ -61,12 +64,15 @@ _SP, _PP = ctypes.POINTER(Shape), ctypes.POINTER(Plan)
 
 _lib.nsv_abi_version.restype = _i32
 _lib.nsv_abi_version.argtypes = []
+if _lib.nsv_abi_version() != ABI_VERSION:
+    raise ImportError("libnsv.so has ABI version %d, this binding expects %d; rebuild it"
+                      % (_lib.nsv_abi_version(), ABI_VERSION))
 _lib.nsv_strerror.restype = ctypes.c_char_p
 _lib.nsv_strerror.argtypes = [_i32]
 _lib.nsv_plan_split.restype = _i32
 _lib.nsv_plan_split.argtypes = [_SP, _i32, _PP]
 _lib.nsv_plan_custom.restype = _i32
-_lib.nsv_plan_custom.argtypes = [_SP, _i32, _i32, _i32, _i32, _i32, _i32, _PP]
+_lib.nsv_plan_custom.argtypes = [_SP, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _PP]
 _lib.nsv_kv_write.restype = _i32
 _lib.nsv_kv_write.argtypes = [_SP, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.nsv_paged_decode.restype = _i32
@@ -166,11 +172,11 @@ def plan_split(shape, num_sms=0):
 
 
 def plan_custom(shape, num_sms=0, kv_heads_per_cta=0, stages=0, ctas_per_sm=0, grid=0,
-                vectors_per_warp=0):
+                vectors_per_warp=0, consumer=CONSUMER_AUTO):
     p = Plan()
     _check(_lib.nsv_plan_custom(ctypes.byref(shape), int(num_sms), int(kv_heads_per_cta),
                                 int(stages), int(ctas_per_sm), int(grid), int(vectors_per_warp),
-                                ctypes.byref(p)), "nsv_plan_custom")
+                                int(consumer), ctypes.byref(p)), "nsv_plan_custom")
     return p
 
 

@@ -50,7 +50,7 @@ def test_library_exports_nothing_else(nsv):
 
 
 def test_abi_version_and_strerror(nsv):
-    assert nsv.abi_version() == 100
+    assert nsv.abi_version() == nsv.ABI_VERSION == 101
     for code in (0, -1, -2, -3, -4, -5, -6, -7, -8, -10):
         assert nsv.strerror(code) and "unknown" not in nsv.strerror(code)
     assert "unknown" in nsv.strerror(-99)
@@ -89,7 +89,11 @@ def test_plan_shapes_of_every_workload(nsv):
         nvec = p.kv_heads_per_cta * (wl.heads // wl.kv_heads) * wl.query_len
         assert 0 < p.workspace_bytes < 152 * 4 * 2 * nvec * (wl.head_dim * 4 + 8) + (1 << 16)
         assert wl.kv_heads % p.kv_heads_per_cta == 0
-        assert (p.threads // 32 - 1) * p.vectors_per_warp == nvec
+        if p.consumer == nsv.CONSUMER_TENSOR:  # one warp per KV head of the group
+            assert p.vectors_per_warp == 1 and p.threads // 32 - 1 == p.kv_heads_per_cta
+        else:
+            assert p.consumer == nsv.CONSUMER_CUDA
+            assert (p.threads // 32 - 1) * p.vectors_per_warp == nvec
 
 
 @pytest.mark.parametrize("heads,kv_heads,qlen,qw,warps", [
@@ -97,10 +101,12 @@ def test_plan_shapes_of_every_workload(nsv):
     (32, 32, 3, 1, 6), (16, 1, 1, 2, 8), (32, 8, 8, 2, 16), (8, 8, 5, 1, 5),
 ])
 def test_plan_query_vectors(nsv, heads, kv_heads, qlen, qw, warps):
-    """By default a consumer warp serves two query vectors when the vectors
-    per KV head (query heads per KV head x tokens) pair up, else one."""
-    p = nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen),
-                       num_sms=152)
+    """On the CUDA cores a consumer warp serves two query vectors by default
+    when the vectors per KV head (query heads per KV head x tokens) pair up,
+    else one."""
+    p = nsv.plan_custom(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen),
+                        num_sms=152, consumer=nsv.CONSUMER_CUDA)
+    assert p.consumer == nsv.CONSUMER_CUDA
     assert p.vectors_per_warp == qw
     assert p.threads == (warps + 1) * 32
 
@@ -112,6 +118,49 @@ def test_plan_refuses_too_many_query_vectors(nsv, heads, kv_heads, qlen):
         nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen),
                        num_sms=152)
     assert e.value.code == -3
+
+
+@pytest.mark.parametrize("heads,kv_heads,qlen,dtype,consumer,hg", [
+    (32, 32, 1, "bf16", 1, 8),    # one vector per KV head: CUDA cores
+    (32, 8, 1, "bf16", 2, 8),     # 4 query heads per KV head: tensor cores
+    (32, 32, 4, "bf16", 2, 8),    # 4 query tokens
+    (32, 32, 3, "bf16", 2, 8),
+    (16, 1, 1, "bf16", 2, 1),     # 16 vectors: one full MMA tile
+    (32, 8, 8, "bf16", 1, 1),     # 32 vectors: more than one MMA tile holds
+    (32, 8, 1, "f32", 1, 4),      # fp32 stays on the CUDA cores
+])
+def test_plan_consumer_choice(nsv, heads, kv_heads, qlen, dtype, consumer, hg):
+    """The default plan runs bf16 shapes with 2 to 16 query vectors per KV
+    head on the tensor cores, one warp per KV head of the group."""
+    p = nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen,
+                              dtype=nsv.BF16 if dtype == "bf16" else nsv.F32), num_sms=152)
+    assert p.consumer == consumer and p.kv_heads_per_cta == hg
+    if consumer == nsv.CONSUMER_TENSOR:
+        assert p.vectors_per_warp == 1 and p.threads == (hg + 1) * 32
+    assert p.reserved == 0
+
+
+@pytest.mark.parametrize("kw,ckw", [
+    (dict(num_kv_heads=32), dict(consumer=2)),                      # 1 vector per KV head
+    (dict(num_kv_heads=8, dtype=1), dict(consumer=2, vectors_per_warp=2)),
+    (dict(num_kv_heads=8, dtype=0), dict(consumer=2)),              # fp32
+    (dict(num_kv_heads=8, query_len=8), dict(consumer=2)),          # 32 vectors
+    (dict(num_kv_heads=8), dict(consumer=3)),
+    (dict(num_kv_heads=8, num_blocks=(1 << 24)), dict(consumer=2)), # TMA row index overflows
+])
+def test_plan_tensor_consumer_refusals(nsv, kw, ckw):
+    with pytest.raises(nsv.NsvError) as e:
+        nsv.plan_custom(_shape(nsv, **kw), num_sms=152, **ckw)
+    assert e.value.code == -5
+
+
+def test_plan_tensor_consumer_needs_32bit_rows(nsv):
+    """Where the pools have 2^31 or more 16-token tile rows the default plan
+    keeps the CUDA-core consumer."""
+    p = nsv.plan_split(_shape(nsv, num_kv_heads=8, num_blocks=(1 << 24)), num_sms=152)
+    assert p.consumer == nsv.CONSUMER_CUDA
+    p = nsv.plan_split(_shape(nsv, num_kv_heads=8, num_blocks=(1 << 24) - 2), num_sms=152)
+    assert p.consumer == nsv.CONSUMER_TENSOR
 
 
 def test_plan_four_vectors_per_warp_on_request(nsv):

@@ -1,0 +1,140 @@
+"""The tensor-core consumer (bf16 mma.sync over TMA-staged, 128-byte-swizzled
+K/V tiles) against the oracle: grouped query heads and several query tokens
+per row, both head dims, every plan shape the planner allows, the slot-table
+gather, and rows whose early query tokens see no position."""
+
+import numpy as np
+import pytest
+
+import oracle
+from gpu_common import (assert_parity, device_inputs, gpu_out_f64, gpu_read, gpu_step,
+                        host_copy, oracle_read, oracle_step, status)
+from paged_kv_decode_nsv_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+LENS = [40, 513, 0, 2048, 77, 1, 15, 16, 17, 300]
+
+
+@pytest.fixture(scope="module")
+def nsv():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from paged_kv_decode_nsv_gb300 import nsv as mod
+    mod.device_status(clear=True)
+    return mod
+
+
+def _case(heads, kv_heads, qlen, head_dim, lens=LENS, seed=5, free_frac=0.3):
+    return W.custom("tc", seed, rows=len(lens), heads=heads, kv_heads=kv_heads,
+                    head_dim=head_dim, block_size=16, max_blocks=140, dtype="bf16", lens=lens,
+                    free_frac=free_frac, query_len=qlen)
+
+
+def _plan(nsv, inp, **kw):
+    shape = nsv.shape_of(inp["q"], inp["k_pool"], inp["block_tables"])
+    return nsv.plan_custom(shape, **kw)
+
+
+@pytest.mark.parametrize("heads,kv_heads,qlen,head_dim", [
+    (32, 8, 1, 128),    # 4 query heads per KV head
+    (16, 1, 1, 128),    # 16: a full MMA tile, one KV head
+    (8, 8, 2, 128),     # 2 query tokens
+    (8, 8, 3, 64),      # odd vector count, head_dim 64
+    (12, 3, 4, 64),     # 4 heads x 4 tokens = 16
+    (32, 32, 4, 128),   # 32 KV heads in groups of 8
+    (6, 2, 5, 128),     # 3 heads x 5 tokens = 15
+])
+def test_tensor_consumer_against_the_oracle(nsv, heads, kv_heads, qlen, head_dim):
+    wl = _case(heads, kv_heads, qlen, head_dim)
+    inp = device_inputs(wl)
+    host = host_copy(inp)
+    plan = _plan(nsv, inp, consumer=nsv.CONSUMER_TENSOR)
+    assert plan.consumer == nsv.CONSUMER_TENSOR
+    out = gpu_step(wl, inp, plan=plan)
+    st, walked = status()
+    assert st == 0 and walked == oracle.walked_tiles(wl.context_lens, 16)
+    assert_parity("bf16", gpu_out_f64(out), oracle_step(wl, host))
+
+
+@pytest.mark.parametrize("kw", [
+    dict(grid=1),                            # one CTA walks every unit
+    dict(grid=3),
+    dict(grid=5000),                         # more CTAs than units
+    dict(stages=2, grid=9),
+    dict(stages=6, kv_heads_per_cta=2),
+    dict(kv_heads_per_cta=1),
+    dict(kv_heads_per_cta=2, ctas_per_sm=2),
+    dict(kv_heads_per_cta=8, ctas_per_sm=1, grid=100),
+])
+def test_tensor_consumer_plans(nsv, kw):
+    wl = _case(32, 8, 2, 128, seed=7)
+    inp = device_inputs(wl)
+    host = host_copy(inp)
+    plan = _plan(nsv, inp, consumer=nsv.CONSUMER_TENSOR, **kw)
+    out = gpu_read(wl, inp, plan=plan)
+    assert status()[0] == 0
+    assert_parity("bf16", gpu_out_f64(out), oracle_read(wl, host))
+
+
+def test_both_consumers_agree_with_the_oracle(nsv):
+    """The same inputs through the CUDA-core and the tensor-core consumer."""
+    wl = _case(16, 4, 2, 128, seed=9)
+    inp = device_inputs(wl)
+    host = host_copy(inp)
+    ref = oracle_read(wl, host)
+    errs = {}
+    for c in (nsv.CONSUMER_CUDA, nsv.CONSUMER_TENSOR):
+        out = gpu_read(wl, inp, plan=_plan(nsv, inp, consumer=c))
+        assert status()[0] == 0
+        errs[c] = assert_parity("bf16", gpu_out_f64(out), ref)
+    # P rounded to bf16 costs the tensor path a little, never an order of magnitude
+    assert errs[nsv.CONSUMER_TENSOR] <= max(10 * errs[nsv.CONSUMER_CUDA], 1e-2)
+
+
+def test_early_query_tokens_that_see_nothing(nsv):
+    """query_len 4 over rows shorter than 4: query token j sees
+    ctx - 4 + 1 + j positions, none when that is not positive (output 0)."""
+    lens = [1, 2, 3, 4, 5, 0, 33]
+    wl = _case(8, 2, 4, 128, lens=lens, seed=13)
+    inp = device_inputs(wl)
+    host = host_copy(inp)
+    out = gpu_step(wl, inp, plan=_plan(nsv, inp, consumer=nsv.CONSUMER_TENSOR))
+    assert status()[0] == 0
+    got = gpu_out_f64(out)
+    ref = oracle_step(wl, host)
+    assert_parity("bf16", got, ref)
+    assert np.all(got[0, :3] == 0) and np.all(got[1, :2] == 0) and np.all(got[2, :1] == 0)
+    assert np.all(got[5] == 0)
+
+
+def test_tensor_consumer_slot_gather(nsv):
+    """Tokens scattered one by one over the pool: the producer warp gathers
+    them into the swizzled layout the MMA reads."""
+    import torch
+    wl = _case(16, 4, 2, 128, seed=17, free_frac=1.5)
+    inp = device_inputs(wl)
+    host = host_copy(inp)
+    rng = np.random.default_rng(21)
+    pool_slots = (wl.num_blocks + 1) * 16
+    width = wl.max_blocks * 16
+    table = np.zeros((wl.rows, width), dtype=np.int64)
+    for r in range(wl.rows):
+        table[r] = rng.choice(pool_slots - 16, size=width, replace=False)
+    # about half the blocks keep one aligned run: the bulk path beside the gather
+    for r in range(wl.rows):
+        for b in range(0, wl.max_blocks, 2):
+            base = int(rng.integers(0, wl.num_blocks)) * 16
+            table[r, b * 16:(b + 1) * 16] = base + np.arange(16)
+    table = np.ascontiguousarray(table)
+    out = torch.empty_like(inp["q"])
+    plan = _plan(nsv, inp, consumer=nsv.CONSUMER_TENSOR)
+    nsv.paged_decode_slots(inp["q"], inp["k_pool"], inp["v_pool"],
+                           torch.from_numpy(table).cuda(), inp["context_lens"], wl.scale, out,
+                           workspace=nsv.workspace_for(plan), plan=plan,
+                           max_blocks=wl.max_blocks)
+    torch.cuda.synchronize()
+    assert status()[0] == 0
+    ref = oracle.paged_decode_slots(host["q"], host["k_pool"], host["v_pool"], table, width,
+                                    wl.context_lens, wl.scale)
+    assert_parity("bf16", gpu_out_f64(out), ref)
