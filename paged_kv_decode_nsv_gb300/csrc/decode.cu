@@ -51,6 +51,8 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+// Slack of the tensor consumer's lazily raised running max, in log2 units.
+constexpr float kRescaleSlack = 8.f;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -98,15 +100,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete; false if
-// it has not after kWaitLimitNs.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// it has not after kWaitLimitNs.  The first try is inline (the common case:
+// the phase is already complete); the bounded loop is out of line.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = global_ns();
   while (true) {
     for (int i = 0; i < 16; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (global_ns() - t0 > kWaitLimitNs) return false;
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity);
 }
 
 __device__ __forceinline__ uint64_t evict_first_policy() {
@@ -501,37 +507,45 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
           mma_bf16(sc[1], qa[ks], b2, b3);
         }
       }
-      // online softmax per row (a row's 16 scores sit on 4 lanes)
+      // Online softmax per row (a row's 16 scores sit on 4 lanes).  The
+      // running max is raised lazily: only when a block's max exceeds it by
+      // more than kRescaleSlack (log2 units) are l and O rescaled, so most
+      // blocks skip the rescale and the probabilities stay <= 2^kRescaleSlack.
+      // Any reference max gives the same softmax; l and O always refer to m.
+      // A block every row sees in full needs no masks: rows past the vector
+      // count have zero queries, finite scores, and are never written.
+      const bool dense = nvalid == kBlock && tmask == 0xffff && rem - (NQ - 1) >= kBlock;
       uint32_t pa[4];
 #pragma unroll
       for (int rh = 0; rh < 2; ++rh) {
-        const int nv = rem - (NQ - 1 - rjq[rh]);  // positions this row's query sees
         float x[4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int e = 0; e < 4; ++e) x[e] = sc[e >> 1][rh * 2 + (e & 1)] * p.qscale;
+        if (!dense) {
+          const int nv = rem - (NQ - 1 - rjq[rh]);  // positions this row's query sees
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int tok = nt * 8 + t4 * 2 + e;
-            const bool ok = rok[rh] && tok < nv && ((tmask >> tok) & 1);
-            x[nt * 2 + e] = ok ? sc[nt][rh * 2 + e] * p.qscale : -INFINITY;
+          for (int e = 0; e < 4; ++e) {
+            const int tok = (e >> 1) * 8 + t4 * 2 + (e & 1);
+            if (!(rok[rh] && tok < nv && ((tmask >> tok) & 1))) x[e] = -INFINITY;
           }
         }
         float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
         mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-        const float mn = fmaxf(m[rh], mx);
-        const float alpha = (mn == -INFINITY) ? 1.f : exp2f(m[rh] - mn);
-        m[rh] = mn;
-        l[rh] *= alpha;
+        if (mx > m[rh] + kRescaleSlack) {  // also the first finite max (m = -inf)
+          const float alpha = exp2f(m[rh] - mx);
+          m[rh] = mx;
+          l[rh] *= alpha;
 #pragma unroll
-        for (int nd = 0; nd < kNd; ++nd) {
-          o[nd][rh * 2] *= alpha;
-          o[nd][rh * 2 + 1] *= alpha;
+          for (int nd = 0; nd < kNd; ++nd) {
+            o[nd][rh * 2] *= alpha;
+            o[nd][rh * 2 + 1] *= alpha;
+          }
         }
         float pv[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          pv[e] = (x[e] == -INFINITY) ? 0.f : exp2f(x[e] - mn);
+          pv[e] = (dense || x[e] != -INFINITY) ? exp2f(x[e] - m[rh]) : 0.f;
           l[rh] += pv[e];
         }
         pa[rh] = pack_bf16(pv[0], pv[1]);      // row rh*8 + g, tokens 2*t4, 2*t4+1
