@@ -95,9 +95,11 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic():
-    """DRAM bytes per decode-kernel launch from a committed ncu capture, if
-    it was taken on the kernel source as it is now (else None)."""
+def recorded_traffic(consumer, read_bytes):
+    """DRAM bytes per decode-kernel launch, from the committed ncu capture of
+    the same consumer variant taken on the kernel source as it is now (else
+    None): the capture's traffic/algorithmic ratio times this launch's
+    algorithmic read bytes."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
@@ -105,8 +107,9 @@ def recorded_traffic():
             sha = hashlib.sha256(f.read()).hexdigest()
         if d.get("decode_cu_sha256") != sha:
             return None
-        return d.get("traffic_bytes_per_launch_full_size")
-    except (OSError, ValueError):
+        cap = d["captures"]["tensor" if consumer == 2 else "cuda"]
+        return cap["traffic_over_algorithmic"] * read_bytes
+    except (OSError, ValueError, KeyError):
         return None
 
 
@@ -406,9 +409,10 @@ def run_nsv(args, wl):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback",
-                     "kernel": "decode read (decode_kernel)",
+                     "kernel": "decode read (decode_kernel, %s consumer)"
+                               % ("tensor-core" if plan.consumer == 2 else "CUDA-core"),
                      "bytes_per_launch": wl.read_bytes(), "us_per_launch": ms_read * 1e3,
-                     "traffic": recorded_traffic()},
+                     "traffic": recorded_traffic(plan.consumer, wl.read_bytes())},
         "e2e": {"value": whole_job_gbs(step_bytes, ws, e2e_ms), "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": K * launches_per_step,

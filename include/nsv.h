@@ -301,6 +301,21 @@ NSV_API int nsv_paged_decode_slots(const nsv_shape *shape, const nsv_plan *plan,
                                    size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Self-test of the bounded wait (the pages have no counterpart; this checks
+ * the library's own failure detection).  Every pipeline wait of the decode
+ * kernel gives up after a limit (1 s) instead of spinning forever; a wait
+ * that gives up sets NSV_DEV_TIMEOUT and the kernel returns, leaving the
+ * context usable.  This call runs that same wait routine in a one-thread
+ * kernel, with limit_ns (1 us .. 2 s), on an mbarrier phase that nothing
+ * completes, so it must give up.  Synchronous on `stream`; touches neither
+ * the device status word nor any caller memory.  On NSV_OK, *gave_up is 1
+ * when the wait gave up (the expected outcome) and *waited_ns is how long it
+ * waited.  Returns NSV_ERR_{NULLPTR, RANGE, CUDA}.
+ */
+NSV_API int nsv_selftest_bounded_wait(uint64_t limit_ns, int *gave_up, uint64_t *waited_ns,
+                                      cudaStream_t stream);
+
+/*
  * Synchronise the current device, then report its status word (NSV_DEV_*
  * bits raised since the last clear) and the number of (row, block) pairs the
  * decode kernels walked (each row's cdiv(ctx, block_size) blocks, counted

@@ -100,19 +100,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete; false if
-// it has not after kWaitLimitNs.  The first try is inline (the common case:
-// the phase is already complete); the bounded loop is out of line.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
+// it has not after limit_ns.  The first try is inline (the common case: the
+// phase is already complete); the bounded loop is out of line.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                            unsigned long long limit_ns) {
   const unsigned long long t0 = global_ns();
   while (true) {
     for (int i = 0; i < 16; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity);
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, kWaitLimitNs);
+}
+
+// Self-test of the bounded wait: one thread waits, with limit_ns, for a
+// phase of a fresh mbarrier that nothing completes.  result[0] = 1 when the
+// wait gave up, result[1] = the nanoseconds it waited.
+__global__ void bounded_wait_probe(unsigned long long limit_ns, unsigned long long* result) {
+  __shared__ __align__(8) unsigned long long bar_word;
+  if (threadIdx.x != 0) return;
+  const uint32_t bar = smem_u32(&bar_word);
+  mbar_init(bar, 1);
+  fence_mbar_init();
+  const unsigned long long t0 = global_ns();
+  const bool completed = mbar_wait_slow(bar, 0, limit_ns);
+  result[1] = global_ns() - t0;
+  result[0] = completed ? 0ull : 1ull;
 }
 
 __device__ __forceinline__ uint64_t evict_first_policy() {
@@ -1119,6 +1135,12 @@ void launch_typed(const DecodeParams& p, int qw, int consumer, int grid, int thr
 }
 
 }  // namespace
+
+cudaError_t launch_wait_probe(unsigned long long limit_ns, unsigned long long* result,
+                              cudaStream_t stream) {
+  bounded_wait_probe<<<1, 32, 0, stream>>>(limit_ns, result);
+  return cudaGetLastError();
+}
 
 cudaError_t prepare_decode_kernels() {
   cudaError_t e;

@@ -16,6 +16,8 @@ namespace nsv {
 // Sticky device status (NSV_DEV_* bits) and the walked-block counter.
 __device__ uint32_t g_status;
 __device__ unsigned long long g_walked;
+// Result of the bounded-wait self-test: gave up (0/1), nanoseconds waited.
+__device__ unsigned long long g_probe[2];
 
 namespace {
 
@@ -431,6 +433,27 @@ NSV_API int nsv_paged_decode_slots(const nsv_shape* shape, const nsv_plan* plan,
   return decode_impl(shape, plan, q, k_pool, v_pool, nullptr, slot_table, slot_cols,
                      slot_row_stride, context_lens, scale, out, workspace, workspace_bytes,
                      lib_ws, stream);
+}
+
+NSV_API int nsv_selftest_bounded_wait(uint64_t limit_ns, int* gave_up, uint64_t* waited_ns,
+                                      cudaStream_t stream) {
+  if (!gave_up || !waited_ns) return NSV_ERR_NULLPTR;
+  if (limit_ns < 1000 || limit_ns > 2000000000ull) return NSV_ERR_RANGE;
+  DeviceState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc) return rc;
+  unsigned long long* res = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&res), g_probe) != cudaSuccess)
+    return cuda_fail();
+  if (cudaMemsetAsync(res, 0xff, sizeof(g_probe), stream) != cudaSuccess) return cuda_fail();
+  if (launch_wait_probe(limit_ns, res, stream) != cudaSuccess) return cuda_fail();
+  unsigned long long h[2] = {0, 0};
+  if (cudaMemcpyAsync(h, res, sizeof h, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return cuda_fail();
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return cuda_fail();
+  *gave_up = h[0] == 1ull ? 1 : 0;
+  *waited_ns = (uint64_t)h[1];
+  return NSV_OK;
 }
 
 NSV_API int nsv_device_status(uint32_t* status, uint64_t* blocks_walked, int clear) {

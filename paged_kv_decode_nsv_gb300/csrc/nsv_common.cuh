@@ -158,5 +158,8 @@ cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int qw
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
 // One-time per-device attribute set-up of the decode kernels.
 cudaError_t prepare_decode_kernels();
+// The bounded-wait self-test kernel (result: device [gave_up, waited_ns]).
+cudaError_t launch_wait_probe(unsigned long long limit_ns, unsigned long long* result,
+                              cudaStream_t stream);
 
 }  // namespace nsv

@@ -90,6 +90,9 @@ _lib.nsv_paged_decode_noalloc.argtypes = [_SP, _vp, _vp, _vp, _vp, _vp, _f, _vp,
 _lib.nsv_device_status.restype = _i32
 _lib.nsv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32),
                                    ctypes.POINTER(ctypes.c_uint64), _i32]
+_lib.nsv_selftest_bounded_wait.restype = _i32
+_lib.nsv_selftest_bounded_wait.argtypes = [ctypes.c_uint64, ctypes.POINTER(ctypes.c_int),
+                                           ctypes.POINTER(ctypes.c_uint64), _vp]
 
 
 class NsvError(RuntimeError):
@@ -291,6 +294,17 @@ def decode_step(q, k_new, v_new, write_slots, k_pool, v_pool, block_tables, cont
                                 _ptr(out, "out"), ws_ptr, ws_bytes, _stream(stream)),
            "nsv_decode_step")
     return out
+
+
+def selftest_bounded_wait(limit_ns, stream=None):
+    """Run the decode kernel's bounded wait on a barrier nothing completes;
+    returns (gave_up, waited_ns).  Synchronises the stream."""
+    gave_up = ctypes.c_int(0)
+    waited = ctypes.c_uint64(0)
+    _check(_lib.nsv_selftest_bounded_wait(int(limit_ns), ctypes.byref(gave_up),
+                                          ctypes.byref(waited), _stream(stream)),
+           "nsv_selftest_bounded_wait")
+    return gave_up.value, waited.value
 
 
 def device_status(clear=True):

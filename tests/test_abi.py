@@ -234,3 +234,15 @@ def test_tampered_plan_refused_before_any_device_call(nsv):
     rc = lib.nsv_paged_decode_ws(ctypes.byref(s), ctypes.byref(p), fake, fake, fake, fake, fake,
                                  1.0, fake, fake, 1 << 30, None)
     assert rc == -5
+
+
+@pytest.mark.parametrize("limit", [0, 999, 2000000001])
+def test_bounded_wait_selftest_refuses_limits_out_of_range(nsv, limit):
+    """Checked on the host before any device call."""
+    g, w = ctypes.c_int(0), ctypes.c_uint64(0)
+    rc = nsv._lib.nsv_selftest_bounded_wait(limit, ctypes.byref(g), ctypes.byref(w), None)
+    assert rc == -5
+
+
+def test_bounded_wait_selftest_refuses_null_results(nsv):
+    assert nsv._lib.nsv_selftest_bounded_wait(1000000, None, None, None) == -1
