@@ -53,6 +53,10 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 // Slack of the tensor consumer's lazily raised running max, in log2 units.
 constexpr float kRescaleSlack = 8.f;
+// Tensor-core consumer forms (the kernel's MMA template argument; 0: CUDA cores).
+constexpr int kMmaVectorRows = 1;  // query vectors as the MMA rows (M = 16)
+constexpr int kMmaTokenRows = 2;   // the block's tokens as the MMA rows, vectors as N = 8
+constexpr int kMmaTokenRowsMaxVectors = 8;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -182,6 +186,13 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The transpose of an 8x8 b16 matrix held one 32-bit pair per lane.
+__device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -622,7 +633,220 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
   }
 }
 
-template <typename T, int D, int QW, bool MMA>
+// Tensor-core consumer with the block's 16 tokens as the MMA rows (bf16, at
+// most 8 query vectors per KV head, one warp per KV head).  Per block:
+// S^T = K.Q^T (M = 16 tokens, N = 8 vectors, K = head_dim), the online
+// softmax down the columns of S^T, then O^T += V^T.P^T (M = head_dim, N = 8
+// vectors, K = 16 tokens).  The probabilities go from the S^T accumulators
+// to the P^T operand with one movmatrix transpose per 8 tokens.  Against
+// vectors as the rows this takes half the MMAs and half the accumulators.
+// Fragment layout of m16n8k16: lane = 4*g + t4 holds rows g and g+8,
+// columns 2*t4 and 2*t4+1 of C; column g of B.
+template <int D>
+__device__ __forceinline__ void consume_mma_t(const DecodeParams& p, unsigned char* smem,
+                                              const SmemLayout& L, const int4* s_meta,
+                                              uint32_t bars, const int* s_prefix,
+                                              volatile int* s_abort, int N, long long U,
+                                              int nhg, int nvec, int ncw, int warp, int lane) {
+  using T = __nv_bfloat16;
+  constexpr int kKs = D / 16;  // k-steps of S^T, and m-tiles of O^T
+  const int G = p.group, NQ = p.query_len, HG = p.heads_per_cta, S = p.stages;
+  if (warp > ncw) return;
+  const int cw = warp - 1;
+  const int kvl = cw;                   // one warp per KV head of the group
+  const int vpk = G * NQ;               // its query vectors (<= 8)
+  const int vbase = kvl * vpk;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int hq = HG * G;
+  const uint32_t half_bytes = (uint32_t)HG * kBlock * 128;
+  volatile int* s_merge = s_abort + 1;
+
+  // B-operand column g: the query vector this lane loads.  Accumulator
+  // columns 2*t4 + c (c = 0, 1): the vectors whose softmax state it keeps.
+  const bool gok = g < vpk;
+  const int gqh = kvl * G + (gok ? g : 0) / NQ, gjq = (gok ? g : 0) % NQ;
+  bool cok[2];
+  int cqh[2], cjq[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int v = 2 * t4 + c;
+    cok[c] = v < vpk;
+    const int vv = cok[c] ? v : 0;
+    cqh[c] = kvl * G + vv / NQ;
+    cjq[c] = vv % NQ;
+  }
+
+  // Empty rows see nothing: zeros for all their (token, head) vectors.
+  constexpr int kChunks = D * 2 / 16;
+  for (int r = blockIdx.x; r < p.rows; r += gridDim.x) {
+    if (s_prefix[r + 1] != s_prefix[r]) continue;
+    for (int vh = cw; vh < NQ * p.heads; vh += ncw)
+      for (int c = lane; c < kChunks; c += 32)
+        reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)r * NQ * p.heads + vh) * D)[c] =
+            make_uint4(0u, 0u, 0u, 0u);
+  }
+
+  uint32_t qb[kKs][2];
+  float o[kKs][4], m[2], l[2];
+#pragma unroll
+  for (int ks = 0; ks < kKs; ++ks) qb[ks][0] = qb[ks][1] = 0u;
+#pragma unroll
+  for (int mt = 0; mt < kKs; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  m[0] = m[1] = -INFINITY;
+  l[0] = l[1] = 0.f;
+  const int mi = lane >> 3, i8 = lane & 7;  // ldmatrix: matrix and row this lane addresses
+
+  for (uint32_t n = 0;; ++n) {
+    const uint32_t s = n % S;
+    if (!mbar_wait(bars + 8 * s, (n / S) & 1)) {
+      if (lane == 0) atomicOr(p.status, (uint32_t)NSV_DEV_TIMEOUT);
+      *s_abort = 1;
+      return;
+    }
+    const int4 meta = s_meta[s];
+    const int flags = meta.w;
+    if (flags & kEnd) break;
+    unsigned char* st = smem + s * L.stage_bytes;
+    const uint32_t kbase = smem_u32(st), vbase_s = kbase + L.kv_bytes;
+    const int tmask = meta.y;
+    const int qh0 = (flags >> 16) * G;
+
+    if (flags & kFirst) {
+      m[0] = m[1] = -INFINITY;
+      l[0] = l[1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < kKs; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      if (flags & kHasQ) {
+        const unsigned char* row =
+            st + 2 * L.kv_bytes + ((size_t)(gjq * hq + gqh) * D + t4 * 2) * sizeof(T);
+#pragma unroll
+        for (int ks = 0; ks < kKs; ++ks) {
+          qb[ks][0] = gok ? *reinterpret_cast<const uint32_t*>(row + ks * 32) : 0u;
+          qb[ks][1] = gok ? *reinterpret_cast<const uint32_t*>(row + ks * 32 + 16) : 0u;
+        }
+      }
+    }
+
+    if (flags & kData) {
+      const int rem = flags & 0xff;
+      const int nvalid = min(kBlock, rem);
+      // V rows that hold no data (past the row's length, or tokens the
+      // producer did not gather) become zeros: P is 0 there, but 0 * NaN is not.
+      if (nvalid < kBlock || tmask != 0xffff) {
+        for (int c = lane; c < kBlock * kChunks; c += 32) {
+          const int t = c / kChunks, dc = c - t * kChunks;
+          if (!(t < nvalid && ((tmask >> t) & 1)))
+            *reinterpret_cast<uint4*>(st + L.kv_bytes + swz(kvl * kBlock + t, dc, half_bytes)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      // S^T: two accumulation chains (even and odd k-steps) for latency
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int r = kvl * kBlock + (mi & 1) * 8 + i8;
+#pragma unroll
+        for (int ks = 0; ks < kKs; ++ks) {
+          uint32_t a[4];
+          ldsm_x4(kbase + swz(r, ks * 2 + (mi >> 1), half_bytes), a[0], a[1], a[2], a[3]);
+          mma_bf16((ks & 1) ? sb : sa, a, qb[ks][0], qb[ks][1]);
+        }
+      }
+      // Online softmax down each column (a vector's 16 scores: tokens g and
+      // g + 8 on the 8 lanes of equal t4), with the lazily raised running max
+      // of the other tensor form; full blocks need no masks.
+      const bool dense = nvalid == kBlock && tmask == 0xffff && rem - (NQ - 1) >= kBlock;
+      float pr[2][2];  // [column c][token g, token g + 8]
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float x0 = (sa[c] + sb[c]) * p.qscale;
+        float x1 = (sa[2 + c] + sb[2 + c]) * p.qscale;
+        if (!dense) {
+          const int nv = rem - (NQ - 1 - cjq[c]);  // positions this vector's query sees
+          if (!(cok[c] && g < nv && ((tmask >> g) & 1))) x0 = -INFINITY;
+          if (!(cok[c] && g + 8 < nv && ((tmask >> (g + 8)) & 1))) x1 = -INFINITY;
+        }
+        float mx = fmaxf(x0, x1);
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+        if (mx > m[c] + kRescaleSlack) {  // also the first finite max (m = -inf)
+          const float alpha = exp2f(m[c] - mx);
+          m[c] = mx;
+          l[c] *= alpha;
+#pragma unroll
+          for (int mt = 0; mt < kKs; ++mt) {
+            o[mt][c] *= alpha;
+            o[mt][2 + c] *= alpha;
+          }
+        }
+        pr[c][0] = (dense || x0 != -INFINITY) ? exp2f(x0 - m[c]) : 0.f;
+        pr[c][1] = (dense || x1 != -INFINITY) ? exp2f(x1 - m[c]) : 0.f;
+        l[c] += pr[c][0] + pr[c][1];
+      }
+      // P^T operand: the 8x8 blocks [token][vector] of tokens 0-7 and 8-15,
+      // transposed to [vector][token] pairs.
+      const uint32_t b0 = movm_trans(pack_bf16(pr[0][0], pr[1][0]));
+      const uint32_t b1 = movm_trans(pack_bf16(pr[0][1], pr[1][1]));
+      // O^T += V^T.P^T: m-tiles of 16 dims, V read transposed
+      {
+        const int r = kvl * kBlock + (mi >> 1) * 8 + i8;
+#pragma unroll
+        for (int mt = 0; mt < kKs; ++mt) {
+          uint32_t a[4];
+          ldsm_x4_t(vbase_s + swz(r, mt * 2 + (mi & 1), half_bytes), a[0], a[1], a[2], a[3]);
+          mma_bf16(o[mt], a, b0, b1);
+        }
+      }
+    }
+
+    if (flags & kLast) {
+      const int row = meta.x;
+      float lt[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        lt[c] = l[c];
+        lt[c] += __shfl_xor_sync(kFull, lt[c], 4);
+        lt[c] += __shfl_xor_sync(kFull, lt[c], 8);
+        lt[c] += __shfl_xor_sync(kFull, lt[c], 16);
+      }
+      if (flags & kFinal) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (!cok[c]) continue;
+          const float inv = lt[c] > 0.f ? 1.f / lt[c] : 0.f;
+          T* out = static_cast<T*>(p.out) +
+                   (((size_t)row * NQ + cjq[c]) * p.heads + qh0 + cqh[c]) * D + g;
+#pragma unroll
+          for (int mt = 0; mt < kKs; ++mt) {
+            out[mt * 16] = __float2bfloat16_rn(o[mt][c] * inv);
+            out[mt * 16 + 8] = __float2bfloat16_rn(o[mt][2 + c] * inv);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (!cok[c]) continue;
+          const size_t slot = (size_t)meta.z * nvec + vbase + 2 * t4 + c;
+          float* a = p.ws_acc + slot * D + g;
+#pragma unroll
+          for (int mt = 0; mt < kKs; ++mt) {
+            a[mt * 16] = o[mt][c];
+            a[mt * 16 + 8] = o[mt][2 + c];
+          }
+          if (g == 0) p.ws_ml[slot] = make_float2(m[c], lt[c]);
+        }
+        finish_cut_row<T, D>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, vbase, vpk, ncw, cw,
+                             lane, s_merge);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (S + s));
+  }
+}
+
+template <typename T, int D, int QW, int MMA>
 __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
                                       : (QW <= 2 ? kMaxThreads : kMaxThreadsMulti), 1)
     decode_kernel(const __grid_constant__ DecodeParams p) {
@@ -886,8 +1110,12 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
   }
 
   // -------------------------------------------------------------------- consumers
-  if constexpr (MMA) {
+  if constexpr (MMA == kMmaVectorRows) {
     consume_mma<D>(p, smem, L, s_meta, bars, s_prefix, s_abort, N, U, nhg, nvec, ncw, warp, lane);
+    return;
+  } else if constexpr (MMA == kMmaTokenRows) {
+    consume_mma_t<D>(p, smem, L, s_meta, bars, s_prefix, s_abort, N, U, nhg, nvec, ncw, warp,
+                     lane);
     return;
   } else {
   // A consumer warp serves QW query vectors that read the same KV head: the
@@ -1101,7 +1329,7 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
   }  // CUDA-core consumer
 }
 
-template <typename T, int D, int QW, bool MMA>
+template <typename T, int D, int QW, int MMA>
 cudaError_t set_attr() {
   return cudaFuncSetAttribute(decode_kernel<T, D, QW, MMA>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -1110,10 +1338,13 @@ cudaError_t set_attr() {
 template <typename T, int D>
 cudaError_t set_attrs() {
   cudaError_t e;
-  if ((e = set_attr<T, D, 1, false>()) != cudaSuccess) return e;
-  if ((e = set_attr<T, D, 2, false>()) != cudaSuccess) return e;
-  if ((e = set_attr<T, D, 4, false>()) != cudaSuccess) return e;
-  if constexpr (sizeof(T) == 2) return set_attr<T, D, 1, true>();
+  if ((e = set_attr<T, D, 1, 0>()) != cudaSuccess) return e;
+  if ((e = set_attr<T, D, 2, 0>()) != cudaSuccess) return e;
+  if ((e = set_attr<T, D, 4, 0>()) != cudaSuccess) return e;
+  if constexpr (sizeof(T) == 2) {
+    if ((e = set_attr<T, D, 1, kMmaVectorRows>()) != cudaSuccess) return e;
+    return set_attr<T, D, 1, kMmaTokenRows>();
+  }
   return cudaSuccess;
 }
 
@@ -1122,16 +1353,20 @@ void launch_typed(const DecodeParams& p, int qw, int consumer, int grid, int thr
                   cudaStream_t stream) {
   if constexpr (sizeof(T) == 2) {
     if (consumer == kConsumerTensor) {
-      decode_kernel<T, D, 1, true><<<grid, threads, smem, stream>>>(p);
+      // Up to 8 query vectors per KV head: tokens as the MMA rows; more: vectors.
+      if (p.group * p.query_len <= kMmaTokenRowsMaxVectors)
+        decode_kernel<T, D, 1, kMmaTokenRows><<<grid, threads, smem, stream>>>(p);
+      else
+        decode_kernel<T, D, 1, kMmaVectorRows><<<grid, threads, smem, stream>>>(p);
       return;
     }
   }
   if (qw == 4)
-    decode_kernel<T, D, 4, false><<<grid, threads, smem, stream>>>(p);
+    decode_kernel<T, D, 4, 0><<<grid, threads, smem, stream>>>(p);
   else if (qw == 2)
-    decode_kernel<T, D, 2, false><<<grid, threads, smem, stream>>>(p);
+    decode_kernel<T, D, 2, 0><<<grid, threads, smem, stream>>>(p);
   else
-    decode_kernel<T, D, 1, false><<<grid, threads, smem, stream>>>(p);
+    decode_kernel<T, D, 1, 0><<<grid, threads, smem, stream>>>(p);
 }
 
 }  // namespace

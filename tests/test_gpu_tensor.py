@@ -1,7 +1,11 @@
 """The tensor-core consumer (bf16 mma.sync over TMA-staged, 128-byte-swizzled
 K/V tiles) against the oracle: grouped query heads and several query tokens
 per row, both head dims, every plan shape the planner allows, the slot-table
-gather, and rows whose early query tokens see no position."""
+gather, and rows whose early query tokens see no position.
+
+Up to 8 query vectors per KV head run with the block's tokens as the MMA
+rows; 9 to 16 with the query vectors as the rows.  Every test below covers
+both forms."""
 
 import numpy as np
 import pytest
@@ -67,8 +71,9 @@ def test_tensor_consumer_against_the_oracle(nsv, heads, kv_heads, qlen, head_dim
     dict(kv_heads_per_cta=2, ctas_per_sm=2),
     dict(kv_heads_per_cta=8, ctas_per_sm=1, grid=100),
 ])
-def test_tensor_consumer_plans(nsv, kw):
-    wl = _case(32, 8, 2, 128, seed=7)
+@pytest.mark.parametrize("qlen", [2, 3])   # 8 and 12 vectors per KV head
+def test_tensor_consumer_plans(nsv, kw, qlen):
+    wl = _case(32, 8, qlen, 128, seed=7)
     inp = device_inputs(wl)
     host = host_copy(inp)
     plan = _plan(nsv, inp, consumer=nsv.CONSUMER_TENSOR, **kw)
@@ -77,9 +82,10 @@ def test_tensor_consumer_plans(nsv, kw):
     assert_parity("bf16", gpu_out_f64(out), oracle_read(wl, host))
 
 
-def test_both_consumers_agree_with_the_oracle(nsv):
+@pytest.mark.parametrize("qlen", [2, 4])   # 8 and 16 vectors per KV head
+def test_both_consumers_agree_with_the_oracle(nsv, qlen):
     """The same inputs through the CUDA-core and the tensor-core consumer."""
-    wl = _case(16, 4, 2, 128, seed=9)
+    wl = _case(16, 4, qlen, 128, seed=9)
     inp = device_inputs(wl)
     host = host_copy(inp)
     ref = oracle_read(wl, host)
@@ -92,11 +98,12 @@ def test_both_consumers_agree_with_the_oracle(nsv):
     assert errs[nsv.CONSUMER_TENSOR] <= max(10 * errs[nsv.CONSUMER_CUDA], 1e-2)
 
 
-def test_early_query_tokens_that_see_nothing(nsv):
+@pytest.mark.parametrize("heads,kv_heads", [(8, 2), (4, 2)])   # 16 and 8 vectors
+def test_early_query_tokens_that_see_nothing(nsv, heads, kv_heads):
     """query_len 4 over rows shorter than 4: query token j sees
     ctx - 4 + 1 + j positions, none when that is not positive (output 0)."""
     lens = [1, 2, 3, 4, 5, 0, 33]
-    wl = _case(8, 2, 4, 128, lens=lens, seed=13)
+    wl = _case(heads, kv_heads, 4, 128, lens=lens, seed=13)
     inp = device_inputs(wl)
     host = host_copy(inp)
     out = gpu_step(wl, inp, plan=_plan(nsv, inp, consumer=nsv.CONSUMER_TENSOR))
@@ -108,11 +115,12 @@ def test_early_query_tokens_that_see_nothing(nsv):
     assert np.all(got[5] == 0)
 
 
-def test_tensor_consumer_slot_gather(nsv):
+@pytest.mark.parametrize("heads,kv_heads,head_dim", [(16, 4, 128), (16, 2, 128), (8, 4, 64)])
+def test_tensor_consumer_slot_gather(nsv, heads, kv_heads, head_dim):
     """Tokens scattered one by one over the pool: the producer warp gathers
     them into the swizzled layout the MMA reads."""
     import torch
-    wl = _case(16, 4, 2, 128, seed=17, free_frac=1.5)
+    wl = _case(heads, kv_heads, 2, head_dim, seed=17, free_frac=1.5)
     inp = device_inputs(wl)
     host = host_copy(inp)
     rng = np.random.default_rng(21)
