@@ -160,12 +160,15 @@ typedef struct nsv_plan {
  *                       dtype and shape.
  *  NSV_CONSUMER_TENSOR: bf16 only.  One warp per KV head runs all of that KV
  *                       head's query vectors (query heads of the group x
- *                       query tokens, 2 to 16 of them) as the rows of 16x8x16
- *                       bf16 tensor-core MMAs with fp32 accumulation: scores
- *                       Q.K^T and the weighted sum P.V, with the
- *                       probabilities P rounded to bf16 for the second
- *                       product.  K/V tiles arrive by 2-D TMA with a 128-byte
- *                       swizzle.  Needs (num_blocks+1)*num_kv_heads*16 < 2^31.
+ *                       query tokens, 2 to 16 of them) through 16x8x16 bf16
+ *                       tensor-core MMAs with fp32 accumulation: scores
+ *                       against the block's keys, then the weighted sum of
+ *                       its values, with the probabilities rounded to bf16
+ *                       for the second product.  Up to 8 vectors use the
+ *                       block's 16 tokens as the MMA rows, 9 to 16 the
+ *                       vectors.  K/V tiles arrive by 2-D TMA with a
+ *                       128-byte swizzle.  Needs
+ *                       (num_blocks+1)*num_kv_heads*16 < 2^31.
  * The default plan takes the tensor consumer for bf16 shapes with 2 to 16
  * query vectors per KV head, and the CUDA-core one otherwise. */
 enum { NSV_CONSUMER_AUTO = 0, NSV_CONSUMER_CUDA = 1, NSV_CONSUMER_TENSOR = 2 };
