@@ -275,9 +275,11 @@ def run_nsv(args, wl):
     from paged_kv_decode_nsv_gb300 import workloads as W
 
     # The oracle sample runs first, on the host, before the GPU work starts.
-    cpu = None
+    cpu = cpu1 = None
     if rank == 0 and ws == 1 and args.cpu_seconds > 0:
         cpu = oracle_throughput(wl, args.cpu_seconds)
+        # and on one core, a shorter sample
+        cpu1 = oracle_throughput(wl, max(1.0, args.cpu_seconds / 4), threads=1)
 
     stream = torch.cuda.current_stream()
     q, kp, vp, kn, vn = W.device_values(wl, "cuda")
@@ -424,6 +426,11 @@ def run_nsv(args, wl):
             "value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": "%d of %d rows of %s, %.1f s of oracle time (fp64, full-width rectangle "
                       "per row)" % (nrows, wl.rows, wl.name, secs)}
+        if cpu1 is not None:
+            g1, n1, s1, _ = cpu1
+            line["cpu_baseline"]["single_core"] = {
+                "value": g1, "unit": "GB/s", "cores": 1,
+                "sample": "%d rows of %s, %.1f s of oracle time" % (n1, wl.name, s1)}
     print(json.dumps(line), flush=True)
     return 0
 
