@@ -16,24 +16,28 @@ from paged_kv_decode_nsv_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _batches():
-    base = dict(rows=6, heads=8, kv_heads=8, head_dim=128, block_size=16, max_blocks=70,
-                dtype="bf16", num_blocks=400)
+def _batches(heads, kv_heads):
+    base = dict(rows=6, heads=heads, kv_heads=kv_heads, head_dim=128, block_size=16,
+                max_blocks=70, dtype="bf16", num_blocks=400)
     a = W.custom("graph_a", 41, lens=[100, 1, 0, 1100, 333, 17], **base)
     b = W.custom("graph_b", 42, lens=[5, 900, 64, 0, 2, 1024], **base)
     return base, a, b
 
 
-def test_graph_recorded_on_padding_replays_real_steps():
+@pytest.mark.parametrize("heads,kv_heads,consumer", [(8, 8, 1), (16, 4, 2)])
+def test_graph_recorded_on_padding_replays_real_steps(heads, kv_heads, consumer):
+    """Both consumers; the tensor-core one holds its TMA tensor maps (over the
+    pool, which the graph's replays keep) in the captured launch."""
     import torch
     from paged_kv_decode_nsv_gb300 import nsv
-    base, wa, wb = _batches()
+    base, wa, wb = _batches(heads, kv_heads)
     R, H, D, NB = base["rows"], base["heads"], base["head_dim"], base["num_blocks"]
+    HKV = base["kv_heads"]
     dev = "cuda"
     # persistent buffers: the pool (the cache) and the step's inputs
     _, kp, vp, _, _ = W.device_values(wa, dev, value_seed=7)
     q = torch.zeros((R, H, D), dtype=torch.bfloat16, device=dev)
-    kn = torch.zeros((R, H, D), dtype=torch.bfloat16, device=dev)
+    kn = torch.zeros((R, HKV, D), dtype=torch.bfloat16, device=dev)
     vn = torch.zeros_like(kn)
     slots = torch.full((R,), NB * 16, dtype=torch.int64, device=dev)     # all to the sink
     tables = torch.full((R, base["max_blocks"]), -1, dtype=torch.int32, device=dev)
@@ -41,6 +45,7 @@ def test_graph_recorded_on_padding_replays_real_steps():
     out = torch.full((R, H, D), 3.0, dtype=torch.bfloat16, device=dev)
     shape = nsv.shape_of(q, kp, tables)
     plan = nsv.plan_split(shape)
+    assert plan.consumer == consumer
     ws = nsv.workspace_for(plan)
     scale = wa.scale
 

@@ -54,7 +54,10 @@ def _noalloc_call(nsv, wl, inp, out):
     lambda: W.custom("noalloc_bf16", 31, rows=10, heads=8, kv_heads=8, head_dim=128,
                      block_size=16, max_blocks=66, dtype="bf16",
                      lens=[1, 0, 17, 256, 1000, 333, 16, 15, 1024, 47], free_frac=0.2),
-], ids=["uniform_f32", "ragged_bf16_10rows"])
+    lambda: W.custom("noalloc_gqa", 32, rows=10, heads=8, kv_heads=4, head_dim=128,
+                     block_size=16, max_blocks=66, dtype="bf16",
+                     lens=[1, 0, 17, 256, 1000, 333, 16, 15, 1024, 47], free_frac=0.2),
+], ids=["uniform_f32", "ragged_bf16_10rows", "gqa_bf16_tensor_cores"])
 def test_noalloc_matches_existing_entry_point_on_two_calls(nsv, make):
     import torch
     wl = make()
@@ -77,8 +80,8 @@ def test_noalloc_refuses_shapes_beyond_its_buffer(nsv):
     before anything is launched.  The tensors are real and every row is empty,
     so even a launch could not read or write out of bounds."""
     import torch
-    # 16 query heads per KV head: one KV head per CTA, 16 consumer warps and two
-    # CTAs per SM make the partial-state scratch larger than the buffer.
+    # 16 query heads per KV head: 8 KV heads per CTA carry 128 query vectors,
+    # whose partial states make the scratch larger than the buffer.
     rows, heads, kv_heads, head_dim, max_blocks = 256, 128, 8, 128, 512
     q = torch.zeros((rows, heads, head_dim), dtype=torch.bfloat16, device="cuda")
     out = torch.zeros_like(q)
