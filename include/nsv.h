@@ -114,8 +114,8 @@ enum {
  * multiple of num_kv_heads with num_heads/num_kv_heads <= 16; head_dim 64 or
  * 128; block_size 16; 1 <= max_blocks with max_blocks*block_size < 2^31;
  * 1 <= num_blocks < 2^31 - 1; query_len 0 or 1 (one query token per row) up
- * to 32 with query_len * num_heads/num_kv_heads <= 32, and <= 15 when that
- * product is odd. */
+ * to 32 with query_len * num_heads/num_kv_heads <= 32, and, on the CUDA-core
+ * consumer (fp32), <= 15 when that product is odd. */
 typedef struct nsv_shape {
     int32_t rows;
     int32_t num_heads;
@@ -158,18 +158,18 @@ typedef struct nsv_plan {
  *  NSV_CONSUMER_CUDA:   fp32 FMAs on the CUDA cores; a warp serves
  *                       vectors_per_warp query vectors of one KV head.  Any
  *                       dtype and shape.
- *  NSV_CONSUMER_TENSOR: bf16 only.  One warp per KV head runs all of that KV
- *                       head's query vectors (query heads of the group x
- *                       query tokens, 2 to 16 of them) through 16x8x16 bf16
- *                       tensor-core MMAs with fp32 accumulation: scores
- *                       against the block's keys, then the weighted sum of
- *                       its values, with the probabilities rounded to bf16
- *                       for the second product.  Up to 8 vectors use the
- *                       block's 16 tokens as the MMA rows, 9 to 16 the
- *                       vectors.  K/V tiles arrive by 2-D TMA with a
- *                       128-byte swizzle.  Needs
+ *  NSV_CONSUMER_TENSOR: bf16 only.  A KV head's query vectors (query heads
+ *                       of the group x query tokens, 2 to 32 of them) go
+ *                       through 16x8x16 bf16 tensor-core MMAs with fp32
+ *                       accumulation: scores against the block's keys, then
+ *                       the weighted sum of its values, with the
+ *                       probabilities rounded to bf16 for the second
+ *                       product.  Up to 8 vectors use the block's 16 tokens
+ *                       as the MMA rows (one warp per KV head); 9 to 32 use
+ *                       the vectors as the rows, 16 per warp.  K/V tiles
+ *                       arrive by 2-D TMA with a 128-byte swizzle.  Needs
  *                       (num_blocks+1)*num_kv_heads*16 < 2^31.
- * The default plan takes the tensor consumer for bf16 shapes with 2 to 16
+ * The default plan takes the tensor consumer for bf16 shapes with 2 or more
  * query vectors per KV head, and the CUDA-core one otherwise. */
 enum { NSV_CONSUMER_AUTO = 0, NSV_CONSUMER_CUDA = 1, NSV_CONSUMER_TENSOR = 2 };
 

@@ -410,10 +410,12 @@ __device__ __forceinline__ void finish_cut_row(const DecodeParams& p, int row, i
   }
 }
 
-// Tensor-core consumer (bf16): one warp per KV head of the group; its query
-// vectors (the group's query heads of that KV head times the query tokens,
-// at most 16) are the rows of mma.sync.m16n8k16 (bf16 inputs, fp32
-// accumulate).  Per 16-token block: S = Q.K^T from the K tile staged by
+// Tensor-core consumer (bf16) with the query vectors as the MMA rows: a KV
+// head's query vectors (the group's query heads of that KV head times the
+// query tokens, 9 to 32 of them) are the rows of mma.sync.m16n8k16 (bf16
+// inputs, fp32 accumulate), 16 rows per warp, so one or two warps per KV
+// head read the same K/V tile.  Each warp zeroes the tile's empty V rows
+// itself (both write the same zeros).  Per 16-token block: S = Q.K^T from the K tile staged by
 // swizzled TMA loads and read with ldmatrix, the online softmax on the score
 // fragments, then O += P.V with P (bf16) taken straight from the score
 // fragments and V read with ldmatrix.trans.  Fragment layout of m16n8k16:
@@ -430,9 +432,12 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
   const int G = p.group, NQ = p.query_len, HG = p.heads_per_cta, S = p.stages;
   if (warp > ncw) return;
   const int cw = warp - 1;
-  const int kvl = cw;                   // one warp per KV head of the group
-  const int vpk = G * NQ;               // its query vectors (<= 16)
-  const int vbase = kvl * vpk;
+  const int vpk = G * NQ;               // query vectors per KV head (<= 32)
+  const int wpk = ncw / HG;             // warps per KV head: one per 16 vectors
+  const int kvl = cw / wpk;             // this warp's KV head within the group
+  const int v0w = (cw - kvl * wpk) * kMmaRows;  // its first vector of that KV head
+  const int nvw = min(kMmaRows, vpk - v0w);     // and how many it runs (<= 16)
+  const int vbase = kvl * vpk + v0w;
   const int g = lane >> 2, t4 = lane & 3;
   const int hq = HG * G;
   const uint32_t half_bytes = (uint32_t)HG * kBlock * 128;
@@ -444,8 +449,8 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
 #pragma unroll
   for (int rh = 0; rh < 2; ++rh) {
     const int r = g + 8 * rh;
-    rok[rh] = r < vpk;
-    const int rr = rok[rh] ? r : 0;
+    rok[rh] = r < nvw;
+    const int rr = v0w + (rok[rh] ? r : 0);
     rqh[rh] = kvl * G + rr / NQ;
     rjq[rh] = rr % NQ;
   }
@@ -624,7 +629,7 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
             *reinterpret_cast<float2*>(a + nd * 8) = make_float2(o[nd][rh * 2], o[nd][rh * 2 + 1]);
           if (t4 == 0) p.ws_ml[slot] = make_float2(m[rh], lt[rh]);
         }
-        finish_cut_row<T, D>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, vbase, vpk, ncw, cw,
+        finish_cut_row<T, D>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, vbase, nvw, ncw, cw,
                              lane, s_merge);
       }
     }
@@ -867,7 +872,11 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
   const int NQ = p.query_len;
   const int HG = p.heads_per_cta;
   const int nvec = HG * G * NQ;          // query vectors per CTA
-  const int ncw = MMA ? HG : nvec / QW;  // consumer warps
+  // consumer warps: per KV head one (tokens as MMA rows) or one per 16
+  // vectors (vectors as MMA rows); QW vectors per warp on the CUDA cores
+  const int ncw = MMA == kMmaTokenRows    ? HG
+                  : MMA == kMmaVectorRows ? HG * ((G * NQ + kMmaRows - 1) / kMmaRows)
+                                          : nvec / QW;
   const int S = p.stages;
   const SmemLayout L = make_layout((int)sizeof(T), D, HG, nvec, S, p.rows);
 

@@ -128,7 +128,7 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   const int elem = elem_bytes(s->dtype);
   const int G = s->num_heads / s->num_kv_heads;
   const int vpk = G * query_len(s);                // query vectors per KV head
-  const bool tensor_ok = s->dtype == NSV_BF16 && vpk >= 2 && vpk <= kMmaRows &&
+  const bool tensor_ok = s->dtype == NSV_BF16 && vpk >= 2 && vpk <= kMaxVectorsPerKvHead &&
                          tensor_rows_fit(s);
   if (consumer == NSV_CONSUMER_AUTO) {
     // The tensor cores pay off once several query vectors share a K/V tile:
@@ -152,7 +152,9 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
     return NSV_ERR_RANGE;
   }
   const bool tensor = consumer == kConsumerTensor;
-  const int wpk = tensor ? 1 : vpk / qw;           // consumer warps per KV head
+  // consumer warps per KV head: on the tensor cores one (tokens as the MMA
+  // rows, up to 8 vectors) or one per 16 vectors (vectors as the rows)
+  const int wpk = tensor ? (vpk <= 8 ? 1 : (vpk + kMmaRows - 1) / kMmaRows) : vpk / qw;
   const int max_warps = tensor ? kMaxConsumerWarpsMulti : max_consumer_warps(qw);
   const int tile = kBlock * s->head_dim * elem;
   if (hg <= 0) {

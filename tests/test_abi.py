@@ -89,8 +89,10 @@ def test_plan_shapes_of_every_workload(nsv):
         nvec = p.kv_heads_per_cta * (wl.heads // wl.kv_heads) * wl.query_len
         assert 0 < p.workspace_bytes < 152 * 4 * 2 * nvec * (wl.head_dim * 4 + 8) + (1 << 16)
         assert wl.kv_heads % p.kv_heads_per_cta == 0
-        if p.consumer == nsv.CONSUMER_TENSOR:  # one warp per KV head of the group
-            assert p.vectors_per_warp == 1 and p.threads // 32 - 1 == p.kv_heads_per_cta
+        if p.consumer == nsv.CONSUMER_TENSOR:  # one warp per KV head, or per 16 vectors
+            vpk = (wl.heads // wl.kv_heads) * wl.query_len
+            wpk = 1 if vpk <= 8 else -(-vpk // 16)
+            assert p.vectors_per_warp == 1 and p.threads // 32 - 1 == p.kv_heads_per_cta * wpk
         else:
             assert p.consumer == nsv.CONSUMER_CUDA
             assert (p.threads // 32 - 1) * p.vectors_per_warp == nvec
@@ -111,32 +113,42 @@ def test_plan_query_vectors(nsv, heads, kv_heads, qlen, qw, warps):
     assert p.threads == (warps + 1) * 32
 
 
-@pytest.mark.parametrize("heads,kv_heads,qlen", [(32, 8, 9), (32, 32, 33), (32, 32, 17),
-                                                 (64, 4, 3)])
-def test_plan_refuses_too_many_query_vectors(nsv, heads, kv_heads, qlen):
+@pytest.mark.parametrize("heads,kv_heads,qlen,dtype", [
+    (32, 8, 9, 1), (32, 32, 33, 1), (64, 4, 3, 1),   # more than 32 vectors per KV head
+    (32, 32, 17, 0),   # fp32 (CUDA cores): an odd count above 15 needs 17 warps
+])
+def test_plan_refuses_too_many_query_vectors(nsv, heads, kv_heads, qlen, dtype):
     with pytest.raises(nsv.NsvError) as e:
-        nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen),
-                       num_sms=152)
+        nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen,
+                              dtype=dtype), num_sms=152)
     assert e.value.code == -3
 
 
-@pytest.mark.parametrize("heads,kv_heads,qlen,dtype,consumer,hg", [
-    (32, 32, 1, "bf16", 1, 8),    # one vector per KV head: CUDA cores
-    (32, 8, 1, "bf16", 2, 8),     # 4 query heads per KV head: tensor cores
-    (32, 32, 4, "bf16", 2, 8),    # 4 query tokens
-    (32, 32, 3, "bf16", 2, 8),
-    (16, 1, 1, "bf16", 2, 1),     # 16 vectors: one full MMA tile
-    (32, 8, 8, "bf16", 1, 1),     # 32 vectors: more than one MMA tile holds
-    (32, 8, 1, "f32", 1, 4),      # fp32 stays on the CUDA cores
+def test_odd_vector_counts_above_15_run_on_the_tensor_cores(nsv):
+    p = nsv.plan_split(_shape(nsv, query_len=17), num_sms=152)
+    assert p.consumer == nsv.CONSUMER_TENSOR and p.threads == (p.kv_heads_per_cta * 2 + 1) * 32
+
+
+@pytest.mark.parametrize("heads,kv_heads,qlen,dtype,consumer,hg,warps", [
+    (32, 32, 1, "bf16", 1, 8, 8),    # one vector per KV head: CUDA cores
+    (32, 8, 1, "bf16", 2, 8, 8),     # 4 query heads per KV head: tensor cores
+    (32, 32, 4, "bf16", 2, 8, 8),    # 4 query tokens
+    (32, 32, 3, "bf16", 2, 8, 8),
+    (16, 1, 1, "bf16", 2, 1, 1),     # 16 vectors: one full MMA tile
+    (32, 8, 8, "bf16", 2, 4, 8),     # 32 vectors: two MMA tiles, two warps per KV head
+    (32, 8, 5, "bf16", 2, 4, 8),     # 20 vectors
+    (32, 8, 1, "f32", 1, 4, 8),      # fp32 stays on the CUDA cores
 ])
-def test_plan_consumer_choice(nsv, heads, kv_heads, qlen, dtype, consumer, hg):
-    """The default plan runs bf16 shapes with 2 to 16 query vectors per KV
-    head on the tensor cores, one warp per KV head of the group."""
+def test_plan_consumer_choice(nsv, heads, kv_heads, qlen, dtype, consumer, hg, warps):
+    """The default plan runs bf16 shapes with 2 or more query vectors per KV
+    head on the tensor cores: one warp per KV head up to 8 vectors, one per
+    16 vectors beyond."""
     p = nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen,
                               dtype=nsv.BF16 if dtype == "bf16" else nsv.F32), num_sms=152)
     assert p.consumer == consumer and p.kv_heads_per_cta == hg
+    assert p.threads == (warps + 1) * 32
     if consumer == nsv.CONSUMER_TENSOR:
-        assert p.vectors_per_warp == 1 and p.threads == (hg + 1) * 32
+        assert p.vectors_per_warp == 1
     assert p.reserved == 0
 
 
@@ -144,7 +156,6 @@ def test_plan_consumer_choice(nsv, heads, kv_heads, qlen, dtype, consumer, hg):
     (dict(num_kv_heads=32), dict(consumer=2)),                      # 1 vector per KV head
     (dict(num_kv_heads=8, dtype=1), dict(consumer=2, vectors_per_warp=2)),
     (dict(num_kv_heads=8, dtype=0), dict(consumer=2)),              # fp32
-    (dict(num_kv_heads=8, query_len=8), dict(consumer=2)),          # 32 vectors
     (dict(num_kv_heads=8), dict(consumer=3)),
     (dict(num_kv_heads=8, num_blocks=(1 << 24)), dict(consumer=2)), # TMA row index overflows
 ])
