@@ -183,8 +183,20 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   }
   if (L.total > (uint32_t)kSmemPerCta) return NSV_ERR_RANGE;
   const int threads = (hg * wpk + 1) * 32;
-  const int fit = kSmemPerSm / (int)(L.total + kSmemReserved);
+  int fit = kSmemPerSm / (int)(L.total + kSmemReserved);
   const int fit_threads = kThreadsPerSm / threads;
+  if (tensor && auto_stages && cps <= 0 && fit < 2) {
+    // One CTA per SM either way: spend the rest of its shared memory on a
+    // deeper ring (up to 6 stages), which keeps more bytes in flight for
+    // the consumers that would otherwise wait on HBM latency.
+    while (stages < 6) {
+      const SmemLayout L2 = make_layout(elem, s->head_dim, hg, nvec, stages + 1, rows_for_layout);
+      if (L2.total > (uint32_t)kSmemPerCta) break;
+      ++stages;
+      L = L2;
+    }
+    fit = kSmemPerSm / (int)(L.total + kSmemReserved);
+  }
   if (cps <= 0) {
     cps = fit < 2 ? fit : 2;
     if (cps > fit_threads) cps = fit_threads;
