@@ -18,16 +18,24 @@
 //    [c*U/G, (c+1)*U/G): every CTA streams the same number of blocks (stream-K
 //    style), whatever the length mix.  Every CTA derives the sequence from
 //    context_lens in shared memory, so the launch depends on shape alone.
-//  * Warp 0 is the producer.  Per block it issues two cp.async.bulk copies
-//    (the head group's K tiles and V tiles are each one contiguous run in the
-//    [block][kv_head][token][dim] pool) into a ring of shared-memory stages
-//    guarded by mbarriers, plus the query vectors at each segment's first
-//    stage.  The block ids of the next 32 units are loaded a window ahead.
-//  * Warps 1..N are consumers, one per query head.  A lane owns 16 bytes of
-//    a key row; the score of each token of the tile is reduced with a
-//    transposing butterfly (one shuffle per token instead of five), the
-//    tile max with a plain butterfly, probabilities go through shared memory
-//    to the lanes that own the value dims, and P.V accumulates in fp32.
+//  * Warp 0 is the producer.  Per block it copies the head group's K tiles
+//    and V tiles (each one contiguous run in the [block][kv_head][token][dim]
+//    pool) into a ring of shared-memory stages guarded by mbarriers: two
+//    cp.async.bulk copies for the CUDA-core consumer, 2-D TMA tiles with the
+//    128-byte swizzle for the tensor-core one; plus the query vectors at each
+//    segment's first stage.  The block ids of the next 32 units are loaded a
+//    window ahead.  A slot-table block that is not one aligned run of slots
+//    is gathered token by token by the producer warp instead.
+//  * Warps 1..N are consumers.  On the CUDA cores (fp32, or one query
+//    vector per KV head) a warp serves 1, 2 or 4 query vectors of one KV
+//    head: a lane owns 16 bytes of a key row; the score of each token of the
+//    tile is reduced with a transposing butterfly (one shuffle per token
+//    instead of five), the tile max with a plain butterfly, probabilities go
+//    through shared memory to the lanes that own the value dims, and P.V
+//    accumulates in fp32.  On the tensor cores (bf16, 2 to 32 query vectors
+//    per KV head) the same two contractions run as mma.sync.m16n8k16: with
+//    the block's 16 tokens as the MMA rows for up to 8 vectors, with the
+//    vectors as the rows (16 per warp) beyond.
 //  * A segment (a CTA's run of one row) that covers the whole row writes
 //    `out` directly.  A row cut by CTA boundaries leaves one partial (m, l,
 //    acc) per CTA it crosses -- at most two per CTA.  Each piece's CTA then
@@ -35,7 +43,6 @@
 //    last merges the pieces (flash-decoding style) and writes `out`.  Nobody
 //    waits for anybody: the last arrival finds every partial already
 //    written.  Empty rows get their zero output from the consumers up front.
-//  * No tensor cores: one query per head makes each tile a GEMV.
 // Every wait is bounded; a wait that gives up sets NSV_DEV_TIMEOUT and the
 // kernel returns.  Bad lengths and block ids are skipped and flagged.
 
