@@ -107,7 +107,7 @@ def recorded_traffic(consumer, read_bytes):
             sha = hashlib.sha256(f.read()).hexdigest()
         if d.get("decode_cu_sha256") != sha:
             return None
-        cap = d["captures"]["tensor" if consumer == 2 else "cuda"]
+        cap = d["captures"][{1: "cuda", 2: "tensor", 3: "tensor_vector_rows"}[consumer]]
         return cap["traffic_over_algorithmic"] * read_bytes
     except (OSError, ValueError, KeyError):
         return None
@@ -412,7 +412,8 @@ def run_nsv(args, wl):
                      "frac": achieved / peak, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback",
                      "kernel": "decode read (decode_kernel, %s consumer)"
-                               % ("tensor-core" if plan.consumer == 2 else "CUDA-core"),
+                               % {1: "CUDA-core", 2: "tensor-core",
+                                  3: "tensor-core, vectors as rows"}[plan.consumer],
                      "bytes_per_launch": wl.read_bytes(), "us_per_launch": ms_read * 1e3,
                      "traffic": recorded_traffic(plan.consumer, wl.read_bytes())},
         "e2e": {"value": whole_job_gbs(step_bytes, ws, e2e_ms), "unit": "GB/s",

@@ -149,7 +149,7 @@ typedef struct nsv_plan {
                                  that share a KV head) one consumer warp
                                  serves from each K/V tile: 1, 2 or 4
                                  (CUDA-core consumer; 1 for the tensor one) */
-    int32_t consumer;         /* NSV_CONSUMER_CUDA or NSV_CONSUMER_TENSOR */
+    int32_t consumer;         /* NSV_CONSUMER_CUDA, _TENSOR or _TENSOR_VECTOR_ROWS */
     int32_t reserved;         /* 0 */
     int64_t workspace_bytes;  /* device scratch the read needs */
 } nsv_plan;
@@ -164,14 +164,21 @@ typedef struct nsv_plan {
  *                       accumulation: scores against the block's keys, then
  *                       the weighted sum of its values, with the
  *                       probabilities rounded to bf16 for the second
- *                       product.  Up to 8 vectors use the block's 16 tokens
- *                       as the MMA rows (one warp per KV head); 9 to 32 use
- *                       the vectors as the rows, 16 per warp.  K/V tiles
- *                       arrive by 2-D TMA with a 128-byte swizzle.  Needs
+ *                       product.  The block's 16 tokens are the MMA rows and
+ *                       the vectors its columns, 8 per warp (one to four
+ *                       warps per KV head).  K/V tiles arrive by 2-D TMA
+ *                       with a 128-byte swizzle.  Needs
  *                       (num_blocks+1)*num_kv_heads*16 < 2^31.
- * The default plan takes the tensor consumer for bf16 shapes with 2 or more
+ *  NSV_CONSUMER_TENSOR_VECTOR_ROWS: the same with the query vectors as the
+ *                       MMA rows, 16 per warp (one or two warps per KV head).
+ * The default plan takes NSV_CONSUMER_TENSOR for bf16 shapes with 2 or more
  * query vectors per KV head, and the CUDA-core one otherwise. */
-enum { NSV_CONSUMER_AUTO = 0, NSV_CONSUMER_CUDA = 1, NSV_CONSUMER_TENSOR = 2 };
+enum {
+    NSV_CONSUMER_AUTO = 0,
+    NSV_CONSUMER_CUDA = 1,
+    NSV_CONSUMER_TENSOR = 2,
+    NSV_CONSUMER_TENSOR_VECTOR_ROWS = 3
+};
 
 /*
  * Plan the decode read for `shape` on a GPU with `num_sms` SMs (<= 0: the
@@ -195,6 +202,18 @@ NSV_API int nsv_plan_split(const nsv_shape *shape, int num_sms, nsv_plan *plan);
 NSV_API int nsv_plan_custom(const nsv_shape *shape, int num_sms, int kv_heads_per_cta,
                             int stages, int ctas_per_sm, int grid, int vectors_per_warp,
                             int consumer, nsv_plan *plan);
+
+/*
+ * How many CTAs of `plan`'s kernel one SM of the current device holds at the
+ * plan's threads and shared memory (the CUDA occupancy calculator on the
+ * compiled kernel).  A plan's grid is sized as num_sms * ctas_per_sm on the
+ * assumption that all of them are resident at once; this reports whether
+ * the device agrees (*ctas_per_sm >= plan->ctas_per_sm).  `plan` must be one
+ * the planner made for `shape`.  Returns NSV_ERR_{NULLPTR, RANGE, CUDA} or a
+ * shape error.
+ */
+NSV_API int nsv_plan_resident_ctas(const nsv_shape *shape, const nsv_plan *plan,
+                                   int *ctas_per_sm);
 
 /*
  * KV append: for every row r (and each of its query_len new tokens j),

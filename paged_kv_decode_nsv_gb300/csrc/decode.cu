@@ -63,7 +63,7 @@ constexpr float kRescaleSlack = 8.f;
 // Tensor-core consumer forms (the kernel's MMA template argument; 0: CUDA cores).
 constexpr int kMmaVectorRows = 1;  // query vectors as the MMA rows (M = 16)
 constexpr int kMmaTokenRows = 2;   // the block's tokens as the MMA rows, vectors as N = 8
-constexpr int kMmaTokenRowsMaxVectors = 8;
+constexpr int kMmaCols = 8;        // query vectors per warp with tokens as rows
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -645,8 +645,10 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
   }
 }
 
-// Tensor-core consumer with the block's 16 tokens as the MMA rows (bf16, at
-// most 8 query vectors per KV head, one warp per KV head).  Per block:
+// Tensor-core consumer with the block's 16 tokens as the MMA rows (bf16): a
+// KV head's query vectors (2 to 32) are the MMA columns, 8 per warp, so one
+// to four warps per KV head read the same K/V tile.  Each warp zeroes the
+// tile's empty V rows itself (they all write the same zeros).  Per block:
 // S^T = K.Q^T (M = 16 tokens, N = 8 vectors, K = head_dim), the online
 // softmax down the columns of S^T, then O^T += V^T.P^T (M = head_dim, N = 8
 // vectors, K = 16 tokens).  The probabilities go from the S^T accumulators
@@ -665,9 +667,12 @@ __device__ __forceinline__ void consume_mma_t(const DecodeParams& p, unsigned ch
   const int G = p.group, NQ = p.query_len, HG = p.heads_per_cta, S = p.stages;
   if (warp > ncw) return;
   const int cw = warp - 1;
-  const int kvl = cw;                   // one warp per KV head of the group
-  const int vpk = G * NQ;               // its query vectors (<= 8)
-  const int vbase = kvl * vpk;
+  const int vpk = G * NQ;               // query vectors per KV head (<= 32)
+  const int wpk = ncw / HG;             // warps per KV head: one per 8 vectors
+  const int kvl = cw / wpk;             // this warp's KV head within the group
+  const int v0w = (cw - kvl * wpk) * kMmaCols;  // its first vector of that KV head
+  const int nvw = min(kMmaCols, vpk - v0w);     // and how many it runs (<= 8)
+  const int vbase = kvl * vpk + v0w;
   const int g = lane >> 2, t4 = lane & 3;
   const int hq = HG * G;
   const uint32_t half_bytes = (uint32_t)HG * kBlock * 128;
@@ -675,15 +680,16 @@ __device__ __forceinline__ void consume_mma_t(const DecodeParams& p, unsigned ch
 
   // B-operand column g: the query vector this lane loads.  Accumulator
   // columns 2*t4 + c (c = 0, 1): the vectors whose softmax state it keeps.
-  const bool gok = g < vpk;
-  const int gqh = kvl * G + (gok ? g : 0) / NQ, gjq = (gok ? g : 0) % NQ;
+  const bool gok = g < nvw;
+  const int gv = v0w + (gok ? g : 0);
+  const int gqh = kvl * G + gv / NQ, gjq = gv % NQ;
   bool cok[2];
   int cqh[2], cjq[2];
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     const int v = 2 * t4 + c;
-    cok[c] = v < vpk;
-    const int vv = cok[c] ? v : 0;
+    cok[c] = v < nvw;
+    const int vv = v0w + (cok[c] ? v : 0);
     cqh[c] = kvl * G + vv / NQ;
     cjq[c] = vv % NQ;
   }
@@ -849,7 +855,7 @@ __device__ __forceinline__ void consume_mma_t(const DecodeParams& p, unsigned ch
           }
           if (g == 0) p.ws_ml[slot] = make_float2(m[c], lt[c]);
         }
-        finish_cut_row<T, D>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, vbase, vpk, ncw, cw,
+        finish_cut_row<T, D>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, vbase, nvw, ncw, cw,
                              lane, s_merge);
       }
     }
@@ -860,7 +866,10 @@ __device__ __forceinline__ void consume_mma_t(const DecodeParams& p, unsigned ch
 
 template <typename T, int D, int QW, int MMA>
 __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
-                                      : (QW <= 2 ? kMaxThreads : kMaxThreadsMulti), 1)
+                                      : (QW <= 2 ? kMaxThreads : kMaxThreadsMulti))
+    __maxnreg__(decode_regs(MMA == kMmaTokenRows    ? kConsumerTensor
+                            : MMA == kMmaVectorRows ? kConsumerTensorVectorRows
+                                                    : kConsumerCuda, QW))
     decode_kernel(const __grid_constant__ DecodeParams p) {
   using E = Elem<T>;
   constexpr int kDpl = E::kDpl;           // dims per lane per 16-byte load
@@ -879,9 +888,9 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
   const int NQ = p.query_len;
   const int HG = p.heads_per_cta;
   const int nvec = HG * G * NQ;          // query vectors per CTA
-  // consumer warps: per KV head one (tokens as MMA rows) or one per 16
-  // vectors (vectors as MMA rows); QW vectors per warp on the CUDA cores
-  const int ncw = MMA == kMmaTokenRows    ? HG
+  // consumer warps: per KV head one per 8 vectors (tokens as MMA rows) or
+  // one per 16 (vectors as MMA rows); QW vectors per warp on the CUDA cores
+  const int ncw = MMA == kMmaTokenRows    ? HG * ((G * NQ + kMmaCols - 1) / kMmaCols)
                   : MMA == kMmaVectorRows ? HG * ((G * NQ + kMmaRows - 1) / kMmaRows)
                                           : nvec / QW;
   const int S = p.stages;
@@ -1369,11 +1378,11 @@ void launch_typed(const DecodeParams& p, int qw, int consumer, int grid, int thr
                   cudaStream_t stream) {
   if constexpr (sizeof(T) == 2) {
     if (consumer == kConsumerTensor) {
-      // Up to 8 query vectors per KV head: tokens as the MMA rows; more: vectors.
-      if (p.group * p.query_len <= kMmaTokenRowsMaxVectors)
-        decode_kernel<T, D, 1, kMmaTokenRows><<<grid, threads, smem, stream>>>(p);
-      else
-        decode_kernel<T, D, 1, kMmaVectorRows><<<grid, threads, smem, stream>>>(p);
+      decode_kernel<T, D, 1, kMmaTokenRows><<<grid, threads, smem, stream>>>(p);
+      return;
+    }
+    if (consumer == kConsumerTensorVectorRows) {
+      decode_kernel<T, D, 1, kMmaVectorRows><<<grid, threads, smem, stream>>>(p);
       return;
     }
   }
@@ -1385,7 +1394,36 @@ void launch_typed(const DecodeParams& p, int qw, int consumer, int grid, int thr
     decode_kernel<T, D, 1, 0><<<grid, threads, smem, stream>>>(p);
 }
 
+template <typename T, int D>
+cudaError_t occupancy_typed(int qw, int consumer, int threads, int smem, int* ctas) {
+  const void* fn;
+  if constexpr (sizeof(T) == 2) {
+    if (consumer == kConsumerTensor)
+      fn = reinterpret_cast<const void*>(decode_kernel<T, D, 1, kMmaTokenRows>);
+    else if (consumer == kConsumerTensorVectorRows)
+      fn = reinterpret_cast<const void*>(decode_kernel<T, D, 1, kMmaVectorRows>);
+    else
+      fn = qw == 4   ? reinterpret_cast<const void*>(decode_kernel<T, D, 4, 0>)
+           : qw == 2 ? reinterpret_cast<const void*>(decode_kernel<T, D, 2, 0>)
+                     : reinterpret_cast<const void*>(decode_kernel<T, D, 1, 0>);
+  } else {
+    fn = qw == 4   ? reinterpret_cast<const void*>(decode_kernel<T, D, 4, 0>)
+         : qw == 2 ? reinterpret_cast<const void*>(decode_kernel<T, D, 2, 0>)
+                   : reinterpret_cast<const void*>(decode_kernel<T, D, 1, 0>);
+  }
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, fn, threads, (size_t)smem);
+}
+
 }  // namespace
+
+cudaError_t decode_occupancy(int dtype, int head_dim, int qw, int consumer, int threads,
+                             int smem, int* ctas) {
+  if (dtype == NSV_F32)
+    return head_dim == 64 ? occupancy_typed<float, 64>(qw, consumer, threads, smem, ctas)
+                          : occupancy_typed<float, 128>(qw, consumer, threads, smem, ctas);
+  return head_dim == 64 ? occupancy_typed<__nv_bfloat16, 64>(qw, consumer, threads, smem, ctas)
+                        : occupancy_typed<__nv_bfloat16, 128>(qw, consumer, threads, smem, ctas);
+}
 
 cudaError_t launch_wait_probe(unsigned long long limit_ns, unsigned long long* result,
                               cudaStream_t stream) {

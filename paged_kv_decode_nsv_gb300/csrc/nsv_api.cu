@@ -7,6 +7,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "nsv_common.cuh"
@@ -131,16 +132,21 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   const bool tensor_ok = s->dtype == NSV_BF16 && vpk >= 2 && vpk <= kMaxVectorsPerKvHead &&
                          tensor_rows_fit(s);
   if (consumer == NSV_CONSUMER_AUTO) {
-    // The tensor cores pay off once several query vectors share a K/V tile:
-    // one MMA row each, where the CUDA cores repeat the work per vector.
-    consumer = (tensor_ok && qw <= 0) ? kConsumerTensor : kConsumerCuda;
-  } else if (consumer == kConsumerTensor) {
+    // The tensor cores pay off once several query vectors share a K/V tile,
+    // where the CUDA cores repeat the work per vector.  Up to 8 vectors the
+    // tokens are the MMA rows (one warp per KV head); beyond, the vectors
+    // (16 per warp), which measured faster than 8 per warp with tokens as rows.
+    consumer = !(tensor_ok && qw <= 0) ? kConsumerCuda
+               : vpk <= 8              ? kConsumerTensor
+                                       : kConsumerTensorVectorRows;
+  } else if (consumer == kConsumerTensor || consumer == kConsumerTensorVectorRows) {
     if (!tensor_ok || qw > 1) return NSV_ERR_RANGE;
   } else if (consumer != kConsumerCuda) {
     return NSV_ERR_RANGE;
   }
-  if (consumer == kConsumerTensor) {
-    qw = 1;  // unused: a warp runs its KV head's vectors as MMA rows
+  const bool tensor = consumer != kConsumerCuda;
+  if (tensor) {
+    qw = 1;  // unused: a warp runs 8 or 16 of its KV head's vectors on the MMAs
   } else if (qw <= 0) {
     // Two vectors per warp when they pair up: one widening of each tile
     // serves both, and their registers still let 16 warps run per SM (two
@@ -151,10 +157,11 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
              vpk / qw > max_consumer_warps(qw)) {
     return NSV_ERR_RANGE;
   }
-  const bool tensor = consumer == kConsumerTensor;
-  // consumer warps per KV head: on the tensor cores one (tokens as the MMA
-  // rows, up to 8 vectors) or one per 16 vectors (vectors as the rows)
-  const int wpk = tensor ? (vpk <= 8 ? 1 : (vpk + kMmaRows - 1) / kMmaRows) : vpk / qw;
+  // consumer warps per KV head: on the tensor cores one per 8 vectors
+  // (tokens as the MMA rows) or one per 16 (vectors as the rows)
+  const int wpk = consumer == kConsumerTensor            ? (vpk + 7) / 8
+                  : consumer == kConsumerTensorVectorRows ? (vpk + kMmaRows - 1) / kMmaRows
+                                                          : vpk / qw;
   const int max_warps = tensor ? kMaxConsumerWarpsMulti : max_consumer_warps(qw);
   const int tile = kBlock * s->head_dim * elem;
   if (hg <= 0) {
@@ -184,7 +191,10 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   if (L.total > (uint32_t)kSmemPerCta) return NSV_ERR_RANGE;
   const int threads = (hg * wpk + 1) * 32;
   int fit = kSmemPerSm / (int)(L.total + kSmemReserved);
-  const int fit_threads = kThreadsPerSm / threads;
+  // CTAs one SM holds by threads and by registers (each kernel variant's
+  // register count is fixed at compile time)
+  const int fit_threads =
+      std::min(kThreadsPerSm / threads, ctas_by_registers(threads, decode_regs(consumer, qw)));
   if (tensor && auto_stages && cps <= 0 && fit < 2) {
     // One CTA per SM either way: spend the rest of its shared memory on a
     // deeper ring (up to 6 stages), which keeps more bytes in flight for
@@ -319,7 +329,7 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   p.qscale = scale * 1.4426950408889634f;  // log2(e): the kernels use exp2
   memset(&p.tmap_k, 0, sizeof(p.tmap_k));
   memset(&p.tmap_v, 0, sizeof(p.tmap_v));
-  if (plan.consumer == kConsumerTensor) {
+  if (plan.consumer == kConsumerTensor || plan.consumer == kConsumerTensorVectorRows) {
     // The pools as [(num_blocks+1)*kv_heads*16 rows][head_dim] bf16; a box is
     // 64 dims (128 bytes, the swizzle span) by the head group's 16-token tiles.
     const cuuint64_t dims[2] = {(cuuint64_t)s->head_dim,
@@ -376,6 +386,23 @@ NSV_API int nsv_plan_custom(const nsv_shape* shape, int num_sms, int kv_heads_pe
                             int consumer, nsv_plan* plan) {
   return make_plan(shape, num_sms, kv_heads_per_cta, stages, ctas_per_sm, grid,
                    vectors_per_warp, consumer, plan);
+}
+
+NSV_API int nsv_plan_resident_ctas(const nsv_shape* shape, const nsv_plan* plan,
+                                   int* ctas_per_sm) {
+  if (!ctas_per_sm) return NSV_ERR_NULLPTR;
+  if (!plan) return NSV_ERR_NULLPTR;
+  nsv_plan use;
+  int rc = check_plan(shape, plan, &use);
+  if (rc) return rc;
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d)) != NSV_OK) return rc;
+  int n = 0;
+  if (decode_occupancy(shape->dtype, shape->head_dim, use.vectors_per_warp, use.consumer,
+                       use.threads, use.smem_bytes, &n) != cudaSuccess)
+    return cuda_fail();
+  *ctas_per_sm = n;
+  return NSV_OK;
 }
 
 NSV_API int nsv_kv_write(const nsv_shape* s, const void* k_new, const void* v_new,

@@ -23,12 +23,27 @@ __host__ __device__ constexpr int max_consumer_warps(int qw) {
 // Largest number of query vectors (query heads x query tokens) that share
 // one KV head.
 constexpr int kMaxVectorsPerKvHead = 32;
-// The tensor-core consumer: one warp per KV head, its query vectors are the
-// rows of one 16-row MMA.
+// Rows of the tensor-core MMA (m16n8k16): 16 query vectors per warp when the
+// vectors are the rows.
 constexpr int kMmaRows = 16;
-enum : int { kConsumerCuda = 1, kConsumerTensor = 2 };
+enum : int { kConsumerCuda = 1, kConsumerTensor = 2, kConsumerTensorVectorRows = 3 };
 constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
 constexpr int kMaxThreadsMulti = (kMaxConsumerWarpsMulti + 1) * 32;
+
+// Registers per thread of each decode-kernel variant, fixed at compile time
+// (__maxnreg__) so that the planner can size the grid to the CTAs that are
+// really resident: CUDA-core consumer with 1 or 2 vectors per warp, and
+// every other variant (4 vectors per warp, both tensor-core forms).
+constexpr int kRegsNarrow = 96;
+constexpr int kRegsWide = 168;
+__host__ __device__ constexpr int decode_regs(int consumer, int qw) {
+  return (consumer == kConsumerCuda && qw <= 2) ? kRegsNarrow : kRegsWide;
+}
+// CTAs of `threads` threads at `regs` registers each that one SM's 64 K
+// registers hold (allocated per warp in units of 256).
+__host__ __device__ constexpr int ctas_by_registers(int threads, int regs) {
+  return (65536 / (((regs * 32 + 255) / 256) * 256)) / ((threads + 31) / 32);
+}
 // Largest batch the decode kernel's per-CTA row tables hold.
 constexpr int kMaxRows = 8192;
 
@@ -158,6 +173,10 @@ cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int qw
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
 // One-time per-device attribute set-up of the decode kernels.
 cudaError_t prepare_decode_kernels();
+// CTAs of the plan's kernel variant that one SM of the current device holds
+// (cudaOccupancyMaxActiveBlocksPerMultiprocessor).
+cudaError_t decode_occupancy(int dtype, int head_dim, int qw, int consumer, int threads,
+                             int smem, int* ctas);
 // The bounded-wait self-test kernel (result: device [gave_up, waited_ns]).
 cudaError_t launch_wait_probe(unsigned long long limit_ns, unsigned long long* result,
                               cudaStream_t stream);

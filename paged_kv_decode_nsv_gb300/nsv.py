@@ -32,7 +32,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 ABI_VERSION = 101  # the layout of Shape and Plan below
 F32, BF16 = 0, 1
-CONSUMER_AUTO, CONSUMER_CUDA, CONSUMER_TENSOR = 0, 1, 2
+CONSUMER_AUTO, CONSUMER_CUDA, CONSUMER_TENSOR, CONSUMER_TENSOR_VECTOR_ROWS = 0, 1, 2, 3
 DEV_BAD_CTX, DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_TIMEOUT = 1, 2, 4, 8
 ERRORS = {0: "NSV_OK", -1: "NSV_ERR_NULLPTR", -2: "NSV_ERR_DTYPE", -3: "NSV_ERR_SHAPE",
           -4: "NSV_ERR_ALIGN", -5: "NSV_ERR_RANGE", -6: "NSV_ERR_CAPTURE", -7: "NSV_ERR_CUDA",
@@ -73,6 +73,8 @@ _lib.nsv_plan_split.restype = _i32
 _lib.nsv_plan_split.argtypes = [_SP, _i32, _PP]
 _lib.nsv_plan_custom.restype = _i32
 _lib.nsv_plan_custom.argtypes = [_SP, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _PP]
+_lib.nsv_plan_resident_ctas.restype = _i32
+_lib.nsv_plan_resident_ctas.argtypes = [_SP, _PP, ctypes.POINTER(ctypes.c_int)]
 _lib.nsv_kv_write.restype = _i32
 _lib.nsv_kv_write.argtypes = [_SP, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.nsv_paged_decode.restype = _i32
@@ -181,6 +183,14 @@ def plan_custom(shape, num_sms=0, kv_heads_per_cta=0, stages=0, ctas_per_sm=0, g
                                 int(stages), int(ctas_per_sm), int(grid), int(vectors_per_warp),
                                 int(consumer), ctypes.byref(p)), "nsv_plan_custom")
     return p
+
+
+def plan_resident_ctas(shape, plan):
+    """CTAs of the plan's kernel that one SM of the current device holds."""
+    n = ctypes.c_int(0)
+    _check(_lib.nsv_plan_resident_ctas(ctypes.byref(shape), ctypes.byref(plan), ctypes.byref(n)),
+           "nsv_plan_resident_ctas")
+    return n.value
 
 
 def workspace_for(plan, device=None):

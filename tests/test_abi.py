@@ -89,9 +89,9 @@ def test_plan_shapes_of_every_workload(nsv):
         nvec = p.kv_heads_per_cta * (wl.heads // wl.kv_heads) * wl.query_len
         assert 0 < p.workspace_bytes < 152 * 4 * 2 * nvec * (wl.head_dim * 4 + 8) + (1 << 16)
         assert wl.kv_heads % p.kv_heads_per_cta == 0
-        if p.consumer == nsv.CONSUMER_TENSOR:  # one warp per KV head, or per 16 vectors
-            vpk = (wl.heads // wl.kv_heads) * wl.query_len
-            wpk = 1 if vpk <= 8 else -(-vpk // 16)
+        vpk = (wl.heads // wl.kv_heads) * wl.query_len
+        if p.consumer != nsv.CONSUMER_CUDA:  # one warp per 8 or per 16 vectors of a KV head
+            wpk = -(-vpk // (8 if p.consumer == nsv.CONSUMER_TENSOR else 16))
             assert p.vectors_per_warp == 1 and p.threads // 32 - 1 == p.kv_heads_per_cta * wpk
         else:
             assert p.consumer == nsv.CONSUMER_CUDA
@@ -126,7 +126,17 @@ def test_plan_refuses_too_many_query_vectors(nsv, heads, kv_heads, qlen, dtype):
 
 def test_odd_vector_counts_above_15_run_on_the_tensor_cores(nsv):
     p = nsv.plan_split(_shape(nsv, query_len=17), num_sms=152)
-    assert p.consumer == nsv.CONSUMER_TENSOR and p.threads == (p.kv_heads_per_cta * 2 + 1) * 32
+    assert p.consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS
+    assert p.threads == (p.kv_heads_per_cta * 2 + 1) * 32
+
+
+@pytest.mark.parametrize("qlen,warps", [(2, 1), (16, 1), (17, 2), (32, 2)])
+def test_plan_vector_rows_form(nsv, qlen, warps):
+    """NSV_CONSUMER_TENSOR_VECTOR_ROWS: one warp per 16 vectors of a KV head."""
+    p = nsv.plan_custom(_shape(nsv, query_len=qlen), num_sms=152,
+                        consumer=nsv.CONSUMER_TENSOR_VECTOR_ROWS)
+    assert p.consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS
+    assert p.threads == (p.kv_heads_per_cta * warps + 1) * 32
 
 
 @pytest.mark.parametrize("heads,kv_heads,qlen,dtype,consumer,hg,warps", [
@@ -134,20 +144,20 @@ def test_odd_vector_counts_above_15_run_on_the_tensor_cores(nsv):
     (32, 8, 1, "bf16", 2, 8, 8),     # 4 query heads per KV head: tensor cores
     (32, 32, 4, "bf16", 2, 8, 8),    # 4 query tokens
     (32, 32, 3, "bf16", 2, 8, 8),
-    (16, 1, 1, "bf16", 2, 1, 1),     # 16 vectors: one full MMA tile
-    (32, 8, 8, "bf16", 2, 4, 8),     # 32 vectors: two MMA tiles, two warps per KV head
-    (32, 8, 5, "bf16", 2, 4, 8),     # 20 vectors
+    (16, 1, 1, "bf16", 3, 1, 1),     # 16 vectors: one warp, vectors as the MMA rows
+    (32, 8, 8, "bf16", 3, 4, 8),     # 32 vectors: two warps per KV head
+    (32, 8, 5, "bf16", 3, 4, 8),     # 20 vectors
     (32, 8, 1, "f32", 1, 4, 8),      # fp32 stays on the CUDA cores
 ])
 def test_plan_consumer_choice(nsv, heads, kv_heads, qlen, dtype, consumer, hg, warps):
     """The default plan runs bf16 shapes with 2 or more query vectors per KV
-    head on the tensor cores: one warp per KV head up to 8 vectors, one per
-    16 vectors beyond."""
+    head on the tensor cores: up to 8 with the tokens as the MMA rows (one
+    warp per KV head), beyond with the vectors as the rows (16 per warp)."""
     p = nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen,
                               dtype=nsv.BF16 if dtype == "bf16" else nsv.F32), num_sms=152)
     assert p.consumer == consumer and p.kv_heads_per_cta == hg
     assert p.threads == (warps + 1) * 32
-    if consumer == nsv.CONSUMER_TENSOR:
+    if consumer != nsv.CONSUMER_CUDA:
         assert p.vectors_per_warp == 1
     assert p.reserved == 0
 
@@ -156,7 +166,8 @@ def test_plan_consumer_choice(nsv, heads, kv_heads, qlen, dtype, consumer, hg, w
     (dict(num_kv_heads=32), dict(consumer=2)),                      # 1 vector per KV head
     (dict(num_kv_heads=8, dtype=1), dict(consumer=2, vectors_per_warp=2)),
     (dict(num_kv_heads=8, dtype=0), dict(consumer=2)),              # fp32
-    (dict(num_kv_heads=8), dict(consumer=3)),
+    (dict(num_kv_heads=8), dict(consumer=4)),
+    (dict(num_kv_heads=8, dtype=0), dict(consumer=3)),              # fp32
     (dict(num_kv_heads=8, num_blocks=(1 << 24)), dict(consumer=2)), # TMA row index overflows
 ])
 def test_plan_tensor_consumer_refusals(nsv, kw, ckw):
@@ -257,3 +268,24 @@ def test_bounded_wait_selftest_refuses_limits_out_of_range(nsv, limit):
 
 def test_bounded_wait_selftest_refuses_null_results(nsv):
     assert nsv._lib.nsv_selftest_bounded_wait(1000000, None, None, None) == -1
+
+
+@pytest.mark.parametrize("kw,regs", [
+    (dict(), 96), (dict(num_kv_heads=8), 168), (dict(num_kv_heads=8, query_len=8), 168),
+    (dict(num_kv_heads=8, dtype=0), 96),
+])
+def test_plan_fits_its_ctas_by_registers(nsv, kw, regs):
+    """A plan's CTAs per SM fit the SM's 64 K registers at the variant's
+    fixed register count (allocated per warp in units of 256)."""
+    p = nsv.plan_split(_shape(nsv, **kw), num_sms=152)
+    warps = p.threads // 32
+    per_warp = -(-regs * 32 // 256) * 256
+    assert p.ctas_per_sm * warps <= 65536 // per_warp
+
+
+def test_cuda_core_plan_with_17_warps_takes_one_cta_per_sm(nsv):
+    """16 consumer warps + the producer at 96 registers: one CTA per SM (two
+    would need 34 warps' registers)."""
+    p = nsv.plan_custom(_shape(nsv, num_kv_heads=8, query_len=8), num_sms=152,
+                        consumer=nsv.CONSUMER_CUDA)
+    assert p.threads == 17 * 32 and p.ctas_per_sm == 1 and p.grid == 152

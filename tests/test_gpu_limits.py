@@ -91,3 +91,33 @@ def test_head_dim_64_grouped_multi_query(nsv, dtype):
     out = gpu_step(wl, inp)
     assert status()[0] == 0
     assert_parity(dtype, gpu_out_f64(out), oracle_step(wl, host))
+
+
+def _occupancy_shapes():
+    base = dict(rows=256, head_dim=128, max_blocks=512, num_blocks=70000)
+    for dt in (0, 1):
+        for heads, kv, ql in [(32, 32, 1), (32, 8, 1), (32, 32, 4), (32, 8, 8), (128, 8, 1),
+                              (16, 16, 17), (8, 8, 3)]:
+            for d in (64, 128):
+                yield dict(base, num_heads=heads, num_kv_heads=kv, query_len=ql, dtype=dt,
+                           head_dim=d)
+
+
+def test_every_plan_is_resident_in_one_wave(nsv):
+    """The planner sizes the persistent grid to num_sms x ctas_per_sm; the
+    device's occupancy calculator must agree that that many CTAs of the
+    plan's kernel fit on one SM at once, for every consumer form it offers."""
+    checked = 0
+    for kw in _occupancy_shapes():
+        shape = nsv.make_shape(**kw)
+        for extra in (dict(), dict(consumer=1), dict(consumer=2), dict(consumer=3),
+                      dict(consumer=1, vectors_per_warp=4), dict(kv_heads_per_cta=1),
+                      dict(kv_heads_per_cta=2, ctas_per_sm=2)):
+            try:
+                plan = nsv.plan_custom(shape, **extra)
+            except nsv.NsvError:
+                continue          # not offered for this shape
+            resident = nsv.plan_resident_ctas(shape, plan)
+            assert resident >= plan.ctas_per_sm, (kw, extra, plan.as_dict(), resident)
+            checked += 1
+    assert checked > 100

@@ -3,9 +3,10 @@ K/V tiles) against the oracle: grouped query heads and several query tokens
 per row, both head dims, every plan shape the planner allows, the slot-table
 gather, and rows whose early query tokens see no position.
 
-Up to 8 query vectors per KV head run with the block's tokens as the MMA
-rows; 9 to 32 with the query vectors as the rows, 16 per warp (two warps per
-KV head above 16).  Every test below covers both forms."""
+Two forms: the block's tokens as the MMA rows and the query vectors as its
+columns, 8 per warp (NSV_CONSUMER_TENSOR, the default); or the vectors as
+the rows, 16 per warp (NSV_CONSUMER_TENSOR_VECTOR_ROWS).  Every test runs
+both."""
 
 import numpy as np
 import pytest
@@ -18,6 +19,11 @@ from paged_kv_decode_nsv_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 LENS = [40, 513, 0, 2048, 77, 1, 15, 16, 17, 300]
+
+
+@pytest.fixture(params=[2, 3], ids=["tokens_as_rows", "vectors_as_rows"])
+def form(request):
+    return request.param
 
 
 @pytest.fixture(scope="module")
@@ -53,12 +59,12 @@ def _plan(nsv, inp, **kw):
     (8, 8, 17, 128),    # 17: an odd count, the second warp runs one vector
     (16, 2, 3, 128),    # 24
 ])
-def test_tensor_consumer_against_the_oracle(nsv, heads, kv_heads, qlen, head_dim):
+def test_tensor_consumer_against_the_oracle(nsv, form, heads, kv_heads, qlen, head_dim):
     wl = _case(heads, kv_heads, qlen, head_dim)
     inp = device_inputs(wl)
     host = host_copy(inp)
-    plan = _plan(nsv, inp, consumer=nsv.CONSUMER_TENSOR)
-    assert plan.consumer == nsv.CONSUMER_TENSOR
+    plan = _plan(nsv, inp, consumer=form)
+    assert plan.consumer == form
     out = gpu_step(wl, inp, plan=plan)
     st, walked = status()
     assert st == 0 and walked == oracle.walked_tiles(wl.context_lens, 16)
@@ -76,14 +82,14 @@ def test_tensor_consumer_against_the_oracle(nsv, heads, kv_heads, qlen, head_dim
     dict(kv_heads_per_cta=8, ctas_per_sm=1, grid=100),
 ])
 @pytest.mark.parametrize("qlen", [2, 3, 6])   # 8, 12 and 24 vectors per KV head
-def test_tensor_consumer_plans(nsv, kw, qlen):
+def test_tensor_consumer_plans(nsv, form, kw, qlen):
     wl = _case(32, 8, qlen, 128, seed=7)
     inp = device_inputs(wl)
     host = host_copy(inp)
     try:
-        plan = _plan(nsv, inp, consumer=nsv.CONSUMER_TENSOR, **kw)
-    except nsv.NsvError as e:   # 8 KV heads of 24 vectors would need 16 warps
-        assert e.code == -5 and qlen == 6 and kw.get("kv_heads_per_cta") == 8
+        plan = _plan(nsv, inp, consumer=form, **kw)
+    except nsv.NsvError as e:   # too many consumer warps, or CTAs per SM, for this shape
+        assert e.code == -5 and qlen >= 3 and ("kv_heads_per_cta" in kw or "ctas_per_sm" in kw)
         pytest.skip("plan does not fit this shape")
     out = gpu_read(wl, inp, plan=plan)
     assert status()[0] == 0
@@ -91,30 +97,30 @@ def test_tensor_consumer_plans(nsv, kw, qlen):
 
 
 @pytest.mark.parametrize("qlen", [2, 4, 7])   # 8, 16 and 28 vectors per KV head
-def test_both_consumers_agree_with_the_oracle(nsv, qlen):
+def test_both_consumers_agree_with_the_oracle(nsv, form, qlen):
     """The same inputs through the CUDA-core and the tensor-core consumer."""
     wl = _case(16, 4, qlen, 128, seed=9)
     inp = device_inputs(wl)
     host = host_copy(inp)
     ref = oracle_read(wl, host)
     errs = {}
-    for c in (nsv.CONSUMER_CUDA, nsv.CONSUMER_TENSOR):
+    for c in (nsv.CONSUMER_CUDA, form):
         out = gpu_read(wl, inp, plan=_plan(nsv, inp, consumer=c))
         assert status()[0] == 0
         errs[c] = assert_parity("bf16", gpu_out_f64(out), ref)
     # P rounded to bf16 costs the tensor path a little, never an order of magnitude
-    assert errs[nsv.CONSUMER_TENSOR] <= max(10 * errs[nsv.CONSUMER_CUDA], 1e-2)
+    assert errs[form] <= max(10 * errs[nsv.CONSUMER_CUDA], 1e-2)
 
 
 @pytest.mark.parametrize("heads,kv_heads,qlen", [(8, 2, 4), (4, 2, 4), (8, 2, 8)])  # 16, 8, 32
-def test_early_query_tokens_that_see_nothing(nsv, heads, kv_heads, qlen):
+def test_early_query_tokens_that_see_nothing(nsv, form, heads, kv_heads, qlen):
     """query_len n over rows shorter than n: query token j sees
     ctx - n + 1 + j positions, none when that is not positive (output 0)."""
     lens = [1, 2, 3, 4, 5, 0, 33]
     wl = _case(heads, kv_heads, qlen, 128, lens=lens, seed=13)
     inp = device_inputs(wl)
     host = host_copy(inp)
-    out = gpu_step(wl, inp, plan=_plan(nsv, inp, consumer=nsv.CONSUMER_TENSOR))
+    out = gpu_step(wl, inp, plan=_plan(nsv, inp, consumer=form))
     assert status()[0] == 0
     got = gpu_out_f64(out)
     ref = oracle_step(wl, host)
@@ -127,7 +133,7 @@ def test_early_query_tokens_that_see_nothing(nsv, heads, kv_heads, qlen):
 
 @pytest.mark.parametrize("heads,kv_heads,head_dim", [(16, 4, 128), (16, 2, 128), (8, 4, 64),
                                                      (32, 2, 128)])   # 8, 16, 4, 32 vectors
-def test_tensor_consumer_slot_gather(nsv, heads, kv_heads, head_dim):
+def test_tensor_consumer_slot_gather(nsv, form, heads, kv_heads, head_dim):
     """Tokens scattered one by one over the pool: the producer warp gathers
     them into the swizzled layout the MMA reads."""
     import torch
@@ -147,7 +153,7 @@ def test_tensor_consumer_slot_gather(nsv, heads, kv_heads, head_dim):
             table[r, b * 16:(b + 1) * 16] = base + np.arange(16)
     table = np.ascontiguousarray(table)
     out = torch.empty_like(inp["q"])
-    plan = _plan(nsv, inp, consumer=nsv.CONSUMER_TENSOR)
+    plan = _plan(nsv, inp, consumer=form)
     nsv.paged_decode_slots(inp["q"], inp["k_pool"], inp["v_pool"],
                            torch.from_numpy(table).cuda(), inp["context_lens"], wl.scale, out,
                            workspace=nsv.workspace_for(plan), plan=plan,
