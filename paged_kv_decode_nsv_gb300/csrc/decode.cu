@@ -61,8 +61,8 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 // Slack of the tensor consumer's lazily raised running max, in log2 units.
 constexpr float kRescaleSlack = 8.f;
 // Tensor-core consumer forms (the kernel's MMA template argument; 0: CUDA cores).
-constexpr int kMmaVectorRows = 1;  // query vectors as the MMA rows (M = 16)
-constexpr int kMmaTokenRows = 2;   // the block's tokens as the MMA rows, vectors as N = 8
+constexpr int kMmaVectorRows = kFormVectorRows;  // query vectors as the MMA rows (M = 16)
+constexpr int kMmaTokenRows = kFormTokenRows;    // the block's tokens as the MMA rows (M = 16)
 constexpr int kMmaCols = 8;        // query vectors per warp with tokens as rows
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -493,7 +493,7 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
     if (flags & kEnd) break;
     unsigned char* st = smem + s * L.stage_bytes;
     const uint32_t kbase = smem_u32(st), vbase_s = kbase + L.kv_bytes;
-    const int tmask = meta.y;
+    const int tmask = meta.y & 0xffff;
     const int qh0 = (flags >> 16) * G;
 
     if (flags & kFirst) {
@@ -502,7 +502,9 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
 #pragma unroll
       for (int nd = 0; nd < kNd; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
       if (flags & kHasQ) {
-        const unsigned char* qs = st + 2 * L.kv_bytes;
+        // q ring: after the S stages; this form has one slot
+        constexpr int qslot = 0;
+        const unsigned char* qs = smem + (size_t)S * L.stage_bytes;
 #pragma unroll
         for (int ks = 0; ks < kKs; ++ks) {
 #pragma unroll
@@ -513,6 +515,8 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
             qa[ks][2 + rh] = rok[rh] ? *reinterpret_cast<const uint32_t*>(row + 16) : 0u;
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8 * (2 * S + qslot));  // the q slot is free
       }
     }
 
@@ -726,7 +730,7 @@ __device__ __forceinline__ void consume_mma_t(const DecodeParams& p, unsigned ch
     if (flags & kEnd) break;
     unsigned char* st = smem + s * L.stage_bytes;
     const uint32_t kbase = smem_u32(st), vbase_s = kbase + L.kv_bytes;
-    const int tmask = meta.y;
+    const int tmask = meta.y & 0xffff;
     const int qh0 = (flags >> 16) * G;
 
     if (flags & kFirst) {
@@ -735,13 +739,19 @@ __device__ __forceinline__ void consume_mma_t(const DecodeParams& p, unsigned ch
 #pragma unroll
       for (int mt = 0; mt < kKs; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
       if (flags & kHasQ) {
+        // q ring: after the S stages, slots of the CTA's query vectors
+        const int qslot = meta.y >> 16;
         const unsigned char* row =
-            st + 2 * L.kv_bytes + ((size_t)(gjq * hq + gqh) * D + t4 * 2) * sizeof(T);
+            smem + (size_t)S * L.stage_bytes +
+            (size_t)qslot * align_up((uint32_t)nvec * D * sizeof(T), 128) +
+            ((size_t)(gjq * hq + gqh) * D + t4 * 2) * sizeof(T);
 #pragma unroll
         for (int ks = 0; ks < kKs; ++ks) {
           qb[ks][0] = gok ? *reinterpret_cast<const uint32_t*>(row + ks * 32) : 0u;
           qb[ks][1] = gok ? *reinterpret_cast<const uint32_t*>(row + ks * 32 + 16) : 0u;
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8 * (2 * S + qslot));  // the q slot is free
       }
     }
 
@@ -894,7 +904,7 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
                   : MMA == kMmaVectorRows ? HG * ((G * NQ + kMmaRows - 1) / kMmaRows)
                                           : nvec / QW;
   const int S = p.stages;
-  const SmemLayout L = make_layout((int)sizeof(T), D, HG, nvec, S, p.rows);
+  const SmemLayout L = make_layout((int)sizeof(T), D, HG, nvec, S, p.rows, MMA);
 
   int4* s_meta = reinterpret_cast<int4*>(smem + L.off_meta);
   const uint32_t bars = smem_u32(smem + L.off_bars);  // full[s] at +8s, empty[s] at +8(S+s)
@@ -910,6 +920,8 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
       mbar_init(bars + 8 * s, 1);              // full: the producer's arrive + tx bytes
       mbar_init(bars + 8 * (S + s), ncw);      // empty: one arrive per consumer warp
     }
+    for (int j = 0; j < (int)L.q_slots; ++j)
+      mbar_init(bars + 8 * (2 * S + j), ncw);  // qfree: every consumer warp has read it
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -958,7 +970,9 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
     const uint32_t half_bytes = (uint32_t)HG * kBlock * 128;  // swizzled 64-dim half
     const int slot0 = blockIdx.x * 2;
     unsigned long long walked = 0;
-    uint32_t n = 0;  // fills issued (meaningful in lane 0)
+    uint32_t n = 0;   // fills issued (meaningful in lane 0)
+    uint32_t qnext = 0;   // q slot of the next query load (lane 0)
+    uint32_t qphase = 0;  // laps of the q ring completed
     bool ok = true;
 
     // Unit u (this lane's): its row, its block within the row, its stage
@@ -997,15 +1011,23 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
         return mbar_wait(bars + 8 * (S + n % S), ((n / S) - 1) & 1);
       return true;
     };
+    // Wait (lane 0) until the next q slot is free: every consumer warp has
+    // read the query vectors loaded into it q_slots loads ago.
+    auto wait_q = [&]() -> bool {
+      if (qphase > 0) return mbar_wait(bars + 8 * (2 * S + qnext), (qphase - 1) & 1);
+      return true;
+    };
     // Publish the next stage (lane 0): write its metadata, arm its barrier
     // and start its copies (K/V unless the warp gathered them already, q on
-    // a segment's first stage).
+    // a segment's first stage, into the next q slot).
     auto publish = [&](int row, int flags, int phys, int mask) {
       const uint32_t s = n % S;
       const uint32_t full = bars + 8 * s;
       const int kv0 = flags >> 16;
       const int qh0 = kv0 * G;
-      s_meta[s] = make_int4(row, mask, slot0 + ((flags & kSlot1) ? 1 : 0), flags);
+      const uint32_t qslot = qnext;
+      s_meta[s] = make_int4(row, mask | (int)(qslot << 16), slot0 + ((flags & kSlot1) ? 1 : 0),
+                            flags);
       uint32_t bytes = 0;
       if ((flags & kData) && !(flags & kGathered)) bytes += 2 * L.kv_bytes;
       if (flags & kHasQ) bytes += L.q_bytes;
@@ -1030,15 +1052,23 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
           }
         }
         if (flags & kHasQ) {
+          const uint32_t qbase = smem_u32(smem + L.off_q + qslot * L.q_slot_bytes);
           for (int jq = 0; jq < NQ; ++jq)
-            bulk_g2s(base + 2 * L.kv_bytes + jq * q_slice,
-                     qp + (((size_t)row * NQ + jq) * p.heads + qh0) * D, q_slice, full, pol);
+            bulk_g2s(qbase + jq * q_slice, qp + (((size_t)row * NQ + jq) * p.heads + qh0) * D,
+                     q_slice, full, pol);
+        }
+      }
+      if (flags & kHasQ) {
+        if (++qnext == L.q_slots) {
+          qnext = 0;
+          ++qphase;
         }
       }
       ++n;
     };
     auto emit = [&](int row, int flags, int phys) -> bool {
       if (!wait_free()) return false;
+      if ((flags & kHasQ) && !wait_q()) return false;
       publish(row, flags, phys, 0xffff);
       return true;
     };
@@ -1049,7 +1079,7 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
     const long long pool_slots = p.pool_blocks * kBlock;
     auto gather = [&](int row, int blk, int flags) -> bool {
       bool ok2 = true;
-      if (lane == 0) ok2 = wait_free();
+      if (lane == 0) ok2 = wait_free() && (!(flags & kHasQ) || wait_q());
       ok2 = __shfl_sync(kFull, ok2, 0);
       if (!ok2) return false;
       const uint32_t s = __shfl_sync(kFull, n, 0) % S;
@@ -1197,10 +1227,11 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
     const int flags = meta.w;
     if (flags & kEnd) break;
     const unsigned char* st = smem + s * L.stage_bytes;
-    const int tmask = meta.y;              // tokens of the block that hold data
+    const int tmask = meta.y & 0xffff;     // tokens of the block that hold data
     const int qh0 = (flags >> 16) * G;     // the group's first query head
 
     if (flags & kFirst) {
+      const unsigned char* qs = smem + L.off_q + (meta.y >> 16) * L.q_slot_bytes;
 #pragma unroll
       for (int k = 0; k < QW; ++k) {
         m[k] = -INFINITY;
@@ -1209,12 +1240,15 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
         for (int e = 0; e < kDpl; ++e) acc[k][e] = 0.f;
         if (flags & kHasQ) {
           const uint4 raw = *reinterpret_cast<const uint4*>(
-              st + 2 * L.kv_bytes +
-              (((size_t)jq[k] * hq + qhl[k]) * D + sub * kDpl) * sizeof(T));
+              qs + (((size_t)jq[k] * hq + qhl[k]) * D + sub * kDpl) * sizeof(T));
           E::widen(raw, qv[k]);
 #pragma unroll
           for (int e = 0; e < kDpl; ++e) qv[k][e] *= p.qscale;
         }
+      }
+      if (flags & kHasQ) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8 * (2 * S + (meta.y >> 16)));  // the q slot is free
       }
     }
 

@@ -183,10 +183,11 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   const bool auto_stages = stages <= 0;
   if (auto_stages) stages = 3;
   if (stages < 2 || stages > 8) return NSV_ERR_RANGE;
-  SmemLayout L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout);
+  const int form = form_of(consumer);
+  SmemLayout L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout, form);
   while (auto_stages && L.total > (uint32_t)kSmemPerCta && stages > 2) {
     --stages;
-    L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout);
+    L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout, form);
   }
   if (L.total > (uint32_t)kSmemPerCta) return NSV_ERR_RANGE;
   const int threads = (hg * wpk + 1) * 32;
@@ -195,12 +196,13 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   // register count is fixed at compile time)
   const int fit_threads =
       std::min(kThreadsPerSm / threads, ctas_by_registers(threads, decode_regs(consumer, qw)));
-  if (tensor && auto_stages && cps <= 0 && fit < 2) {
+  if (tensor && auto_stages && cps <= 0 && std::min(fit, fit_threads) < 2) {
     // One CTA per SM either way: spend the rest of its shared memory on a
     // deeper ring (up to 6 stages), which keeps more bytes in flight for
     // the consumers that would otherwise wait on HBM latency.
     while (stages < 6) {
-      const SmemLayout L2 = make_layout(elem, s->head_dim, hg, nvec, stages + 1, rows_for_layout);
+      const SmemLayout L2 =
+          make_layout(elem, s->head_dim, hg, nvec, stages + 1, rows_for_layout, form);
       if (L2.total > (uint32_t)kSmemPerCta) break;
       ++stages;
       L = L2;

@@ -128,9 +128,12 @@ struct KvWriteParams {
 struct SmemLayout {
   uint32_t kv_bytes;     // one K (or V) tile set: heads_per_cta * block * D * elem
   uint32_t q_bytes;      // the CTA's query vectors
-  uint32_t stage_bytes;  // K + V + q, rounded to 128
+  uint32_t stage_bytes;  // K + V, rounded to 1024
+  uint32_t q_slots;      // ring of query-vector slots (one per segment in flight)
+  uint32_t q_slot_bytes; // q_bytes rounded to 128
+  uint32_t off_q;        // the q ring
   uint32_t off_meta;     // int4 per stage
-  uint32_t off_bars;     // full[stages], empty[stages] mbarriers
+  uint32_t off_bars;     // full[stages], empty[stages], qfree[q_slots] mbarriers
   uint32_t off_pbuf;     // per query vector: block-size floats
   uint32_t off_ctx;      // rows ints (validated context lengths)
   uint32_t off_prefix;   // rows + 1 ints (work-item prefix sums)
@@ -142,21 +145,45 @@ __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) {
   return (x + a - 1) / a * a;
 }
 
+// Consumer form of a decode-kernel variant (its MMA template argument).
+enum : int { kFormCuda = 0, kFormVectorRows = 1, kFormTokenRows = 2 };
+__host__ __device__ constexpr int form_of(int consumer) {
+  return consumer == kConsumerTensor            ? kFormTokenRows
+         : consumer == kConsumerTensorVectorRows ? kFormVectorRows
+                                                 : kFormCuda;
+}
+
+// Query-vector slots of the q ring: one per stage while the query vectors
+// of a head group are small (a slot is then never waited for: a segment's
+// slot is reused only after the stage that read it was released); one when
+// they are large, which leaves the shared memory to the K/V stages at the
+// price of a wait for segments shorter than the ring of stages.  The
+// vectors-as-rows form, whose query vectors are nearly always large, always
+// takes one slot (a fixed slot keeps its register allocation free of spills).
+__host__ __device__ inline int q_slots_for(uint32_t q_bytes, int stages, int form) {
+  return (form != kFormVectorRows && q_bytes <= 8192u) ? stages : 1;
+}
+
+// The CUDA-core consumer also keeps per-vector probability buffers (the
+// tensor-core forms hold probabilities in registers).
 __host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int heads_per_cta,
-                                                  int nvec, int stages, int rows) {
+                                                  int nvec, int stages, int rows, int form) {
   SmemLayout L;
   L.kv_bytes = (uint32_t)(heads_per_cta * kBlock * head_dim * elem);
   L.q_bytes = (uint32_t)(nvec * head_dim * elem);
   // Stages start on 1024-byte boundaries: 128-byte-swizzled TMA writes
   // need it (the kernel aligns the dynamic shared memory base itself).
-  L.stage_bytes = align_up(2 * L.kv_bytes + L.q_bytes, 1024);
-  uint32_t off = (uint32_t)stages * L.stage_bytes;
+  L.stage_bytes = align_up(2 * L.kv_bytes, 1024);
+  L.q_slots = (uint32_t)q_slots_for(L.q_bytes, stages, form);
+  L.q_slot_bytes = align_up(L.q_bytes, 128);
+  L.off_q = (uint32_t)stages * L.stage_bytes;
+  uint32_t off = L.off_q + L.q_slots * L.q_slot_bytes;
   L.off_meta = off;
   off += (uint32_t)stages * 16;
   L.off_bars = align_up(off, 8);
-  off = L.off_bars + (uint32_t)stages * 16;
+  off = L.off_bars + (uint32_t)(2 * stages + (int)L.q_slots) * 8;
   L.off_pbuf = align_up(off, 16);
-  off = L.off_pbuf + (uint32_t)(nvec * kBlock * 4);
+  off = L.off_pbuf + (form == kFormCuda ? (uint32_t)(nvec * kBlock * 4) : 0u);
   L.off_ctx = off;
   off += (uint32_t)rows * 4;
   L.off_prefix = off;
