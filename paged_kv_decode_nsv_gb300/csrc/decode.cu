@@ -904,7 +904,7 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
                   : MMA == kMmaVectorRows ? HG * ((G * NQ + kMmaRows - 1) / kMmaRows)
                                           : nvec / QW;
   const int S = p.stages;
-  const SmemLayout L = make_layout((int)sizeof(T), D, HG, nvec, S, p.rows, MMA);
+  const SmemLayout L = make_layout((int)sizeof(T), D, HG, nvec, S, p.rows, MMA, QW);
 
   int4* s_meta = reinterpret_cast<int4*>(smem + L.off_meta);
   const uint32_t bars = smem_u32(smem + L.off_bars);  // full[s] at +8s, empty[s] at +8(S+s)
@@ -1231,7 +1231,9 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
     const int qh0 = (flags >> 16) * G;     // the group's first query head
 
     if (flags & kFirst) {
-      const unsigned char* qs = smem + L.off_q + (meta.y >> 16) * L.q_slot_bytes;
+      // q ring slot of this segment (always slot 0 with 2 or 4 vectors per warp)
+      const int qslot = fixed_q_slot(kFormCuda, QW) ? 0 : (meta.y >> 16);
+      const unsigned char* qs = smem + L.off_q + qslot * L.q_slot_bytes;
 #pragma unroll
       for (int k = 0; k < QW; ++k) {
         m[k] = -INFINITY;
@@ -1248,7 +1250,7 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
       }
       if (flags & kHasQ) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(bars + 8 * (2 * S + (meta.y >> 16)));  // the q slot is free
+        if (lane == 0) mbar_arrive(bars + 8 * (2 * S + qslot));  // the q slot is free
       }
     }
 

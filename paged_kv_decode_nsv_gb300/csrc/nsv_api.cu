@@ -184,25 +184,26 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   if (auto_stages) stages = 3;
   if (stages < 2 || stages > 8) return NSV_ERR_RANGE;
   const int form = form_of(consumer);
-  SmemLayout L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout, form);
+  SmemLayout L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout, form, qw);
   while (auto_stages && L.total > (uint32_t)kSmemPerCta && stages > 2) {
     --stages;
-    L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout, form);
+    L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout, form, qw);
   }
   if (L.total > (uint32_t)kSmemPerCta) return NSV_ERR_RANGE;
   const int threads = (hg * wpk + 1) * 32;
   int fit = kSmemPerSm / (int)(L.total + kSmemReserved);
   // CTAs one SM holds by threads and by registers (each kernel variant's
   // register count is fixed at compile time)
-  const int fit_threads =
-      std::min(kThreadsPerSm / threads, ctas_by_registers(threads, decode_regs(consumer, qw)));
+  const int regs = decode_regs(consumer, qw);
+  const int fit_threads = std::min(kThreadsPerSm / threads, ctas_by_registers(threads, regs));
+  if (fit_threads < 1) return NSV_ERR_RANGE;  // one CTA would not fit the register file
   if (tensor && auto_stages && cps <= 0 && std::min(fit, fit_threads) < 2) {
     // One CTA per SM either way: spend the rest of its shared memory on a
     // deeper ring (up to 6 stages), which keeps more bytes in flight for
     // the consumers that would otherwise wait on HBM latency.
     while (stages < 6) {
       const SmemLayout L2 =
-          make_layout(elem, s->head_dim, hg, nvec, stages + 1, rows_for_layout, form);
+          make_layout(elem, s->head_dim, hg, nvec, stages + 1, rows_for_layout, form, qw);
       if (L2.total > (uint32_t)kSmemPerCta) break;
       ++stages;
       L = L2;

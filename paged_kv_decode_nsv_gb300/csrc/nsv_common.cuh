@@ -32,17 +32,20 @@ constexpr int kMaxThreadsMulti = (kMaxConsumerWarpsMulti + 1) * 32;
 
 // Registers per thread of each decode-kernel variant, fixed at compile time
 // (__maxnreg__) so that the planner can size the grid to the CTAs that are
-// really resident: CUDA-core consumer with 1 or 2 vectors per warp, and
-// every other variant (4 vectors per warp, both tensor-core forms).
+// really resident: CUDA-core consumer with 1 or 2 vectors per warp (96: a
+// 17-warp CTA fits, 5 warps of it per sub-partition, and two 9-warp CTAs
+// do), and every other variant (4 vectors per warp, both tensor-core forms,
+// at most 9 warps a CTA).
 constexpr int kRegsNarrow = 96;
 constexpr int kRegsWide = 168;
 __host__ __device__ constexpr int decode_regs(int consumer, int qw) {
   return (consumer == kConsumerCuda && qw <= 2) ? kRegsNarrow : kRegsWide;
 }
-// CTAs of `threads` threads at `regs` registers each that one SM's 64 K
-// registers hold (allocated per warp in units of 256).
+// CTAs of `threads` threads at `regs` registers each that one SM's
+// registers hold: 4 sub-partitions of 16 K registers, each holding whole
+// warps (allocated in units of 256 registers).
 __host__ __device__ constexpr int ctas_by_registers(int threads, int regs) {
-  return (65536 / (((regs * 32 + 255) / 256) * 256)) / ((threads + 31) / 32);
+  return 4 * (16384 / (((regs * 32 + 255) / 256) * 256)) / ((threads + 31) / 32);
 }
 // Largest batch the decode kernel's per-CTA row tables hold.
 constexpr int kMaxRows = 8192;
@@ -153,28 +156,36 @@ __host__ __device__ constexpr int form_of(int consumer) {
                                                  : kFormCuda;
 }
 
+// Whether a variant reads its query vectors from one fixed q slot: the
+// vectors-as-rows form (whose query vectors are nearly always large) and the
+// CUDA-core consumer with 2 or 4 vectors per warp.  A slot index known at
+// compile time keeps their register allocations free of spills.
+__host__ __device__ constexpr bool fixed_q_slot(int form, int qw) {
+  return form == kFormVectorRows || (form == kFormCuda && qw >= 2);
+}
+
 // Query-vector slots of the q ring: one per stage while the query vectors
 // of a head group are small (a slot is then never waited for: a segment's
 // slot is reused only after the stage that read it was released); one when
 // they are large, which leaves the shared memory to the K/V stages at the
-// price of a wait for segments shorter than the ring of stages.  The
-// vectors-as-rows form, whose query vectors are nearly always large, always
-// takes one slot (a fixed slot keeps its register allocation free of spills).
-__host__ __device__ inline int q_slots_for(uint32_t q_bytes, int stages, int form) {
-  return (form != kFormVectorRows && q_bytes <= 8192u) ? stages : 1;
+// price of a wait for segments shorter than the ring of stages, and one for
+// the variants that read a fixed slot.
+__host__ __device__ inline int q_slots_for(uint32_t q_bytes, int stages, int form, int qw) {
+  return (!fixed_q_slot(form, qw) && q_bytes <= 8192u) ? stages : 1;
 }
 
 // The CUDA-core consumer also keeps per-vector probability buffers (the
 // tensor-core forms hold probabilities in registers).
 __host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int heads_per_cta,
-                                                  int nvec, int stages, int rows, int form) {
+                                                  int nvec, int stages, int rows, int form,
+                                                  int qw) {
   SmemLayout L;
   L.kv_bytes = (uint32_t)(heads_per_cta * kBlock * head_dim * elem);
   L.q_bytes = (uint32_t)(nvec * head_dim * elem);
   // Stages start on 1024-byte boundaries: 128-byte-swizzled TMA writes
   // need it (the kernel aligns the dynamic shared memory base itself).
   L.stage_bytes = align_up(2 * L.kv_bytes, 1024);
-  L.q_slots = (uint32_t)q_slots_for(L.q_bytes, stages, form);
+  L.q_slots = (uint32_t)q_slots_for(L.q_bytes, stages, form, qw);
   L.q_slot_bytes = align_up(L.q_bytes, 128);
   L.off_q = (uint32_t)stages * L.stage_bytes;
   uint32_t off = L.off_q + L.q_slots * L.q_slot_bytes;

@@ -272,15 +272,16 @@ def test_bounded_wait_selftest_refuses_null_results(nsv):
 
 @pytest.mark.parametrize("kw,regs", [
     (dict(), 96), (dict(num_kv_heads=8), 168), (dict(num_kv_heads=8, query_len=8), 168),
-    (dict(num_kv_heads=8, dtype=0), 96),
+    (dict(num_kv_heads=8, dtype=0), 96),    # fp32 grouped: 2 vectors per warp
 ])
 def test_plan_fits_its_ctas_by_registers(nsv, kw, regs):
-    """A plan's CTAs per SM fit the SM's 64 K registers at the variant's
-    fixed register count (allocated per warp in units of 256)."""
+    """A plan's CTAs per SM fit the SM's registers at the variant's fixed
+    register count: 4 sub-partitions of 16 K registers, each holding whole
+    warps (allocated per warp in units of 256)."""
     p = nsv.plan_split(_shape(nsv, **kw), num_sms=152)
     warps = p.threads // 32
     per_warp = -(-regs * 32 // 256) * 256
-    assert p.ctas_per_sm * warps <= 65536 // per_warp
+    assert p.ctas_per_sm * warps <= 4 * (16384 // per_warp)
 
 
 def test_cuda_core_plan_with_17_warps_takes_one_cta_per_sm(nsv):
@@ -289,3 +290,32 @@ def test_cuda_core_plan_with_17_warps_takes_one_cta_per_sm(nsv):
     p = nsv.plan_custom(_shape(nsv, num_kv_heads=8, query_len=8), num_sms=152,
                         consumer=nsv.CONSUMER_CUDA)
     assert p.threads == 17 * 32 and p.ctas_per_sm == 1 and p.grid == 152
+
+
+def test_every_plan_round_trips(nsv):
+    """A plan the planner makes, handed back with all its choices fixed (as
+    nsv_paged_decode_ws checks a caller's plan), must come out identical:
+    no choice the heuristic takes may be one the explicit path refuses."""
+    base = dict(rows=256, max_blocks=512, num_blocks=70000)
+    checked = 0
+    for dtype in (nsv.F32, nsv.BF16):
+        for heads, kv, ql in [(32, 32, 1), (32, 8, 1), (32, 32, 4), (32, 8, 8), (128, 8, 1),
+                              (16, 16, 17), (8, 8, 3), (16, 1, 2), (8, 2, 16)]:
+            for d in (64, 128):
+                shape = nsv.make_shape(num_heads=heads, num_kv_heads=kv, query_len=ql,
+                                       dtype=dtype, head_dim=d, **base)
+                for extra in (dict(), dict(consumer=1), dict(consumer=2), dict(consumer=3),
+                              dict(consumer=1, vectors_per_warp=4), dict(kv_heads_per_cta=1),
+                              dict(kv_heads_per_cta=2, ctas_per_sm=2), dict(stages=2)):
+                    try:
+                        p = nsv.plan_custom(shape, num_sms=152, **extra)
+                    except nsv.NsvError:
+                        continue
+                    q = nsv.plan_custom(shape, num_sms=p.num_sms,
+                                        kv_heads_per_cta=p.kv_heads_per_cta, stages=p.stages,
+                                        ctas_per_sm=p.ctas_per_sm, grid=p.grid,
+                                        vectors_per_warp=p.vectors_per_warp,
+                                        consumer=p.consumer)
+                    assert bytes(q) == bytes(p), (heads, kv, ql, dtype, d, extra)
+                    checked += 1
+    assert checked > 150
