@@ -263,6 +263,9 @@ NSV_API int nsv_paged_decode_ws(const nsv_shape *shape, const nsv_plan *plan,
  * context_lens already count the appended token (its write slot is the
  * row's last real position).  plan/workspace as in nsv_paged_decode_ws;
  * workspace NULL with workspace_bytes 0 uses the library-owned workspace.
+ * Both halves' arguments are checked before either is launched: on an
+ * error return nothing was launched.  The append's launch also zeroes the
+ * read's arrival counters, so the step is two kernels and no memset.
  */
 NSV_API int nsv_decode_step(const nsv_shape *shape, const nsv_plan *plan, const void *q,
                             const void *k_new, const void *v_new,

@@ -8,7 +8,9 @@
 // contiguous head_dim run inside its (block, head) tile of the
 // [block][kv_head][token][dim] pool, so every write is a whole number of
 // 32-byte sectors.  A slot outside the pool array is skipped and flagged;
-// nothing here can write out of bounds.
+// nothing here can write out of bounds.  When the append and the read form
+// one step, the same launch also zeroes the read's arrival counters, which
+// saves the step a separate memset.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -20,6 +22,7 @@ namespace {
 
 __global__ void __launch_bounds__(256) kv_write_kernel(const KvWriteParams p) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < p.zero_count) p.zero_words[i] = 0;
   const long long per_row = (long long)p.kv_heads * p.vec_per_head;
   if (i >= (long long)p.rows * per_row) return;
   const int r = (int)(i / per_row);
@@ -43,7 +46,8 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const KvWriteParams p) {
 }  // namespace
 
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream) {
-  const long long n = (long long)p.rows * p.kv_heads * p.vec_per_head;
+  long long n = (long long)p.rows * p.kv_heads * p.vec_per_head;
+  if (p.zero_count > n) n = p.zero_count;
   if (n == 0) return cudaSuccess;
   const int threads = 256;
   const long long grid = (n + threads - 1) / threads;

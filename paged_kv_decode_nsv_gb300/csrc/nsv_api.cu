@@ -248,14 +248,44 @@ int check_plan(const nsv_shape* s, const nsv_plan* given, nsv_plan* use) {
   return NSV_OK;
 }
 
+// Checks the append's arguments and fills its launch parameters (no launch).
+int kv_write_prepare(const nsv_shape* s, const void* k_new, const void* v_new,
+                     const int64_t* write_slots, void* k_pool, void* v_pool, KvWriteParams* p) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (s->rows == 0) return NSV_OK;  // an empty batch: nothing to write
+  if (!k_new || !v_new || !write_slots || !k_pool || !v_pool) return NSV_ERR_NULLPTR;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      (reinterpret_cast<uintptr_t>(write_slots) & 7u))
+    return NSV_ERR_ALIGN;
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d)) != NSV_OK) return rc;
+  p->k_new = k_new;
+  p->v_new = v_new;
+  p->write_slots = write_slots;
+  p->k_pool = k_pool;
+  p->v_pool = v_pool;
+  p->status = d->status;
+  p->pool_slots = (s->num_blocks + 1) * (long long)s->block_size;
+  p->rows = s->rows * query_len(s);  // every new token of every row
+  p->kv_heads = s->num_kv_heads;
+  p->vec_per_head = s->head_dim * elem_bytes(s->dtype) / 16;
+  p->block_size = s->block_size;
+  p->zero_words = nullptr;
+  p->zero_count = 0;
+  return NSV_OK;
+}
+
 // The read through either addressing form: block_tables (slots null) or a
 // slot table `slots` with `slot_cols` readable columns per row and row
-// stride `slot_stride` (block_tables null).
+// stride `slot_stride` (block_tables null).  With `append` (the fused step)
+// the append is launched right before the read, after every check has
+// passed, and zeroes the read's arrival counters itself.
 int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, const void* k_pool,
                 const void* v_pool, const int32_t* block_tables, const int64_t* slots,
                 int64_t slot_cols, int64_t slot_stride, const int32_t* context_lens,
                 float scale, void* out, void* ws, size_t ws_bytes, bool library_ws,
-                cudaStream_t stream) {
+                cudaStream_t stream, KvWriteParams* append = nullptr) {
   int rc = check_shape(s);
   if (rc) return rc;
   if (s->rows == 0) return NSV_OK;  // an empty batch: nothing to read
@@ -303,8 +333,6 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   const WsLayout W = make_ws_layout(s->rows, s->num_kv_heads / plan.kv_heads_per_cta, plan.grid,
                                     nvec, s->head_dim);
   char* wsb = static_cast<char*>(ws);
-  // The arrival counters of cut rows start every call at zero.
-  if (cudaMemsetAsync(wsb, 0, W.cnt_bytes, stream) != cudaSuccess) return cuda_fail();
   DecodeParams p;
   p.q = q;
   p.k_pool = k_pool;
@@ -348,6 +376,15 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return NSV_ERR_CUDA;
     }
+  }
+  // The arrival counters of cut rows start every call at zero: zeroed by
+  // the step's append launch, or by a memset.
+  if (append) {
+    append->zero_words = reinterpret_cast<int32_t*>(wsb);
+    append->zero_count = (int)(W.cnt_bytes / 4);
+    if (launch_kv_write(*append, stream) != cudaSuccess) return cuda_fail();
+  } else if (cudaMemsetAsync(wsb, 0, W.cnt_bytes, stream) != cudaSuccess) {
+    return cuda_fail();
   }
   if (launch_decode(p, s->dtype, s->head_dim, plan.vectors_per_warp, plan.consumer, plan.grid,
                     plan.threads, plan.smem_bytes, stream) != cudaSuccess)
@@ -411,28 +448,10 @@ NSV_API int nsv_plan_resident_ctas(const nsv_shape* shape, const nsv_plan* plan,
 NSV_API int nsv_kv_write(const nsv_shape* s, const void* k_new, const void* v_new,
                          const int64_t* write_slots, void* k_pool, void* v_pool,
                          cudaStream_t stream) {
-  int rc = check_shape(s);
+  KvWriteParams p;
+  int rc = kv_write_prepare(s, k_new, v_new, write_slots, k_pool, v_pool, &p);
   if (rc) return rc;
   if (s->rows == 0) return NSV_OK;  // an empty batch: nothing to write
-  if (!k_new || !v_new || !write_slots || !k_pool || !v_pool) return NSV_ERR_NULLPTR;
-  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
-      (reinterpret_cast<uintptr_t>(write_slots) & 7u))
-    return NSV_ERR_ALIGN;
-  DeviceState* d = nullptr;
-  if ((rc = device_state(&d)) != NSV_OK) return rc;
-  if (s->rows == 0) return NSV_OK;
-  KvWriteParams p;
-  p.k_new = k_new;
-  p.v_new = v_new;
-  p.write_slots = write_slots;
-  p.k_pool = k_pool;
-  p.v_pool = v_pool;
-  p.status = d->status;
-  p.pool_slots = (s->num_blocks + 1) * (long long)s->block_size;
-  p.rows = s->rows * query_len(s);  // every new token of every row
-  p.kv_heads = s->num_kv_heads;
-  p.vec_per_head = s->head_dim * elem_bytes(s->dtype) / 16;
-  p.block_size = s->block_size;
   if (launch_kv_write(p, stream) != cudaSuccess) return cuda_fail();
   return NSV_OK;
 }
@@ -459,11 +478,14 @@ NSV_API int nsv_decode_step(const nsv_shape* shape, const nsv_plan* plan, const 
                             void* k_pool, void* v_pool, const int32_t* block_tables,
                             const int32_t* context_lens, float scale, void* out,
                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  int rc = nsv_kv_write(shape, k_new, v_new, write_slots, k_pool, v_pool, stream);
+  KvWriteParams append;
+  int rc = kv_write_prepare(shape, k_new, v_new, write_slots, k_pool, v_pool, &append);
   if (rc) return rc;
   const bool lib_ws = workspace == nullptr && workspace_bytes == 0;
+  // Checks both halves before launching either: the append and the read
+  // are launched back to back by decode_impl, or neither is.
   return decode_impl(shape, plan, q, k_pool, v_pool, block_tables, nullptr, 0, 0, context_lens,
-                     scale, out, workspace, workspace_bytes, lib_ws, stream);
+                     scale, out, workspace, workspace_bytes, lib_ws, stream, &append);
 }
 
 NSV_API int nsv_paged_decode_slots(const nsv_shape* shape, const nsv_plan* plan, const void* q,

@@ -125,6 +125,10 @@ struct KvWriteParams {
   long long pool_slots;  // (num_blocks + 1) * block_size
   int rows, kv_heads, vec_per_head;  // 16-byte vectors per (row, head)
   int block_size;
+  // Words set to zero on the way (the decode read's arrival counters when
+  // the append and the read form one step), or none.
+  int32_t* zero_words;
+  int zero_count;
 };
 
 // Shared-memory carve-up of one decode CTA.
