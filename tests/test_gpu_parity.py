@@ -345,6 +345,26 @@ def test_host_side_refusals(nsv):
     assert e.value.code == -4
 
 
+def test_refused_step_launches_nothing(nsv):
+    """nsv_decode_step checks the read's arguments before launching the
+    append: a step whose read is refused leaves the pool untouched."""
+    import torch
+    wl = _custom("step_refused", [40, 100], dtype="bf16", seed=29)
+    inp = device_inputs(wl)
+    k0, v0 = inp["k_pool"].clone(), inp["v_pool"].clone()
+    out = torch.empty_like(inp["q"])
+    odd = torch.empty(out.numel() * 2 + 8, dtype=torch.uint8, device="cuda")[8:]
+    odd = odd.view(torch.bfloat16).view(out.shape)          # misaligned output
+    with pytest.raises(nsv.NsvError) as e:
+        nsv.decode_step(inp["q"], inp["k_new"], inp["v_new"], inp["write_slots"],
+                        inp["k_pool"], inp["v_pool"], inp["block_tables"], inp["context_lens"],
+                        wl.scale, odd)
+    assert e.value.code == -4
+    torch.cuda.synchronize()
+    assert torch.equal(inp["k_pool"], k0) and torch.equal(inp["v_pool"], v0)
+    assert status()[0] == 0
+
+
 # ---------------------------------------------------------------------------
 # several query tokens per row (causal among themselves) and grouped heads:
 # a consumer warp serves up to 4 query vectors from one K/V tile
