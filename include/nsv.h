@@ -111,11 +111,13 @@ enum {
 };
 
 /* Sizes of one decode batch.  Limits: 0 <= rows <= 8192; num_heads a
- * multiple of num_kv_heads with num_heads/num_kv_heads <= 16; head_dim 64 or
- * 128; block_size 16; 1 <= max_blocks with max_blocks*block_size < 2^31;
- * 1 <= num_blocks < 2^31 - 1; query_len 0 or 1 (one query token per row) up
- * to 32 with query_len * num_heads/num_kv_heads <= 32, and, on the CUDA-core
- * consumer (fp32), <= 15 when that product is odd. */
+ * multiple of num_kv_heads; head_dim 64 or 128; block_size 16; 1 <=
+ * max_blocks with max_blocks*block_size < 2^31; 1 <= num_blocks < 2^31 - 1;
+ * query_len 0 or 1 (one query token per row) up to 64.  The query vectors
+ * per KV head, query_len * num_heads/num_kv_heads, are at most 64 for bf16
+ * (the tensor-core consumer) and at most 32 for fp32 (the CUDA-core
+ * consumer; at most 15 when odd); beyond, the planner refuses with
+ * NSV_ERR_SHAPE. */
 typedef struct nsv_shape {
     int32_t rows;
     int32_t num_heads;
@@ -159,7 +161,7 @@ typedef struct nsv_plan {
  *                       vectors_per_warp query vectors of one KV head.  Any
  *                       dtype and shape.
  *  NSV_CONSUMER_TENSOR: bf16 only.  A KV head's query vectors (query heads
- *                       of the group x query tokens, 2 to 32 of them) go
+ *                       of the group x query tokens, 2 to 64 of them) go
  *                       through 16x8x16 bf16 tensor-core MMAs with fp32
  *                       accumulation: scores against the block's keys, then
  *                       the weighted sum of its values, with the

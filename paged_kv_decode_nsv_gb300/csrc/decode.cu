@@ -32,7 +32,7 @@
 //    tile is reduced with a transposing butterfly (one shuffle per token
 //    instead of five), the tile max with a plain butterfly, probabilities go
 //    through shared memory to the lanes that own the value dims, and P.V
-//    accumulates in fp32.  On the tensor cores (bf16, 2 to 32 query vectors
+//    accumulates in fp32.  On the tensor cores (bf16, 2 to 64 query vectors
 //    per KV head) the same two contractions run as mma.sync.m16n8k16: with
 //    the block's 16 tokens as the MMA rows for up to 8 vectors, with the
 //    vectors as the rows (16 per warp) beyond.
@@ -419,10 +419,11 @@ __device__ __forceinline__ void finish_cut_row(const DecodeParams& p, int row, i
 
 // Tensor-core consumer (bf16) with the query vectors as the MMA rows: a KV
 // head's query vectors (the group's query heads of that KV head times the
-// query tokens, 9 to 32 of them) are the rows of mma.sync.m16n8k16 (bf16
-// inputs, fp32 accumulate), 16 rows per warp, so one or two warps per KV
-// head read the same K/V tile.  Each warp zeroes the tile's empty V rows
-// itself (both write the same zeros).  Per 16-token block: S = Q.K^T from the K tile staged by
+// query tokens, 2 to 64 of them, by default 9 and more) are the rows of
+// mma.sync.m16n8k16 (bf16 inputs, fp32 accumulate), 16 rows per warp, so
+// one to four warps per KV head read the same K/V tile.  Each warp zeroes
+// the tile's empty V rows itself (they all write the same zeros).  Per
+// 16-token block: S = Q.K^T from the K tile staged by
 // swizzled TMA loads and read with ldmatrix, the online softmax on the score
 // fragments, then O += P.V with P (bf16) taken straight from the score
 // fragments and V read with ldmatrix.trans.  Fragment layout of m16n8k16:
@@ -650,8 +651,8 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
 }
 
 // Tensor-core consumer with the block's 16 tokens as the MMA rows (bf16): a
-// KV head's query vectors (2 to 32) are the MMA columns, 8 per warp, so one
-// to four warps per KV head read the same K/V tile.  Each warp zeroes the
+// KV head's query vectors (2 to 64) are the MMA columns, 8 per warp, so one
+// to eight warps per KV head read the same K/V tile.  Each warp zeroes the
 // tile's empty V rows itself (they all write the same zeros).  Per block:
 // S^T = K.Q^T (M = 16 tokens, N = 8 vectors, K = head_dim), the online
 // softmax down the columns of S^T, then O^T += V^T.P^T (M = head_dim, N = 8

@@ -97,7 +97,6 @@ int check_shape(const nsv_shape* s) {
   if (s->rows < 0 || s->rows > kMaxRows) return NSV_ERR_SHAPE;
   if (s->num_heads < 1 || s->num_kv_heads < 1 || s->num_heads % s->num_kv_heads != 0)
     return NSV_ERR_SHAPE;
-  if (s->num_heads / s->num_kv_heads > kMaxConsumerWarps) return NSV_ERR_SHAPE;
   if ((s->num_heads / s->num_kv_heads) * (s->query_len > 0 ? s->query_len : 1) >
       kMaxVectorsPerKvHead)
     return NSV_ERR_SHAPE;

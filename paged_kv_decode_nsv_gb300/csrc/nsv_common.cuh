@@ -21,8 +21,9 @@ __host__ __device__ constexpr int max_consumer_warps(int qw) {
   return qw <= 2 ? kMaxConsumerWarps : kMaxConsumerWarpsMulti;
 }
 // Largest number of query vectors (query heads x query tokens) that share
-// one KV head.
-constexpr int kMaxVectorsPerKvHead = 32;
+// one KV head: 64 on the tensor cores (4 warps of 16 MMA rows), 32 on the
+// CUDA cores (16 warps of 2).
+constexpr int kMaxVectorsPerKvHead = 64;
 // Rows of the tensor-core MMA (m16n8k16): 16 query vectors per warp when the
 // vectors are the rows.
 constexpr int kMmaRows = 16;

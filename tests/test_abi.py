@@ -114,8 +114,9 @@ def test_plan_query_vectors(nsv, heads, kv_heads, qlen, qw, warps):
 
 
 @pytest.mark.parametrize("heads,kv_heads,qlen,dtype", [
-    (32, 8, 9, 1), (32, 32, 33, 1), (64, 4, 3, 1),   # more than 32 vectors per KV head
-    (32, 32, 17, 0),   # fp32 (CUDA cores): an odd count above 15 needs 17 warps
+    (32, 8, 17, 1), (128, 1, 1, 1), (64, 2, 3, 1),   # more than 64 vectors per KV head
+    (32, 8, 9, 0), (68, 2, 1, 0),     # fp32 (CUDA cores): more than 32
+    (32, 32, 17, 0),   # fp32: an odd count above 15 needs 17 warps
 ])
 def test_plan_refuses_too_many_query_vectors(nsv, heads, kv_heads, qlen, dtype):
     with pytest.raises(nsv.NsvError) as e:
@@ -205,7 +206,8 @@ def test_plan_custom_choices(nsv):
     (dict(head_dim=96), -10), (dict(head_dim=256), -10), (dict(dtype=7), -2),
     (dict(num_heads=30, num_kv_heads=8), -3), (dict(rows=-1), -3), (dict(rows=8193), -3),
     (dict(max_blocks=0), -3), (dict(num_blocks=0), -3),
-    (dict(num_heads=64, num_kv_heads=2), -3),
+    (dict(num_heads=130, num_kv_heads=2), -3),   # 65 query heads per KV head
+    (dict(query_len=65), -3),
 ])
 def test_shape_refusals(nsv, kw, code):
     with pytest.raises(nsv.NsvError) as e:
@@ -300,7 +302,8 @@ def test_every_plan_round_trips(nsv):
     checked = 0
     for dtype in (nsv.F32, nsv.BF16):
         for heads, kv, ql in [(32, 32, 1), (32, 8, 1), (32, 32, 4), (32, 8, 8), (128, 8, 1),
-                              (16, 16, 17), (8, 8, 3), (16, 1, 2), (8, 2, 16)]:
+                              (16, 16, 17), (8, 8, 3), (16, 1, 2), (8, 2, 16), (64, 8, 8),
+                              (64, 1, 1), (32, 32, 64)]:
             for d in (64, 128):
                 shape = nsv.make_shape(num_heads=heads, num_kv_heads=kv, query_len=ql,
                                        dtype=dtype, head_dim=d, **base)
@@ -319,3 +322,15 @@ def test_every_plan_round_trips(nsv):
                     assert bytes(q) == bytes(p), (heads, kv, ql, dtype, d, extra)
                     checked += 1
     assert checked > 150
+
+
+@pytest.mark.parametrize("heads,kv_heads,qlen", [(64, 8, 8), (64, 1, 1), (32, 32, 64),
+                                                 (32, 8, 10), (128, 2, 1)])
+def test_bf16_takes_up_to_64_vectors_per_kv_head(nsv, heads, kv_heads, qlen):
+    """Beyond 32 query vectors per KV head only the tensor cores serve the
+    read: vectors as the MMA rows, one warp per 16 of them."""
+    p = nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen),
+                       num_sms=152)
+    vpk = heads // kv_heads * qlen
+    assert vpk > 32 and p.consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS
+    assert p.threads == (p.kv_heads_per_cta * -(-vpk // 16) + 1) * 32

@@ -97,7 +97,7 @@ def _occupancy_shapes():
     base = dict(rows=256, head_dim=128, max_blocks=512, num_blocks=70000)
     for dt in (0, 1):
         for heads, kv, ql in [(32, 32, 1), (32, 8, 1), (32, 32, 4), (32, 8, 8), (128, 8, 1),
-                              (16, 16, 17), (8, 8, 3)]:
+                              (16, 16, 17), (8, 8, 3), (64, 8, 8), (64, 1, 1)]:
             for d in (64, 128):
                 yield dict(base, num_heads=heads, num_kv_heads=kv, query_len=ql, dtype=dt,
                            head_dim=d)

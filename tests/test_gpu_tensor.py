@@ -4,9 +4,10 @@ per row, both head dims, every plan shape the planner allows, the slot-table
 gather, and rows whose early query tokens see no position.
 
 Two forms: the block's tokens as the MMA rows and the query vectors as its
-columns, 8 per warp (NSV_CONSUMER_TENSOR, the default); or the vectors as
-the rows, 16 per warp (NSV_CONSUMER_TENSOR_VECTOR_ROWS).  Every test runs
-both."""
+columns, 8 per warp (NSV_CONSUMER_TENSOR, the default up to 8 vectors per
+KV head); or the vectors as the rows, 16 per warp
+(NSV_CONSUMER_TENSOR_VECTOR_ROWS, the default beyond).  Every test runs
+both, up to 64 vectors per KV head."""
 
 import numpy as np
 import pytest
@@ -58,6 +59,9 @@ def _plan(nsv, inp, **kw):
     (16, 4, 5, 64),     # 20
     (8, 8, 17, 128),    # 17: an odd count, the second warp runs one vector
     (16, 2, 3, 128),    # 24
+    (64, 8, 8, 128),    # 8 heads x 8 tokens = 64: four warps per KV head
+    (32, 4, 5, 64),     # 40
+    (64, 1, 1, 128),    # 64 query heads on one KV head
 ])
 def test_tensor_consumer_against_the_oracle(nsv, form, heads, kv_heads, qlen, head_dim):
     wl = _case(heads, kv_heads, qlen, head_dim)
@@ -112,7 +116,8 @@ def test_both_consumers_agree_with_the_oracle(nsv, form, qlen):
     assert errs[form] <= max(10 * errs[nsv.CONSUMER_CUDA], 1e-2)
 
 
-@pytest.mark.parametrize("heads,kv_heads,qlen", [(8, 2, 4), (4, 2, 4), (8, 2, 8)])  # 16, 8, 32
+@pytest.mark.parametrize("heads,kv_heads,qlen", [(8, 2, 4), (4, 2, 4), (8, 2, 8),
+                                                 (8, 2, 16)])  # 16, 8, 32, 64 vectors
 def test_early_query_tokens_that_see_nothing(nsv, form, heads, kv_heads, qlen):
     """query_len n over rows shorter than n: query token j sees
     ctx - n + 1 + j positions, none when that is not positive (output 0)."""
