@@ -142,6 +142,13 @@ __global__ void bounded_wait_probe(unsigned long long limit_ns, unsigned long lo
   result[0] = completed ? 0ull : 1ull;
 }
 
+// Programmatic dependent launch: wait until the grid this launch depends on
+// (the step's append) has completed and its writes are visible.  Returns at
+// once when the launch has no such dependency.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -1119,6 +1126,10 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
     long long w0 = beg;
     int c_row = 0, c_blk = 0, c_flags = 0, c_phys = -1;
     if (w0 + lane < end) unit_at(w0 + lane, c_row, c_blk, c_flags, c_phys);
+    // Everything so far read only the step's inputs (lengths, block tables
+    // or slots).  The pools and the arrival counters may still be being
+    // written by the step's append: wait for it before the first copy.
+    griddep_wait();
     while (w0 < end && ok) {
       // Prefetch the next window's units while this one is issued.
       const long long nw0 = w0 + 32;
@@ -1410,25 +1421,38 @@ cudaError_t set_attrs() {
   return cudaSuccess;
 }
 
+// One launch; `pdl` lets it start while the previous kernel on the stream
+// (the step's append) is still running (programmatic stream serialization;
+// the kernel waits for it before touching what it writes).
+cudaError_t launch_one(void (*kernel)(const DecodeParams), const DecodeParams& p, int grid,
+                       int threads, int smem, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 template <typename T, int D>
-void launch_typed(const DecodeParams& p, int qw, int consumer, int grid, int threads, int smem,
-                  cudaStream_t stream) {
+cudaError_t launch_typed(const DecodeParams& p, int qw, int consumer, int grid, int threads,
+                         int smem, cudaStream_t stream, bool pdl) {
   if constexpr (sizeof(T) == 2) {
-    if (consumer == kConsumerTensor) {
-      decode_kernel<T, D, 1, kMmaTokenRows><<<grid, threads, smem, stream>>>(p);
-      return;
-    }
-    if (consumer == kConsumerTensorVectorRows) {
-      decode_kernel<T, D, 1, kMmaVectorRows><<<grid, threads, smem, stream>>>(p);
-      return;
-    }
+    if (consumer == kConsumerTensor)
+      return launch_one(decode_kernel<T, D, 1, kMmaTokenRows>, p, grid, threads, smem, stream,
+                        pdl);
+    if (consumer == kConsumerTensorVectorRows)
+      return launch_one(decode_kernel<T, D, 1, kMmaVectorRows>, p, grid, threads, smem, stream,
+                        pdl);
   }
-  if (qw == 4)
-    decode_kernel<T, D, 4, 0><<<grid, threads, smem, stream>>>(p);
-  else if (qw == 2)
-    decode_kernel<T, D, 2, 0><<<grid, threads, smem, stream>>>(p);
-  else
-    decode_kernel<T, D, 1, 0><<<grid, threads, smem, stream>>>(p);
+  if (qw == 4) return launch_one(decode_kernel<T, D, 4, 0>, p, grid, threads, smem, stream, pdl);
+  if (qw == 2) return launch_one(decode_kernel<T, D, 2, 0>, p, grid, threads, smem, stream, pdl);
+  return launch_one(decode_kernel<T, D, 1, 0>, p, grid, threads, smem, stream, pdl);
 }
 
 template <typename T, int D>
@@ -1477,19 +1501,15 @@ cudaError_t prepare_decode_kernels() {
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int qw, int consumer,
-                          int grid, int threads, int smem, cudaStream_t stream) {
-  if (dtype == NSV_F32) {
-    if (head_dim == 64)
-      launch_typed<float, 64>(p, qw, consumer, grid, threads, smem, stream);
-    else
-      launch_typed<float, 128>(p, qw, consumer, grid, threads, smem, stream);
-  } else {
-    if (head_dim == 64)
-      launch_typed<__nv_bfloat16, 64>(p, qw, consumer, grid, threads, smem, stream);
-    else
-      launch_typed<__nv_bfloat16, 128>(p, qw, consumer, grid, threads, smem, stream);
-  }
-  return cudaGetLastError();
+                          int grid, int threads, int smem, cudaStream_t stream, bool pdl) {
+  if (dtype == NSV_F32)
+    return head_dim == 64
+               ? launch_typed<float, 64>(p, qw, consumer, grid, threads, smem, stream, pdl)
+               : launch_typed<float, 128>(p, qw, consumer, grid, threads, smem, stream, pdl);
+  return head_dim == 64
+             ? launch_typed<__nv_bfloat16, 64>(p, qw, consumer, grid, threads, smem, stream, pdl)
+             : launch_typed<__nv_bfloat16, 128>(p, qw, consumer, grid, threads, smem, stream,
+                                                pdl);
 }
 
 }  // namespace nsv

@@ -21,6 +21,9 @@ namespace nsv {
 namespace {
 
 __global__ void __launch_bounds__(256) kv_write_kernel(const KvWriteParams p) {
+  // The step's read may be scheduled now: it waits for this grid's writes
+  // itself (a no-op when nothing depends on this launch).
+  asm volatile("griddepcontrol.launch_dependents;");
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < p.zero_count) p.zero_words[i] = 0;
   const long long per_row = (long long)p.kv_heads * p.vec_per_head;

@@ -385,8 +385,10 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   } else if (cudaMemsetAsync(wsb, 0, W.cnt_bytes, stream) != cudaSuccess) {
     return cuda_fail();
   }
+  // In the fused step the read may start while the append runs: it reads
+  // only the step's inputs until the append has completed.
   if (launch_decode(p, s->dtype, s->head_dim, plan.vectors_per_warp, plan.consumer, plan.grid,
-                    plan.threads, plan.smem_bytes, stream) != cudaSuccess)
+                    plan.threads, plan.smem_bytes, stream, append != nullptr) != cudaSuccess)
     return cuda_fail();
   return NSV_OK;
 }

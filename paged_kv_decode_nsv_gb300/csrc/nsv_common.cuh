@@ -212,7 +212,7 @@ __host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int he
 
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int qw, int consumer,
-                          int grid, int threads, int smem, cudaStream_t stream);
+                          int grid, int threads, int smem, cudaStream_t stream, bool pdl);
 cudaError_t launch_kv_write(const KvWriteParams& p, cudaStream_t stream);
 // One-time per-device attribute set-up of the decode kernels.
 cudaError_t prepare_decode_kernels();
