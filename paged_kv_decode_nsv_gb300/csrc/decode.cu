@@ -398,15 +398,26 @@ __device__ __forceinline__ void finish_cut_row(const DecodeParams& p, int row, i
           Lsum = fmaf(w, ml.y, Lsum);
         }
       }
+      // Four pieces per step: their loads are independent, so a row cut into
+      // many pieces (a long row of a small batch) does not pay one L2
+      // round trip per piece.
       const int cnt = min(32, ns - base);
-      for (int kk = 0; kk < cnt; ++kk) {
-        const float wk = __shfl_sync(kFull, w, kk);
-        const int ik = __shfl_sync(kFull, idx, kk);
-        if (wk != 0.f) {
-          const float* src = p.ws_acc + (size_t)ik * D + lane * kPer;
+      for (int k0 = 0; k0 < cnt; k0 += 4) {
+        float wk[4], v[4][kPer];
 #pragma unroll
-          for (int e = 0; e < kPer; ++e) a[e] = fmaf(wk, __ldcg(src + e), a[e]);
+        for (int u = 0; u < 4; ++u) {
+          const int kk = (k0 + u) & 31;
+          wk[u] = __shfl_sync(kFull, w, kk);
+          const int ik = __shfl_sync(kFull, idx, kk);
+          if (k0 + u >= cnt) wk[u] = 0.f;
+          const float* src = p.ws_acc + (size_t)(wk[u] != 0.f ? ik : 0) * D + lane * kPer;
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) v[u][e] = wk[u] != 0.f ? __ldcg(src + e) : 0.f;
         }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) a[e] = fmaf(wk[u], v[u][e], a[e]);
       }
     }
 #pragma unroll
