@@ -172,9 +172,10 @@ typedef struct nsv_plan {
  *                       with a 128-byte swizzle.  Needs
  *                       (num_blocks+1)*num_kv_heads*16 < 2^31.
  *  NSV_CONSUMER_TENSOR_VECTOR_ROWS: the same with the query vectors as the
- *                       MMA rows, 16 per warp (one or two warps per KV head).
- * The default plan takes NSV_CONSUMER_TENSOR for bf16 shapes with 2 or more
- * query vectors per KV head, and the CUDA-core one otherwise. */
+ *                       MMA rows, 16 per warp (one to four warps per KV head).
+ * The default plan takes NSV_CONSUMER_TENSOR for bf16 shapes with 2 to 8
+ * query vectors per KV head, NSV_CONSUMER_TENSOR_VECTOR_ROWS for 9 to 64,
+ * and the CUDA-core one otherwise. */
 enum {
     NSV_CONSUMER_AUTO = 0,
     NSV_CONSUMER_CUDA = 1,
