@@ -144,7 +144,11 @@ typedef struct nsv_plan {
     int32_t stages;           /* shared-memory pipeline depth */
     int32_t ctas_per_sm;      /* resident CTAs per SM the grid is sized for */
     int32_t grid;             /* persistent CTAs launched */
-    int32_t threads;          /* threads per CTA */
+    int32_t threads;          /* threads per CTA: a producer warp and the
+                                 consumer warps; with the vectors as the MMA
+                                 rows at head_dim 128 also idle warps 4, 8,
+                                 ..., so that no consumer shares the
+                                 producer's SM sub-partition */
     int32_t smem_bytes;       /* dynamic shared memory per CTA */
     int32_t num_sms;          /* SM count the plan was made for */
     int32_t vectors_per_warp; /* query vectors (query heads x query tokens

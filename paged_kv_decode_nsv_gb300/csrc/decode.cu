@@ -894,7 +894,8 @@ __device__ __forceinline__ void consume_mma_t(const DecodeParams& p, unsigned ch
 }
 
 template <typename T, int D, int QW, int MMA>
-__global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
+__global__ void __launch_bounds__(consumers_off_producer(MMA, D) ? kMaxThreadsOffProducer
+                                  : MMA ? kMaxThreadsMulti
                                       : (QW <= 2 ? kMaxThreads : kMaxThreadsMulti))
     __maxnreg__(decode_regs(MMA == kMmaTokenRows    ? kConsumerTensor
                             : MMA == kMmaVectorRows ? kConsumerTensorVectorRows
@@ -1188,7 +1189,14 @@ __global__ void __launch_bounds__(MMA ? kMaxThreadsMulti
   }
 
   // -------------------------------------------------------------------- consumers
-  if constexpr (MMA == kMmaVectorRows) {
+  if constexpr (consumers_off_producer(MMA, D)) {
+    // Off the producer's sub-partition: warps 4, 8, ... idle; the others
+    // are consumers 1, 2, 3, 4 (warp 5), ... in order.
+    if ((warp & 3) == 0) return;
+    consume_mma<D>(p, smem, L, s_meta, bars, s_prefix, s_abort, N, U, nhg, nvec, ncw,
+                   warp - (warp >> 2), lane);
+    return;
+  } else if constexpr (MMA == kMmaVectorRows) {
     consume_mma<D>(p, smem, L, s_meta, bars, s_prefix, s_abort, N, U, nhg, nvec, ncw, warp, lane);
     return;
   } else if constexpr (MMA == kMmaTokenRows) {

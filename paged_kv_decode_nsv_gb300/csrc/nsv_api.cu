@@ -189,7 +189,7 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
     L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout, form, qw);
   }
   if (L.total > (uint32_t)kSmemPerCta) return NSV_ERR_RANGE;
-  const int threads = (hg * wpk + 1) * 32;
+  const int threads = cta_warps(form_of(consumer), s->head_dim, hg * wpk) * 32;
   int fit = kSmemPerSm / (int)(L.total + kSmemReserved);
   // CTAs one SM holds by threads and by registers (each kernel variant's
   // register count is fixed at compile time)

@@ -161,6 +161,25 @@ __host__ __device__ constexpr int form_of(int consumer) {
                                                  : kFormCuda;
 }
 
+// Whether a variant keeps its consumer warps off the producer's SM
+// sub-partition.  Warp w runs on sub-partition w % 4; in such a variant warps
+// 4, 8, ... are launched idle and return at once, and the consumers take the
+// other warps in order.  With the vectors as the MMA rows at head_dim 128,
+// consumer warps beside the producer measured about a quarter slower per
+// stage than the rest, and as every stage waits for its slowest consumer they
+// set the pace (20-64 vectors per KV head: 5-6 % faster without them); at
+// head_dim 64 and with the tokens as the rows the three-consumer
+// sub-partitions this leaves cost more than it saves.
+__host__ __device__ constexpr bool consumers_off_producer(int form, int head_dim) {
+  return form == kFormVectorRows && head_dim == 128;
+}
+// Warps of a decode CTA: the producer, the consumers and any idle warps.
+__host__ __device__ constexpr int cta_warps(int form, int head_dim, int consumer_warps) {
+  return consumers_off_producer(form, head_dim) ? consumer_warps + 1 + (consumer_warps - 1) / 3
+                                                : consumer_warps + 1;
+}
+constexpr int kMaxThreadsOffProducer = cta_warps(kFormVectorRows, 128, kMaxConsumerWarpsMulti) * 32;
+
 // Whether a variant reads its query vectors from one fixed q slot: the
 // vectors-as-rows form (whose query vectors are nearly always large) and the
 // CUDA-core consumer with 2 or 4 vectors per warp.  A slot index known at

@@ -56,6 +56,15 @@ def test_abi_version_and_strerror(nsv):
     assert "unknown" in nsv.strerror(-99)
 
 
+def _cta_warps(nsv, consumer, consumer_warps, head_dim=128):
+    """Warps of a planned CTA: the producer and the consumers, plus, with the
+    vectors as the MMA rows at head_dim 128, an idle warp at each multiple of
+    4 the consumers pass (none shares the producer's sub-partition)."""
+    if consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS and head_dim == 128:
+        return consumer_warps + 1 + (consumer_warps - 1) // 3
+    return consumer_warps + 1
+
+
 def _shape(nsv, **kw):
     d = dict(rows=256, num_heads=32, num_kv_heads=32, head_dim=128, max_blocks=512,
              num_blocks=70000, dtype=nsv.BF16, query_len=1)
@@ -92,7 +101,9 @@ def test_plan_shapes_of_every_workload(nsv):
         vpk = (wl.heads // wl.kv_heads) * wl.query_len
         if p.consumer != nsv.CONSUMER_CUDA:  # one warp per 8 or per 16 vectors of a KV head
             wpk = -(-vpk // (8 if p.consumer == nsv.CONSUMER_TENSOR else 16))
-            assert p.vectors_per_warp == 1 and p.threads // 32 - 1 == p.kv_heads_per_cta * wpk
+            assert p.vectors_per_warp == 1
+            assert p.threads // 32 == _cta_warps(nsv, p.consumer, p.kv_heads_per_cta * wpk,
+                                                 wl.head_dim)
         else:
             assert p.consumer == nsv.CONSUMER_CUDA
             assert (p.threads // 32 - 1) * p.vectors_per_warp == nvec
@@ -128,7 +139,7 @@ def test_plan_refuses_too_many_query_vectors(nsv, heads, kv_heads, qlen, dtype):
 def test_odd_vector_counts_above_15_run_on_the_tensor_cores(nsv):
     p = nsv.plan_split(_shape(nsv, query_len=17), num_sms=152)
     assert p.consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS
-    assert p.threads == (p.kv_heads_per_cta * 2 + 1) * 32
+    assert p.threads == _cta_warps(nsv, p.consumer, p.kv_heads_per_cta * 2) * 32
 
 
 @pytest.mark.parametrize("qlen,warps", [(2, 1), (16, 1), (17, 2), (32, 2)])
@@ -137,7 +148,7 @@ def test_plan_vector_rows_form(nsv, qlen, warps):
     p = nsv.plan_custom(_shape(nsv, query_len=qlen), num_sms=152,
                         consumer=nsv.CONSUMER_TENSOR_VECTOR_ROWS)
     assert p.consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS
-    assert p.threads == (p.kv_heads_per_cta * warps + 1) * 32
+    assert p.threads == _cta_warps(nsv, p.consumer, p.kv_heads_per_cta * warps) * 32
 
 
 @pytest.mark.parametrize("heads,kv_heads,qlen,dtype,consumer,hg,warps", [
@@ -157,7 +168,7 @@ def test_plan_consumer_choice(nsv, heads, kv_heads, qlen, dtype, consumer, hg, w
     p = nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen,
                               dtype=nsv.BF16 if dtype == "bf16" else nsv.F32), num_sms=152)
     assert p.consumer == consumer and p.kv_heads_per_cta == hg
-    assert p.threads == (warps + 1) * 32
+    assert p.threads == _cta_warps(nsv, consumer, warps) * 32
     if consumer != nsv.CONSUMER_CUDA:
         assert p.vectors_per_warp == 1
     assert p.reserved == 0
@@ -333,4 +344,4 @@ def test_bf16_takes_up_to_64_vectors_per_kv_head(nsv, heads, kv_heads, qlen):
                        num_sms=152)
     vpk = heads // kv_heads * qlen
     assert vpk > 32 and p.consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS
-    assert p.threads == (p.kv_heads_per_cta * -(-vpk // 16) + 1) * 32
+    assert p.threads == _cta_warps(nsv, p.consumer, p.kv_heads_per_cta * -(-vpk // 16)) * 32
