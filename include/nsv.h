@@ -177,6 +177,14 @@ typedef struct nsv_plan {
  *                       (num_blocks+1)*num_kv_heads*16 < 2^31.
  *  NSV_CONSUMER_TENSOR_VECTOR_ROWS: the same with the query vectors as the
  *                       MMA rows, 16 per warp (one to four warps per KV head).
+ *  NSV_CONSUMER_TENSOR_TMEM: bf16 only, on the 5th-generation tensor cores
+ *                       (tcgen05.mma with the accumulators in tensor
+ *                       memory).  The MMA's 128 rows are the query vectors
+ *                       of 4 KV heads (up to 32 vectors each) or 2 (up to
+ *                       64), padded with zero rows; so kv_heads_per_cta is
+ *                       4 or 2, and num_kv_heads must be a multiple of it.
+ *                       Four consumer warps, one thread per row; K/V tiles
+ *                       by 2-D TMA as above.
  * The default plan takes NSV_CONSUMER_TENSOR for bf16 shapes with 2 to 8
  * query vectors per KV head, NSV_CONSUMER_TENSOR_VECTOR_ROWS for 9 to 64,
  * and the CUDA-core one otherwise. */
@@ -184,7 +192,8 @@ enum {
     NSV_CONSUMER_AUTO = 0,
     NSV_CONSUMER_CUDA = 1,
     NSV_CONSUMER_TENSOR = 2,
-    NSV_CONSUMER_TENSOR_VECTOR_ROWS = 3
+    NSV_CONSUMER_TENSOR_VECTOR_ROWS = 3,
+    NSV_CONSUMER_TENSOR_TMEM = 4
 };
 
 /*

@@ -64,6 +64,7 @@ constexpr float kRescaleSlack = 8.f;
 constexpr int kMmaVectorRows = kFormVectorRows;  // query vectors as the MMA rows (M = 16)
 constexpr int kMmaTokenRows = kFormTokenRows;    // the block's tokens as the MMA rows (M = 16)
 constexpr int kMmaCols = 8;        // query vectors per warp with tokens as rows
+constexpr int kMmaTmem = kFormTmem;               // tcgen05.mma, accumulators in tensor memory
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -299,6 +300,99 @@ __device__ __forceinline__ int checked_ctx(const DecodeParams& p, int r) {
 // async-proxy (bulk copy) writes to the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+// Shared-memory matrix descriptor of a tcgen05.mma operand: start address,
+// leading- and stride-dimension byte offsets (16-byte units), the fixed
+// version field, and the swizzle mode.  For a K-major operand with the
+// 128-byte swizzle the stride offset is the step between 8-row groups (the
+// leading one is unused); for an MN-major one the stride offset steps 8 rows
+// of K and the leading one steps 64 elements of M or N; without swizzle
+// (8x16-byte core matrices) the leading offset steps K and the stride
+// offset steps 8 rows.
+constexpr uint32_t kUmmaSwizzleNone = 0, kUmmaSwizzle128 = 2;
+__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t swizzle) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)swizzle << 61);
+}
+// Instruction descriptor of a kind::f16 MMA: fp32 accumulator, bf16 A and B,
+// A K-major, B K-major or MN-major, N / 8 and M / 16.
+__device__ __forceinline__ uint32_t umma_idesc_bf16(int m, int n, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+// D (tensor memory) = A.B (+ D when `accumulate`), issued by one thread.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                          uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+// One arrive on `bar` once every MMA this thread issued so far is complete.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// 16 or 32 consecutive fp32 columns of this thread's TMEM lane (warp-wide).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Block id of a unit under slot-table addressing: the block's `nval` slots
@@ -668,6 +762,309 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
   }
 }
 
+// Tensor-core consumer (bf16) on the 5th-generation tensor cores: tcgen05.mma
+// from shared-memory operands into tensor-memory accumulators.  The MMA has
+// 128 rows: the group's KV heads take R = 32 or 64 rows each (their query
+// vectors, zero rows past them), so one MMA over the stage's tokens (16 per
+// head) gives every row its scores, and each row keeps only its own head's
+// 16 columns.  Four consumer warps, one per TMEM lane quadrant: thread r owns
+// row r (its softmax state in registers, no shuffles).  Per block:
+//   S = Q.K^T          (A: the query rows, 128-byte swizzle; B: the K tile as
+//                       staged by TMA, K-major), committed to a barrier;
+//   the online softmax of each row's 16 scores, read from tensor memory;
+//   P (bf16, zeros outside the row's head) to shared memory;
+//   O += P.V           (A: P, 8x16-byte core matrices; B: the V tile as
+//                       staged, MN-major), committed to the stage's empty
+//                       barrier, which hands the stage back to the producer.
+// The tensor core runs one thread's MMAs in order, so the scores' barrier
+// also covers the previous block's P.V: the lazily raised max may rescale O
+// (tcgen05.ld / st) and P may be rewritten as soon as the scores are in.
+template <int D>
+__device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned char* smem,
+                                             const SmemLayout& L, const int4* s_meta,
+                                             uint32_t bars, const int* s_prefix,
+                                             volatile int* s_abort, int N, long long U, int nhg,
+                                             int nvec, int warp, int lane, uint32_t tmem) {
+  using T = __nv_bfloat16;
+  constexpr int kNcw = kTmemWarps;
+  const int G = p.group, NQ = p.query_len, HG = p.heads_per_cta, S = p.stages;
+  const int vpk = G * NQ;
+  const int R = tmem_rows_per_head(vpk);    // rows per KV head; HG * R == 128
+  const int cw = warp - 1;
+  const int q4 = warp & 3;                  // the TMEM lane quadrant this warp reaches
+  const int r = q4 * 32 + lane;             // this thread's MMA row
+  const int kvl = r / R, v = r - kvl * R;   // its KV head within the group, its vector
+  const bool rok = v < vpk;
+  const int qhl = kvl * G + (rok ? v / NQ : 0);  // query head within the group
+  const int jq = rok ? v % NQ : 0;               // query token
+  const int hq = HG * G;
+  const int ntok = HG * kBlock;             // the scores MMA's N: every head's tokens
+  const int pch = ntok / 8;                 // 16-byte chunks of a P row
+  const uint32_t half_bytes = (uint32_t)HG * kBlock * 128;
+  volatile int* s_merge = s_abort + 1;
+  const uint32_t sbar = bars + 8 * (2 * S + (int)L.q_slots);  // scores ready
+  const uint32_t obar = sbar + 8;                             // a piece's O ready
+  unsigned char* const qa = smem + L.off_pbuf;                // Q: 128 x D, swizzled
+  unsigned char* const pb = qa + kTmemRows * D * 2;           // P: 128 x ntok
+  const uint32_t qa_s = smem_u32(qa), pb_s = smem_u32(pb);
+  const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+  const uint32_t t_o = tmem + lane_base;                       // O: columns [0, D)
+  const uint32_t t_s = tmem + lane_base + (uint32_t)(D + kvl * kBlock);  // this row's scores
+  const bool issuer = cw == 0 && lane == 0;
+  const uint32_t idesc_s = umma_idesc_bf16(kTmemRows, ntok, false);
+  const uint32_t idesc_o = umma_idesc_bf16(kTmemRows, D, true);
+
+  // Empty rows see nothing: zeros for all their (token, head) vectors.
+  constexpr int kChunks = D * 2 / 16;
+  for (int rr = blockIdx.x; rr < p.rows; rr += gridDim.x) {
+    if (s_prefix[rr + 1] != s_prefix[rr]) continue;
+    for (int vh = cw; vh < NQ * p.heads; vh += kNcw)
+      for (int c = lane; c < kChunks; c += 32)
+        reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)rr * NQ * p.heads + vh) * D)[c] =
+            make_uint4(0u, 0u, 0u, 0u);
+  }
+
+  // P rows hold zeros outside their own head's two 16-byte chunks, for good
+  for (int kc = 0; kc < pch; ++kc)
+    *reinterpret_cast<uint4*>(pb + (r >> 3) * (pch * 128) + kc * 128 + (r & 7) * 16) =
+        make_uint4(0u, 0u, 0u, 0u);
+  unsigned char* const prow = pb + (r >> 3) * (pch * 128) + (2 * kvl) * 128 + (r & 7) * 16;
+  // Descriptors are linear in the start address (16-byte units in the low
+  // bits), so each MMA's is a base plus an offset.
+  const uint64_t dq0 = umma_desc(qa_s, 16, 1024, kUmmaSwizzle128);
+  const uint64_t dk0 = umma_desc(0u, 16, 1024, kUmmaSwizzle128);
+  const uint64_t dp0 = umma_desc(pb_s, 128, (uint32_t)pch * 128, kUmmaSwizzleNone);
+  const uint64_t dv0 = umma_desc(0u, half_bytes, 1024, kUmmaSwizzle128);
+  const uint32_t stage0 = smem_u32(smem);
+
+  float m = -INFINITY, l = 0.f;
+  bool fresh = true;  // no P.V issued yet in this piece: O holds nothing of it
+  uint32_t nqk = 0, nout = 0;
+  bool failed = false;
+  uint32_t s = 0, ph = 0;  // stage and its phase parity
+  for (;; s = (s + 1 == (uint32_t)S) ? (ph ^= 1u, 0u) : s + 1) {
+    if (!mbar_wait(bars + 8 * s, ph)) {
+      failed = true;
+      break;
+    }
+    const int4 meta = s_meta[s];
+    const int flags = meta.w;
+    if (flags & kEnd) break;
+    unsigned char* st = smem + s * L.stage_bytes;
+    const uint32_t st_s = stage0 + s * L.stage_bytes;
+    const int tmask = meta.y & 0xffff;
+    const int qh0 = (flags >> 16) * G;
+
+    bool new_q = false;
+    if (flags & kFirst) {
+      m = -INFINITY;
+      l = 0.f;
+      fresh = true;
+      if (flags & kHasQ) {
+        // q ring slot 0 (this form's only one) -> this row of the Q operand:
+        // 16-byte chunk c of a 64-dim half at chunk c ^ (row & 7)
+        const unsigned char* src =
+            smem + (size_t)S * L.stage_bytes + (size_t)(jq * hq + qhl) * D * sizeof(T);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 val = rok ? *reinterpret_cast<const uint4*>(src + c * 16)
+                                : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(qa + (c >> 3) * (kTmemRows * 128) + r * 128 +
+                                    (((c & 7) ^ (r & 7)) * 16)) = val;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8 * (2 * S));  // the q slot is free
+        new_q = true;
+      }
+    }
+
+    if (flags & kData) {
+      const int rem = flags & 0xff;
+      const int nvalid = min(kBlock, rem);
+      // new query rows must be in place before the scores MMA reads them
+      if (new_q) consumer_sync(kNcw * 32);
+      if (issuer) {
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          // 16 dims: 64-dim half ks / 4, 32 bytes into its 128-byte rows
+          const uint32_t qoff = (uint32_t)(ks >> 2) * (kTmemRows * 128) + (uint32_t)(ks & 3) * 32;
+          const uint32_t koff = st_s + (uint32_t)(ks >> 2) * half_bytes + (uint32_t)(ks & 3) * 32;
+          umma_bf16(tmem + D, dq0 + (qoff >> 4), dk0 + (koff >> 4), idesc_s, ks > 0);
+        }
+        umma_commit(sbar);
+      }
+      // V rows that hold no data become zeros (P is 0 there, but 0 * NaN is
+      // not); the tensor core reads V only after the barrier below.
+      if (nvalid < kBlock || tmask != 0xffff) {
+        for (int c = cw * 32 + lane; c < ntok * kChunks; c += kNcw * 32) {
+          const int tr = c / kChunks, dc = c - tr * kChunks;
+          const int t = tr % kBlock;
+          if (!(t < nvalid && ((tmask >> t) & 1)))
+            *reinterpret_cast<uint4*>(st + L.kv_bytes + swz(tr, dc, half_bytes)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      if (!mbar_wait(sbar, nqk & 1)) {
+        failed = true;
+        break;
+      }
+      ++nqk;
+      tc_fence_after();
+      uint32_t sr[16];
+      tmem_ld16(t_s, sr);
+      tmem_wait_ld();
+      // online softmax of this row's 16 scores; the running max is raised
+      // lazily (by more than kRescaleSlack), as in the other tensor forms.
+      // A block every query token sees in full needs no masks.
+      const bool dense = nvalid == kBlock && tmask == 0xffff && rem - (NQ - 1) >= kBlock;
+      float x[16];
+#pragma unroll
+      for (int t = 0; t < kBlock; ++t) x[t] = __uint_as_float(sr[t]) * p.qscale;
+      if (!dense || !rok) {
+        const int nv = rem - (NQ - 1 - jq);  // positions this row's query sees
+#pragma unroll
+        for (int t = 0; t < kBlock; ++t)
+          if (!(rok && t < nv && ((tmask >> t) & 1))) x[t] = -INFINITY;
+      }
+      float mx;
+      {
+        float a8[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) a8[t] = fmaxf(x[t], x[t + 8]);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) a8[t] = fmaxf(a8[t], a8[t + 4]);
+        mx = fmaxf(fmaxf(a8[0], a8[2]), fmaxf(a8[1], a8[3]));
+      }
+      float alpha = 1.f;
+      const bool raise = mx > m + kRescaleSlack;  // also the first finite max (m = -inf)
+      if (raise) {
+        alpha = exp2f(m - mx);
+        m = mx;
+        l *= alpha;
+      }
+      if (!fresh && __any_sync(kFull, raise)) {
+        // O holds earlier blocks of the piece (their P.V is complete):
+        // rescale the warp's rows (1 where this row's max did not move)
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + (uint32_t)c0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+          tmem_st32(t_o + (uint32_t)c0, o);
+        }
+        tmem_wait_st();
+      }
+      // probabilities (none while the row has seen no position: m = -inf)
+      uint32_t pk[8];
+      {
+        float pv[16];
+        const bool live = m != -INFINITY;
+#pragma unroll
+        for (int t = 0; t < kBlock; ++t) pv[t] = live ? exp2f(x[t] - m) : 0.f;
+        float s8[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) s8[t] = pv[t] + pv[t + 8];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) s8[t] += s8[t + 4];
+        l += (s8[0] + s8[2]) + (s8[1] + s8[3]);
+#pragma unroll
+        for (int t2 = 0; t2 < 8; ++t2) pk[t2] = pack_bf16(pv[2 * t2], pv[2 * t2 + 1]);
+      }
+      // this row's head's two 8-token chunks of P (the rest stays zero)
+      *reinterpret_cast<uint4*>(prow) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<uint4*>(prow + 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      consumer_sync(kNcw * 32);  // P, zeroed V rows and any rescaled O are in place
+      if (issuer) {
+        tc_fence_after();
+        const uint32_t vb = st_s + L.kv_bytes;
+        for (int k = 0; k < HG; ++k) {  // one MMA of K = 16 tokens per head
+          umma_bf16(tmem, dp0 + (uint32_t)(k * 16), dv0 + ((vb + (uint32_t)k * (kBlock * 128)) >> 4),
+                    idesc_o, !fresh || k > 0);
+        }
+        umma_commit(bars + 8 * (S + s));  // the stage is free once P.V has read it
+      }
+      fresh = false;
+    } else {
+      // no data: hand the stage back once every thread has read its metadata
+      consumer_sync(kNcw * 32);
+      if (issuer) mbar_arrive(bars + 8 * (S + s));
+    }
+
+    if (flags & kLast) {
+      const int row = meta.x;
+      if (issuer) umma_commit(obar);
+      if (!mbar_wait(obar, nout & 1)) {
+        failed = true;
+        break;
+      }
+      ++nout;
+      tc_fence_after();
+      if (flags & kFinal) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        T* out = static_cast<T*>(p.out) + (((size_t)row * NQ + jq) * p.heads + qh0 + qhl) * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          if (!fresh) {
+            tmem_ld32(t_o + (uint32_t)c0, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = 0u;
+          }
+          if (rok) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8)
+              *reinterpret_cast<uint4*>(out + c0 + j) = make_uint4(
+                  pack_bf16(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv),
+                  pack_bf16(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv),
+                  pack_bf16(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv),
+                  pack_bf16(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv));
+          }
+        }
+      } else {
+        const size_t slot = (size_t)meta.z * nvec + (size_t)(kvl * vpk + v);
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          if (!fresh) {
+            tmem_ld32(t_o + (uint32_t)c0, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = 0u;
+          }
+          if (rok) {
+            float* a = p.ws_acc + slot * D + c0;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(a + j) =
+                  make_float4(__uint_as_float(o[j]), __uint_as_float(o[j + 1]),
+                              __uint_as_float(o[j + 2]), __uint_as_float(o[j + 3]));
+          }
+        }
+        if (rok) p.ws_ml[slot] = make_float2(m, l);
+        // this warp's rows are vectors [vw, vw + 32) of one KV head
+        const int vw = q4 * 32 - kvl * R;
+        const int nvw = max(0, min(32, vpk - vw));
+        finish_cut_row<T, D>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, kvl * vpk + vw,
+                             nvw, kNcw, cw, lane, s_merge);
+      }
+      tc_fence_before();
+    }
+  }
+  if (failed) {
+    if (lane == 0) atomicOr(p.status, (uint32_t)NSV_DEV_TIMEOUT);
+    *s_abort = 1;
+  }
+}
+
 // Tensor-core consumer with the block's 16 tokens as the MMA rows (bf16): a
 // KV head's query vectors (2 to 64) are the MMA columns, 8 per warp, so one
 // to eight warps per KV head read the same K/V tile.  Each warp zeroes the
@@ -894,11 +1291,13 @@ __device__ __forceinline__ void consume_mma_t(const DecodeParams& p, unsigned ch
 }
 
 template <typename T, int D, int QW, int MMA>
-__global__ void __launch_bounds__(consumers_off_producer(MMA, D) ? kMaxThreadsOffProducer
+__global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 1) * 32
+                                  : consumers_off_producer(MMA, D) ? kMaxThreadsOffProducer
                                   : MMA ? kMaxThreadsMulti
                                       : (QW <= 2 ? kMaxThreads : kMaxThreadsMulti))
     __maxnreg__(decode_regs(MMA == kMmaTokenRows    ? kConsumerTensor
                             : MMA == kMmaVectorRows ? kConsumerTensorVectorRows
+                            : MMA == kMmaTmem       ? kConsumerTensorTmem
                                                     : kConsumerCuda, QW))
     decode_kernel(const __grid_constant__ DecodeParams p) {
   using E = Elem<T>;
@@ -922,6 +1321,7 @@ __global__ void __launch_bounds__(consumers_off_producer(MMA, D) ? kMaxThreadsOf
   // one per 16 (vectors as MMA rows); QW vectors per warp on the CUDA cores
   const int ncw = MMA == kMmaTokenRows    ? HG * ((G * NQ + kMmaCols - 1) / kMmaCols)
                   : MMA == kMmaVectorRows ? HG * ((G * NQ + kMmaRows - 1) / kMmaRows)
+                  : MMA == kMmaTmem       ? kTmemWarps
                                           : nvec / QW;
   const int S = p.stages;
   const SmemLayout L = make_layout((int)sizeof(T), D, HG, nvec, S, p.rows, MMA, QW);
@@ -935,16 +1335,26 @@ __global__ void __launch_bounds__(consumers_off_producer(MMA, D) ? kMaxThreadsOf
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  // the TMEM form's tensor-memory columns and their base address
+  const uint32_t tmem_ncols = MMA == kMmaTmem ? (uint32_t)tmem_cols(D, G * NQ) : 0u;
+  uint32_t* const s_tmem = reinterpret_cast<uint32_t*>(smem + L.off_flag + 8);
+
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(bars + 8 * s, 1);              // full: the producer's arrive + tx bytes
-      mbar_init(bars + 8 * (S + s), ncw);      // empty: one arrive per consumer warp
+      mbar_init(bars + 8 * s, 1);  // full: the producer's arrive + tx bytes
+      // empty: one arrive per consumer warp (the TMEM form: one commit of
+      // the MMAs that read the stage)
+      mbar_init(bars + 8 * (S + s), MMA == kMmaTmem ? 1 : ncw);
     }
     for (int j = 0; j < (int)L.q_slots; ++j)
       mbar_init(bars + 8 * (2 * S + j), ncw);  // qfree: every consumer warp has read it
+    if (MMA == kMmaTmem)
+      for (int j = 0; j < 3; ++j)  // scores ready, a piece's O ready, all MMAs drained
+        mbar_init(bars + 8 * (2 * S + (int)L.q_slots + j), 1);
     *s_abort = 0;
     fence_mbar_init();
   }
+  if (MMA == kMmaTmem && warp == 1) tmem_alloc(smem_u32(s_tmem), tmem_ncols);
   // Row table: validated lengths and block counts (prefix computed below).
   for (int r = tid; r < p.rows; r += blockDim.x) {
     const int c = checked_ctx(p, r);
@@ -970,7 +1380,9 @@ __global__ void __launch_bounds__(consumers_off_producer(MMA, D) ? kMaxThreadsOf
     }
     if (lane == 0) s_prefix[0] = 0;
   }
+  if (MMA == kMmaTmem) tc_fence_before();
   __syncthreads();
+  if (MMA == kMmaTmem) tc_fence_after();
 
   const int nhg = p.kv_heads / HG;
   const int N = s_prefix[p.rows];                 // blocks per head group
@@ -1189,6 +1601,25 @@ __global__ void __launch_bounds__(consumers_off_producer(MMA, D) ? kMaxThreadsOf
   }
 
   // -------------------------------------------------------------------- consumers
+  if constexpr (MMA == kMmaTmem) {
+    if (warp > kTmemWarps) return;
+    const uint32_t tmem = *s_tmem;
+    consume_tmem<D>(p, smem, L, s_meta, bars, s_prefix, s_abort, N, U, nhg, nvec, warp, lane,
+                    tmem);
+    // Free the tensor memory once every consumer is done with it and the
+    // tensor core has finished every MMA (bounded wait on a last commit).
+    tc_fence_before();
+    consumer_sync(kTmemWarps * 32);
+    tc_fence_after();
+    if (warp == 1) {
+      const uint32_t fbar = bars + 8 * (2 * S + (int)L.q_slots + 2);
+      if (lane == 0) umma_commit(fbar);
+      (void)mbar_wait(fbar, 0);
+      tc_fence_after();
+      tmem_dealloc(tmem, tmem_ncols);
+    }
+    return;
+  }
   if constexpr (consumers_off_producer(MMA, D)) {
     // Off the producer's sub-partition: warps 4, 8, ... idle; the others
     // are consumers 1, 2, 3, 4 (warp 5), ... in order.
@@ -1435,6 +1866,7 @@ cudaError_t set_attrs() {
   if ((e = set_attr<T, D, 4, 0>()) != cudaSuccess) return e;
   if constexpr (sizeof(T) == 2) {
     if ((e = set_attr<T, D, 1, kMmaVectorRows>()) != cudaSuccess) return e;
+    if ((e = set_attr<T, D, 1, kMmaTmem>()) != cudaSuccess) return e;
     return set_attr<T, D, 1, kMmaTokenRows>();
   }
   return cudaSuccess;
@@ -1468,6 +1900,8 @@ cudaError_t launch_typed(const DecodeParams& p, int qw, int consumer, int grid, 
     if (consumer == kConsumerTensorVectorRows)
       return launch_one(decode_kernel<T, D, 1, kMmaVectorRows>, p, grid, threads, smem, stream,
                         pdl);
+    if (consumer == kConsumerTensorTmem)
+      return launch_one(decode_kernel<T, D, 1, kMmaTmem>, p, grid, threads, smem, stream, pdl);
   }
   if (qw == 4) return launch_one(decode_kernel<T, D, 4, 0>, p, grid, threads, smem, stream, pdl);
   if (qw == 2) return launch_one(decode_kernel<T, D, 2, 0>, p, grid, threads, smem, stream, pdl);
@@ -1482,6 +1916,8 @@ cudaError_t occupancy_typed(int qw, int consumer, int threads, int smem, int* ct
       fn = reinterpret_cast<const void*>(decode_kernel<T, D, 1, kMmaTokenRows>);
     else if (consumer == kConsumerTensorVectorRows)
       fn = reinterpret_cast<const void*>(decode_kernel<T, D, 1, kMmaVectorRows>);
+    else if (consumer == kConsumerTensorTmem)
+      fn = reinterpret_cast<const void*>(decode_kernel<T, D, 1, kMmaTmem>);
     else
       fn = qw == 4   ? reinterpret_cast<const void*>(decode_kernel<T, D, 4, 0>)
            : qw == 2 ? reinterpret_cast<const void*>(decode_kernel<T, D, 2, 0>)

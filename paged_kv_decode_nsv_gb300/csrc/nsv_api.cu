@@ -138,7 +138,8 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
     consumer = !(tensor_ok && qw <= 0) ? kConsumerCuda
                : vpk <= 8              ? kConsumerTensor
                                        : kConsumerTensorVectorRows;
-  } else if (consumer == kConsumerTensor || consumer == kConsumerTensorVectorRows) {
+  } else if (consumer == kConsumerTensor || consumer == kConsumerTensorVectorRows ||
+             consumer == kConsumerTensorTmem) {
     if (!tensor_ok || qw > 1) return NSV_ERR_RANGE;
   } else if (consumer != kConsumerCuda) {
     return NSV_ERR_RANGE;
@@ -163,7 +164,14 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
                                                           : vpk / qw;
   const int max_warps = tensor ? kMaxConsumerWarpsMulti : max_consumer_warps(qw);
   const int tile = kBlock * s->head_dim * elem;
-  if (hg <= 0) {
+  const bool tmem_form = consumer == kConsumerTensorTmem;
+  if (tmem_form) {
+    // one 128-row MMA group per CTA: 4 KV heads of up to 32 vectors, or 2
+    // of up to 64
+    const int gh = tmem_heads(vpk);
+    if (s->num_kv_heads % gh != 0 || (hg > 0 && hg != gh)) return NSV_ERR_RANGE;
+    hg = gh;
+  } else if (hg <= 0) {
     // Largest KV-head group whose K+V stage stays within 64 KiB and whose
     // query vectors fill at most 8 consumer warps: big bulk copies, few CTAs.
     hg = 1;
@@ -189,12 +197,30 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
     L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout, form, qw);
   }
   if (L.total > (uint32_t)kSmemPerCta) return NSV_ERR_RANGE;
-  const int threads = cta_warps(form_of(consumer), s->head_dim, hg * wpk) * 32;
+  const int threads =
+      (tmem_form ? kTmemWarps + 1 : cta_warps(form_of(consumer), s->head_dim, hg * wpk)) * 32;
   int fit = kSmemPerSm / (int)(L.total + kSmemReserved);
   // CTAs one SM holds by threads and by registers (each kernel variant's
   // register count is fixed at compile time)
   const int regs = decode_regs(consumer, qw);
-  const int fit_threads = std::min(kThreadsPerSm / threads, ctas_by_registers(threads, regs));
+  int fit_threads = std::min(kThreadsPerSm / threads, ctas_by_registers(threads, regs));
+  // The TMEM form's CTAs also share the SM's 512 tensor-memory columns.
+  // (The device's occupancy calculator answers one CTA per SM for a kernel
+  // that allocates tensor memory, however few columns it takes; two CTAs of
+  // 256 columns do run side by side: the 64-vector read takes 929 us with two
+  // per SM against 1540 us with one, on GB300.)
+  if (tmem_form) fit_threads = std::min(fit_threads, 512 / tmem_cols(s->head_dim, vpk));
+  if (tmem_form && auto_stages && cps <= 0 && fit < 2 && fit_threads >= 2 && stages > 2) {
+    // Two CTAs with a 2-stage ring each beat one CTA with a deep one: each
+    // CTA's stage is a chain of dependent steps (MMA, softmax, MMA) that the
+    // other CTA's chain overlaps.
+    const SmemLayout L2 = make_layout(elem, s->head_dim, hg, nvec, 2, rows_for_layout, form, qw);
+    if (kSmemPerSm / (int)(L2.total + kSmemReserved) >= 2) {
+      stages = 2;
+      L = L2;
+      fit = kSmemPerSm / (int)(L.total + kSmemReserved);
+    }
+  }
   if (fit_threads < 1) return NSV_ERR_RANGE;  // one CTA would not fit the register file
   if (tensor && auto_stages && cps <= 0 && std::min(fit, fit_threads) < 2) {
     // One CTA per SM either way: spend the rest of its shared memory on a
@@ -359,7 +385,7 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   p.qscale = scale * 1.4426950408889634f;  // log2(e): the kernels use exp2
   memset(&p.tmap_k, 0, sizeof(p.tmap_k));
   memset(&p.tmap_v, 0, sizeof(p.tmap_v));
-  if (plan.consumer == kConsumerTensor || plan.consumer == kConsumerTensorVectorRows) {
+  if (plan.consumer != kConsumerCuda) {
     // The pools as [(num_blocks+1)*kv_heads*16 rows][head_dim] bf16; a box is
     // 64 dims (128 bytes, the swizzle span) by the head group's 16-token tiles.
     const cuuint64_t dims[2] = {(cuuint64_t)s->head_dim,

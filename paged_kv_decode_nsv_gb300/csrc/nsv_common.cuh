@@ -27,7 +27,12 @@ constexpr int kMaxVectorsPerKvHead = 64;
 // Rows of the tensor-core MMA (m16n8k16): 16 query vectors per warp when the
 // vectors are the rows.
 constexpr int kMmaRows = 16;
-enum : int { kConsumerCuda = 1, kConsumerTensor = 2, kConsumerTensorVectorRows = 3 };
+enum : int {
+  kConsumerCuda = 1,
+  kConsumerTensor = 2,
+  kConsumerTensorVectorRows = 3,
+  kConsumerTensorTmem = 4
+};
 constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
 constexpr int kMaxThreadsMulti = (kMaxConsumerWarpsMulti + 1) * 32;
 
@@ -39,8 +44,11 @@ constexpr int kMaxThreadsMulti = (kMaxConsumerWarpsMulti + 1) * 32;
 // at most 9 warps a CTA).
 constexpr int kRegsNarrow = 96;
 constexpr int kRegsWide = 168;
+constexpr int kRegsTmem = 168;
 __host__ __device__ constexpr int decode_regs(int consumer, int qw) {
-  return (consumer == kConsumerCuda && qw <= 2) ? kRegsNarrow : kRegsWide;
+  return consumer == kConsumerTensorTmem                ? kRegsTmem
+         : (consumer == kConsumerCuda && qw <= 2) ? kRegsNarrow
+                                                  : kRegsWide;
 }
 // CTAs of `threads` threads at `regs` registers each that one SM's
 // registers hold: 4 sub-partitions of 16 K registers, each holding whole
@@ -154,11 +162,30 @@ __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) {
 }
 
 // Consumer form of a decode-kernel variant (its MMA template argument).
-enum : int { kFormCuda = 0, kFormVectorRows = 1, kFormTokenRows = 2 };
+enum : int { kFormCuda = 0, kFormVectorRows = 1, kFormTokenRows = 2, kFormTmem = 3 };
 __host__ __device__ constexpr int form_of(int consumer) {
   return consumer == kConsumerTensor            ? kFormTokenRows
          : consumer == kConsumerTensorVectorRows ? kFormVectorRows
+         : consumer == kConsumerTensorTmem       ? kFormTmem
                                                  : kFormCuda;
+}
+
+// The TMEM form (tcgen05.mma, accumulators in tensor memory).  Its MMA has
+// 128 rows: each KV head of the group takes R = 32 or 64 of them (its query
+// vectors, the rest zero), so a group is 4 or 2 KV heads, and one MMA over
+// the group's tokens serves them all (each row uses its own head's 16
+// columns).  Four consumer warps, one per TMEM lane quadrant; a thread owns
+// one row.
+constexpr int kTmemWarps = 4;
+constexpr int kTmemRows = 128;
+__host__ __device__ constexpr int tmem_rows_per_head(int vpk) { return vpk <= 32 ? 32 : 64; }
+__host__ __device__ constexpr int tmem_heads(int vpk) { return kTmemRows / tmem_rows_per_head(vpk); }
+// Tensor-memory columns a CTA allocates (a power of two, at least 32): the
+// output accumulator (head_dim columns) and the scores (16 per KV head).
+__host__ __device__ constexpr int tmem_cols(int head_dim, int vpk) {
+  return head_dim + tmem_heads(vpk) * kBlock <= 128 ? 128
+         : head_dim + tmem_heads(vpk) * kBlock <= 256 ? 256
+                                                     : 512;
 }
 
 // Whether a variant keeps its consumer warps off the producer's SM
@@ -185,7 +212,7 @@ constexpr int kMaxThreadsOffProducer = cta_warps(kFormVectorRows, 128, kMaxConsu
 // CUDA-core consumer with 2 or 4 vectors per warp.  A slot index known at
 // compile time keeps their register allocations free of spills.
 __host__ __device__ constexpr bool fixed_q_slot(int form, int qw) {
-  return form == kFormVectorRows || (form == kFormCuda && qw >= 2);
+  return form == kFormVectorRows || form == kFormTmem || (form == kFormCuda && qw >= 2);
 }
 
 // Query-vector slots of the q ring: one per stage while the query vectors
@@ -216,15 +243,25 @@ __host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int he
   L.off_meta = off;
   off += (uint32_t)stages * 16;
   L.off_bars = align_up(off, 8);
-  off = L.off_bars + (uint32_t)(2 * stages + (int)L.q_slots) * 8;
-  L.off_pbuf = align_up(off, 16);
-  off = L.off_pbuf + (form == kFormCuda ? (uint32_t)(nvec * kBlock * 4) : 0u);
+  // mbarriers: full[stages], empty[stages], qfree[q_slots]; the TMEM form
+  // adds three (scores ready, output ready, drained)
+  off = L.off_bars + (uint32_t)(2 * stages + (int)L.q_slots + (form == kFormTmem ? 3 : 0)) * 8;
+  if (form == kFormTmem) {
+    // its MMA operands: the query rows (128 x head_dim, 128-byte swizzle,
+    // 1024-byte aligned) and the probabilities (128 x the group's tokens)
+    L.off_pbuf = align_up(off, 1024);
+    off = L.off_pbuf + (uint32_t)(kTmemRows * head_dim * 2) +
+          (uint32_t)(kTmemRows * heads_per_cta * kBlock * 2);
+  } else {
+    L.off_pbuf = align_up(off, 16);
+    off = L.off_pbuf + (form == kFormCuda ? (uint32_t)(nvec * kBlock * 4) : 0u);
+  }
   L.off_ctx = off;
   off += (uint32_t)rows * 4;
   L.off_prefix = off;
   off += (uint32_t)(rows + 1) * 4;
   L.off_flag = align_up(off, 4);
-  off = L.off_flag + 8;
+  off = L.off_flag + 16;  // abort flag, merge flag, tensor-memory address
   L.total = align_up(off, 128) + 1024;  // + slack to align the base to 1024
   return L;
 }

@@ -32,7 +32,8 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 ABI_VERSION = 101  # the layout of Shape and Plan below
 F32, BF16 = 0, 1
-CONSUMER_AUTO, CONSUMER_CUDA, CONSUMER_TENSOR, CONSUMER_TENSOR_VECTOR_ROWS = 0, 1, 2, 3
+(CONSUMER_AUTO, CONSUMER_CUDA, CONSUMER_TENSOR, CONSUMER_TENSOR_VECTOR_ROWS,
+ CONSUMER_TENSOR_TMEM) = 0, 1, 2, 3, 4
 DEV_BAD_CTX, DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_TIMEOUT = 1, 2, 4, 8
 ERRORS = {0: "NSV_OK", -1: "NSV_ERR_NULLPTR", -2: "NSV_ERR_DTYPE", -3: "NSV_ERR_SHAPE",
           -4: "NSV_ERR_ALIGN", -5: "NSV_ERR_RANGE", -6: "NSV_ERR_CAPTURE", -7: "NSV_ERR_CUDA",

@@ -142,6 +142,23 @@ def test_odd_vector_counts_above_15_run_on_the_tensor_cores(nsv):
     assert p.threads == _cta_warps(nsv, p.consumer, p.kv_heads_per_cta * 2) * 32
 
 
+@pytest.mark.parametrize("heads,kv_heads,qlen,head_dim,group,cps", [
+    (32, 8, 8, 128, 4, 1), (64, 8, 8, 128, 2, 2), (32, 8, 1, 128, 4, 1), (32, 8, 9, 128, 2, 2),
+    (8, 8, 17, 128, 4, 1), (32, 8, 8, 64, 4, 2), (64, 8, 8, 64, 2, 2)])
+def test_plan_tmem_form(nsv, heads, kv_heads, qlen, head_dim, group, cps):
+    """NSV_CONSUMER_TENSOR_TMEM: one 128-row MMA group per CTA (4 KV heads of
+    up to 32 vectors, 2 of up to 64), a producer and four consumer warps; two
+    CTAs per SM (each with a 2-stage ring) where their shared memory fits, as
+    their 256 (head_dim 128) or 128 tensor-memory columns do."""
+    p = nsv.plan_custom(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen,
+                               head_dim=head_dim),
+                        num_sms=152, consumer=nsv.CONSUMER_TENSOR_TMEM)
+    assert p.consumer == nsv.CONSUMER_TENSOR_TMEM and p.kv_heads_per_cta == group
+    assert p.threads == 5 * 32 and p.vectors_per_warp == 1
+    assert p.ctas_per_sm == cps and p.grid == 152 * cps
+    assert cps == 1 or 2 * (p.smem_bytes + 1024) <= 228 * 1024
+
+
 @pytest.mark.parametrize("qlen,warps", [(2, 1), (16, 1), (17, 2), (32, 2)])
 def test_plan_vector_rows_form(nsv, qlen, warps):
     """NSV_CONSUMER_TENSOR_VECTOR_ROWS: one warp per 16 vectors of a KV head."""
@@ -178,7 +195,10 @@ def test_plan_consumer_choice(nsv, heads, kv_heads, qlen, dtype, consumer, hg, w
     (dict(num_kv_heads=32), dict(consumer=2)),                      # 1 vector per KV head
     (dict(num_kv_heads=8, dtype=1), dict(consumer=2, vectors_per_warp=2)),
     (dict(num_kv_heads=8, dtype=0), dict(consumer=2)),              # fp32
-    (dict(num_kv_heads=8), dict(consumer=4)),
+    (dict(num_kv_heads=8), dict(consumer=5)),                       # no such consumer
+    (dict(num_kv_heads=8, dtype=0), dict(consumer=4)),              # fp32
+    (dict(num_heads=24, num_kv_heads=6), dict(consumer=4)),         # 4-head groups do not divide 6
+    (dict(num_kv_heads=8), dict(consumer=4, kv_heads_per_cta=8)),   # its group is 4 heads
     (dict(num_kv_heads=8, dtype=0), dict(consumer=3)),              # fp32
     (dict(num_kv_heads=8, num_blocks=(1 << 24)), dict(consumer=2)), # TMA row index overflows
 ])

@@ -24,10 +24,11 @@ def _batches(heads, kv_heads):
     return base, a, b
 
 
-@pytest.mark.parametrize("heads,kv_heads,consumer", [(8, 8, 1), (16, 4, 2)])
+@pytest.mark.parametrize("heads,kv_heads,consumer", [(8, 8, 1), (16, 4, 2), (16, 4, 4)])
 def test_graph_recorded_on_padding_replays_real_steps(heads, kv_heads, consumer):
-    """Both consumers; the tensor-core one holds its TMA tensor maps (over the
-    pool, which the graph's replays keep) in the captured launch."""
+    """The CUDA-core and tensor-core consumers, and the TMEM form; the tensor
+    forms hold their TMA tensor maps (over the pool, which the graph's replays
+    keep) in the captured launch."""
     import torch
     from paged_kv_decode_nsv_gb300 import nsv
     base, wa, wb = _batches(heads, kv_heads)
@@ -44,7 +45,8 @@ def test_graph_recorded_on_padding_replays_real_steps(heads, kv_heads, consumer)
     ctx = torch.zeros((R,), dtype=torch.int32, device=dev)                # all padding
     out = torch.full((R, H, D), 3.0, dtype=torch.bfloat16, device=dev)
     shape = nsv.shape_of(q, kp, tables)
-    plan = nsv.plan_split(shape)
+    # the default plan for the first two; the TMEM form is chosen explicitly
+    plan = nsv.plan_split(shape) if consumer < 4 else nsv.plan_custom(shape, consumer=consumer)
     assert plan.consumer == consumer
     ws = nsv.workspace_for(plan)
     scale = wa.scale
