@@ -111,6 +111,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Whether the phase of `bar` with the given parity has completed, without
+// waiting.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `bar` with the given parity to complete; false if
 // it has not after limit_ns.  The first try is inline (the common case: the
 // phase is already complete); the bounded loop is out of line.
@@ -324,20 +338,34 @@ __device__ __forceinline__ uint32_t umma_idesc_bf16(int m, int n, bool b_mn_majo
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
-// D (tensor memory) = A.B (+ D when `accumulate`), issued by one thread.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b,
-                                          uint32_t idesc, bool accumulate) {
+// D (tensor memory) = A.B (+ D when `accumulate`): one MMA, executed by a
+// whole warp (uniform control flow, so the descriptors can stay
+// warp-uniform) with only the `lead` lane issuing.
+__device__ __forceinline__ void umma_bf16_warp(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                               uint32_t idesc, bool accumulate, bool lead) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %4, 0;\n\tsetp.ne.u32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u), "r"(lead ? 1u : 0u)
       : "memory");
 }
-// One arrive on `bar` once every MMA this thread issued so far is complete.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+// One arrive on `bar` once every MMA the `lead` lane issued so far is
+// complete (executed by the whole warp).
+__device__ __forceinline__ void umma_commit_warp(uint32_t bar, bool lead) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar),
+      "r"(lead ? 1u : 0u)
+      : "memory");
+}
+// 2^x by the special-function unit (ex2.approx: relative error about
+// 2^-22, +0 for -inf), for the TMEM form's probabilities, which are rounded
+// to bf16 right after.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -762,23 +790,150 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
   }
 }
 
-// Tensor-core consumer (bf16) on the 5th-generation tensor cores: tcgen05.mma
-// from shared-memory operands into tensor-memory accumulators.  The MMA has
-// 128 rows: the group's KV heads take R = 32 or 64 rows each (their query
+// The TMEM form (bf16) on the 5th-generation tensor cores: tcgen05.mma from
+// shared-memory operands into tensor-memory accumulators.  The MMA has 128
+// rows: the group's KV heads take R = 32 or 64 rows each (their query
 // vectors, zero rows past them), so one MMA over the stage's tokens (16 per
 // head) gives every row its scores, and each row keeps only its own head's
-// 16 columns.  Four consumer warps, one per TMEM lane quadrant: thread r owns
-// row r (its softmax state in registers, no shuffles).  Per block:
-//   S = Q.K^T          (A: the query rows, 128-byte swizzle; B: the K tile as
-//                       staged by TMA, K-major), committed to a barrier;
-//   the online softmax of each row's 16 scores, read from tensor memory;
-//   P (bf16, zeros outside the row's head) to shared memory;
-//   O += P.V           (A: P, 8x16-byte core matrices; B: the V tile as
-//                       staged, MN-major), committed to the stage's empty
-//                       barrier, which hands the stage back to the producer.
-// The tensor core runs one thread's MMAs in order, so the scores' barrier
-// also covers the previous block's P.V: the lazily raised max may rescale O
-// (tcgen05.ld / st) and P may be rewritten as soon as the scores are in.
+// 16 columns.  Roles:
+//   * an MMA warp (one lane issues) runs S = Q.K^T for stage n + 1 while the
+//     softmax warps work on stage n (two score buffers in tensor memory, two
+//     probability buffers in shared memory), then O += P.V for stage n once
+//     they hand P over, committed to the stage's empty barrier;
+//   * four softmax warps, one per TMEM lane quadrant: thread r owns row r
+//     (its online-softmax state in registers), reads its head's 16 scores
+//     with tcgen05.ld and writes its probabilities (bf16) into P.
+// Operands: Q (128 x D, 128-byte swizzle, K-major) copied from the q ring by
+// the softmax warps; K as staged by TMA (K-major); P in 8x16-byte core
+// matrices (zeros outside the row's head); V as staged (MN-major).
+// Barriers beyond the ring's: scores ready [2], probabilities handed over
+// [2], a piece's O complete, every MMA drained, query rows ready, a P.V
+// complete.
+struct TmemBars {
+  uint32_t base;
+  __device__ uint32_t scores(uint32_t b) const { return base + 8 * b; }
+  __device__ uint32_t handed(uint32_t b) const { return base + 16 + 8 * b; }
+  __device__ uint32_t out() const { return base + 32; }
+  __device__ uint32_t drained() const { return base + 40; }
+  __device__ uint32_t qready() const { return base + 48; }
+  __device__ uint32_t pv() const { return base + 56; }
+};
+constexpr int kTmemBars = 8;
+
+// The MMA warp.  The d-th stage with data has its scores in buffer d & 1,
+// stage n's probabilities are in buffer n & 1; every barrier completes once
+// per use and never runs more than one phase ahead of a wait on it, so
+// parity waits suffice.
+template <int D>
+__device__ __forceinline__ bool tmem_mma_warp(const DecodeParams& p, unsigned char* smem,
+                                              const SmemLayout& L, const int4* s_meta,
+                                              uint32_t bars, uint32_t tmem, int lane) {
+  const int HG = p.heads_per_cta, S = p.stages;
+  const int ntok = HG * kBlock;
+  const int pch = ntok / 8;
+  const uint32_t half_bytes = (uint32_t)HG * kBlock * 128;
+  const TmemBars tb{bars + 8 * (2 * S + (int)L.q_slots)};
+  const bool lead = lane == 0;
+  const uint32_t stage0 = smem_u32(smem);
+  const uint32_t qa_s = smem_u32(smem + L.off_pbuf);
+  const uint32_t pb_s = qa_s + (uint32_t)(kTmemRows * D * 2);
+  const uint32_t pbuf_bytes = (uint32_t)(kTmemRows * ntok * 2);
+  // descriptors are linear in the start address: a base plus an offset
+  const uint64_t dq0 = umma_desc(qa_s, 16, 1024, kUmmaSwizzle128);
+  const uint64_t dk0 = umma_desc(0u, 16, 1024, kUmmaSwizzle128);
+  const uint64_t dp0 = umma_desc(pb_s, 128, (uint32_t)pch * 128, kUmmaSwizzleNone);
+  const uint64_t dv0 = umma_desc(0u, half_bytes, 1024, kUmmaSwizzle128);
+  const uint32_t idesc_s = umma_idesc_bf16(kTmemRows, ntok, false);
+  const uint32_t idesc_o = umma_idesc_bf16(kTmemRows, D, true);
+
+  uint32_t nd = 0;  // stages with data whose scores were issued
+  auto issue_scores = [&](uint32_t stage) {
+    tc_fence_after();
+    const uint32_t st_s = stage0 + stage * L.stage_bytes;
+    const uint32_t sb = tmem + (uint32_t)(D + (int)(nd & 1) * ntok);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      // 16 dims: 64-dim half ks / 4, 32 bytes into its 128-byte rows
+      const uint32_t qoff = (uint32_t)(ks >> 2) * (kTmemRows * 128) + (uint32_t)(ks & 3) * 32;
+      const uint32_t koff = st_s + (uint32_t)(ks >> 2) * half_bytes + (uint32_t)(ks & 3) * 32;
+      umma_bf16_warp(sb, dq0 + (qoff >> 4), dk0 + (koff >> 4), idesc_s, ks > 0, lead);
+    }
+    umma_commit_warp(tb.scores(nd & 1), lead);
+    ++nd;
+  };
+
+  uint32_t nq = 0;  // query-row hand-overs waited for
+  bool fresh = true;
+  // stage 0
+  if (!mbar_wait(bars, 0)) return false;
+  int4 meta = s_meta[0];
+  // every stage that brings query rows has them handed over (even one with
+  // no data), so the hand-over barrier's phases match the waits
+  if (!(meta.w & kEnd)) {
+    if (meta.w & kHasQ) {
+      if (!mbar_wait(tb.qready(), nq & 1)) return false;
+      ++nq;
+    }
+    if (meta.w & kData) issue_scores(0);
+  }
+  uint32_t s = 0, ph = 0;
+  for (uint32_t n = 0;; ++n) {
+    const int flags = meta.w;
+    if (flags & kEnd) break;
+    const uint32_t s1 = (s + 1 == (uint32_t)S) ? 0u : s + 1;
+    const uint32_t ph1 = (s + 1 == (uint32_t)S) ? ph ^ 1u : ph;
+    // Look ahead: if stage n + 1 is already in and needs no new query rows,
+    // its scores go to the tensor core before this stage's P.V.
+    bool have_next = mbar_test_wait(bars + 8 * s1, ph1);
+    int4 meta1 = make_int4(0, 0, 0, 0);
+    bool scored1 = false;
+    if (have_next) {
+      meta1 = s_meta[s1];
+      if ((meta1.w & kData) && !(meta1.w & kEnd) && !(meta1.w & kHasQ)) {
+        issue_scores(s1);
+        scored1 = true;
+      }
+    }
+    // Stage n: wait for the probabilities, then P.V (or just release it)
+    if (!mbar_wait(tb.handed(n & 1), (n >> 1) & 1)) return false;
+    tc_fence_after();
+    if (flags & kFirst) fresh = true;
+    if (flags & kData) {
+      const uint32_t vb = stage0 + s * L.stage_bytes + L.kv_bytes;
+      const uint32_t pb = (n & 1) * pbuf_bytes;
+      for (int k = 0; k < HG; ++k)  // one MMA of K = 16 tokens per head
+        umma_bf16_warp(tmem, dp0 + ((pb + (uint32_t)k * 256) >> 4),
+                       dv0 + ((vb + (uint32_t)k * (kBlock * 128)) >> 4), idesc_o,
+                       !fresh || k > 0, lead);
+      fresh = false;
+      umma_commit_warp(bars + 8 * (S + s), lead);  // the stage is free once P.V has read it
+      umma_commit_warp(tb.pv(), lead);
+    } else if (lead) {
+      mbar_arrive(bars + 8 * (S + s));
+    }
+    if (flags & kLast) umma_commit_warp(tb.out(), lead);
+    // stage n + 1
+    if (!have_next) {
+      if (!mbar_wait(bars + 8 * s1, ph1)) return false;
+      meta1 = s_meta[s1];
+    }
+    if (!scored1 && !(meta1.w & kEnd)) {
+      if (meta1.w & kHasQ) {
+        if (!mbar_wait(tb.qready(), nq & 1)) return false;
+        ++nq;
+      }
+      if (meta1.w & kData) issue_scores(s1);
+    }
+    meta = meta1;
+    s = s1;
+    ph = ph1;
+  }
+  return true;
+}
+
+// The four softmax warps of the TMEM form (warps 1-4; warp w reaches TMEM
+// lanes 32 (w % 4) .. + 31).  Thread r owns MMA row r.  The query rows of a
+// piece come straight from global memory (the form keeps no q ring).
 template <int D>
 __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned char* smem,
                                              const SmemLayout& L, const int4* s_meta,
@@ -797,22 +952,16 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
   const bool rok = v < vpk;
   const int qhl = kvl * G + (rok ? v / NQ : 0);  // query head within the group
   const int jq = rok ? v % NQ : 0;               // query token
-  const int hq = HG * G;
-  const int ntok = HG * kBlock;             // the scores MMA's N: every head's tokens
+  const int ntok = HG * kBlock;
   const int pch = ntok / 8;                 // 16-byte chunks of a P row
+  const uint32_t pbuf_bytes = (uint32_t)(kTmemRows * ntok * 2);
   const uint32_t half_bytes = (uint32_t)HG * kBlock * 128;
   volatile int* s_merge = s_abort + 1;
-  const uint32_t sbar = bars + 8 * (2 * S + (int)L.q_slots);  // scores ready
-  const uint32_t obar = sbar + 8;                             // a piece's O ready
-  unsigned char* const qa = smem + L.off_pbuf;                // Q: 128 x D, swizzled
-  unsigned char* const pb = qa + kTmemRows * D * 2;           // P: 128 x ntok
-  const uint32_t qa_s = smem_u32(qa), pb_s = smem_u32(pb);
+  const TmemBars tb{bars + 8 * (2 * S + (int)L.q_slots)};
+  unsigned char* const qa = smem + L.off_pbuf;     // Q: 128 x D, swizzled
+  unsigned char* const pb = qa + kTmemRows * D * 2;  // P: two buffers of 128 x ntok
   const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-  const uint32_t t_o = tmem + lane_base;                       // O: columns [0, D)
-  const uint32_t t_s = tmem + lane_base + (uint32_t)(D + kvl * kBlock);  // this row's scores
-  const bool issuer = cw == 0 && lane == 0;
-  const uint32_t idesc_s = umma_idesc_bf16(kTmemRows, ntok, false);
-  const uint32_t idesc_o = umma_idesc_bf16(kTmemRows, D, true);
+  const uint32_t t_o = tmem + lane_base;  // O: columns [0, D)
 
   // Empty rows see nothing: zeros for all their (token, head) vectors.
   constexpr int kChunks = D * 2 / 16;
@@ -823,26 +972,22 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
         reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)rr * NQ * p.heads + vh) * D)[c] =
             make_uint4(0u, 0u, 0u, 0u);
   }
-
   // P rows hold zeros outside their own head's two 16-byte chunks, for good
-  for (int kc = 0; kc < pch; ++kc)
-    *reinterpret_cast<uint4*>(pb + (r >> 3) * (pch * 128) + kc * 128 + (r & 7) * 16) =
-        make_uint4(0u, 0u, 0u, 0u);
+  for (int b = 0; b < 2; ++b)
+    for (int kc = 0; kc < pch; ++kc)
+      *reinterpret_cast<uint4*>(pb + b * pbuf_bytes + (r >> 3) * (pch * 128) + kc * 128 +
+                                (r & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
   unsigned char* const prow = pb + (r >> 3) * (pch * 128) + (2 * kvl) * 128 + (r & 7) * 16;
-  // Descriptors are linear in the start address (16-byte units in the low
-  // bits), so each MMA's is a base plus an offset.
-  const uint64_t dq0 = umma_desc(qa_s, 16, 1024, kUmmaSwizzle128);
-  const uint64_t dk0 = umma_desc(0u, 16, 1024, kUmmaSwizzle128);
-  const uint64_t dp0 = umma_desc(pb_s, 128, (uint32_t)pch * 128, kUmmaSwizzleNone);
-  const uint64_t dv0 = umma_desc(0u, half_bytes, 1024, kUmmaSwizzle128);
-  const uint32_t stage0 = smem_u32(smem);
 
   float m = -INFINITY, l = 0.f;
-  bool fresh = true;  // no P.V issued yet in this piece: O holds nothing of it
-  uint32_t nqk = 0, nout = 0;
+  bool fresh = true;   // no P.V yet in this piece: O holds nothing of it
+  uint32_t npv = 0;    // P.V products handed over so far (all pieces); also
+                       // the count of stages with data, whose scores
+                       // alternate between two buffers
+  uint32_t nout = 0;   // pieces finished
   bool failed = false;
-  uint32_t s = 0, ph = 0;  // stage and its phase parity
-  for (;; s = (s + 1 == (uint32_t)S) ? (ph ^= 1u, 0u) : s + 1) {
+  uint32_t s = 0, ph = 0;
+  for (uint32_t n = 0;; ++n, s = (s + 1 == (uint32_t)S) ? (ph ^= 1u, 0u) : s + 1) {
     if (!mbar_wait(bars + 8 * s, ph)) {
       failed = true;
       break;
@@ -851,52 +996,38 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
     const int flags = meta.w;
     if (flags & kEnd) break;
     unsigned char* st = smem + s * L.stage_bytes;
-    const uint32_t st_s = stage0 + s * L.stage_bytes;
     const int tmask = meta.y & 0xffff;
     const int qh0 = (flags >> 16) * G;
+    const uint32_t b = n & 1;
 
-    bool new_q = false;
     if (flags & kFirst) {
       m = -INFINITY;
       l = 0.f;
       fresh = true;
       if (flags & kHasQ) {
-        // q ring slot 0 (this form's only one) -> this row of the Q operand:
-        // 16-byte chunk c of a 64-dim half at chunk c ^ (row & 7)
-        const unsigned char* src =
-            smem + (size_t)S * L.stage_bytes + (size_t)(jq * hq + qhl) * D * sizeof(T);
+        // this row's query vector -> row r of the Q operand: 16-byte chunk c
+        // of a 64-dim half at chunk c ^ (r & 7).  Every earlier scores MMA is
+        // complete (each was waited for below).
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const T*>(p.q) + (((size_t)meta.x * NQ + jq) * p.heads + qh0 + qhl) * D);
+        uint4 vals[D / 8];
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          const uint4 val = rok ? *reinterpret_cast<const uint4*>(src + c * 16)
-                                : make_uint4(0u, 0u, 0u, 0u);
+        for (int c = 0; c < D / 8; ++c) vals[c] = rok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c)
           *reinterpret_cast<uint4*>(qa + (c >> 3) * (kTmemRows * 128) + r * 128 +
-                                    (((c & 7) ^ (r & 7)) * 16)) = val;
-        }
+                                    (((c & 7) ^ (r & 7)) * 16)) = vals[c];
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bars + 8 * (2 * S));  // the q slot is free
-        new_q = true;
+        if (lane == 0) mbar_arrive(tb.qready());
       }
     }
 
     if (flags & kData) {
       const int rem = flags & 0xff;
       const int nvalid = min(kBlock, rem);
-      // new query rows must be in place before the scores MMA reads them
-      if (new_q) consumer_sync(kNcw * 32);
-      if (issuer) {
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          // 16 dims: 64-dim half ks / 4, 32 bytes into its 128-byte rows
-          const uint32_t qoff = (uint32_t)(ks >> 2) * (kTmemRows * 128) + (uint32_t)(ks & 3) * 32;
-          const uint32_t koff = st_s + (uint32_t)(ks >> 2) * half_bytes + (uint32_t)(ks & 3) * 32;
-          umma_bf16(tmem + D, dq0 + (qoff >> 4), dk0 + (koff >> 4), idesc_s, ks > 0);
-        }
-        umma_commit(sbar);
-      }
       // V rows that hold no data become zeros (P is 0 there, but 0 * NaN is
-      // not); the tensor core reads V only after the barrier below.
+      // not); the MMA warp reads V only after the hand-over below.
       if (nvalid < kBlock || tmask != 0xffff) {
         for (int c = cw * 32 + lane; c < ntok * kChunks; c += kNcw * 32) {
           const int tr = c / kChunks, dc = c - tr * kChunks;
@@ -906,16 +1037,15 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
                 make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      if (!mbar_wait(sbar, nqk & 1)) {
+      if (!mbar_wait(tb.scores(npv & 1), (npv >> 1) & 1)) {
         failed = true;
         break;
       }
-      ++nqk;
       tc_fence_after();
       uint32_t sr[16];
-      tmem_ld16(t_s, sr);
+      tmem_ld16(tmem + lane_base + (uint32_t)(D + (int)(npv & 1) * ntok + kvl * kBlock), sr);
       tmem_wait_ld();
-      // online softmax of this row's 16 scores; the running max is raised
+      // Online softmax of this row's 16 scores; the running max is raised
       // lazily (by more than kRescaleSlack), as in the other tensor forms.
       // A block every query token sees in full needs no masks.
       const bool dense = nvalid == kBlock && tmask == 0xffff && rem - (NQ - 1) >= kBlock;
@@ -945,8 +1075,13 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
         l *= alpha;
       }
       if (!fresh && __any_sync(kFull, raise)) {
-        // O holds earlier blocks of the piece (their P.V is complete):
-        // rescale the warp's rows (1 where this row's max did not move)
+        // O holds earlier blocks of the piece: once the last P.V handed over
+        // is complete, rescale the warp's rows (1 where the max did not move)
+        if (!mbar_wait(tb.pv(), (npv - 1) & 1)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
@@ -964,7 +1099,7 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
         float pv[16];
         const bool live = m != -INFINITY;
 #pragma unroll
-        for (int t = 0; t < kBlock; ++t) pv[t] = live ? exp2f(x[t] - m) : 0.f;
+        for (int t = 0; t < kBlock; ++t) pv[t] = live ? ex2_approx(x[t] - m) : 0.f;
         float s8[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) s8[t] = pv[t] + pv[t + 8];
@@ -975,31 +1110,23 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
         for (int t2 = 0; t2 < 8; ++t2) pk[t2] = pack_bf16(pv[2 * t2], pv[2 * t2 + 1]);
       }
       // this row's head's two 8-token chunks of P (the rest stays zero)
-      *reinterpret_cast<uint4*>(prow) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      *reinterpret_cast<uint4*>(prow + 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      unsigned char* pr = prow + b * pbuf_bytes;
+      *reinterpret_cast<uint4*>(pr) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<uint4*>(pr + 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       fence_proxy_async_smem();
-      tc_fence_before();
-      consumer_sync(kNcw * 32);  // P, zeroed V rows and any rescaled O are in place
-      if (issuer) {
-        tc_fence_after();
-        const uint32_t vb = st_s + L.kv_bytes;
-        for (int k = 0; k < HG; ++k) {  // one MMA of K = 16 tokens per head
-          umma_bf16(tmem, dp0 + (uint32_t)(k * 16), dv0 + ((vb + (uint32_t)k * (kBlock * 128)) >> 4),
-                    idesc_o, !fresh || k > 0);
-        }
-        umma_commit(bars + 8 * (S + s));  // the stage is free once P.V has read it
-      }
+      ++npv;
       fresh = false;
-    } else {
-      // no data: hand the stage back once every thread has read its metadata
-      consumer_sync(kNcw * 32);
-      if (issuer) mbar_arrive(bars + 8 * (S + s));
     }
+    // hand the stage over: P (and zeroed V rows, rescaled O) are in place, or
+    // the stage had no data and its metadata has been read
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tb.handed(b));
 
     if (flags & kLast) {
       const int row = meta.x;
-      if (issuer) umma_commit(obar);
-      if (!mbar_wait(obar, nout & 1)) {
+      // the piece's last P.V is complete
+      if (!mbar_wait(tb.out(), nout & 1)) {
         failed = true;
         break;
       }
@@ -1291,7 +1418,7 @@ __device__ __forceinline__ void consume_mma_t(const DecodeParams& p, unsigned ch
 }
 
 template <typename T, int D, int QW, int MMA>
-__global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 1) * 32
+__global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
                                   : consumers_off_producer(MMA, D) ? kMaxThreadsOffProducer
                                   : MMA ? kMaxThreadsMulti
                                       : (QW <= 2 ? kMaxThreads : kMaxThreadsMulti))
@@ -1348,9 +1475,14 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 1) * 32
     }
     for (int j = 0; j < (int)L.q_slots; ++j)
       mbar_init(bars + 8 * (2 * S + j), ncw);  // qfree: every consumer warp has read it
-    if (MMA == kMmaTmem)
-      for (int j = 0; j < 3; ++j)  // scores ready, a piece's O ready, all MMAs drained
-        mbar_init(bars + 8 * (2 * S + (int)L.q_slots + j), 1);
+    if (MMA == kMmaTmem) {
+      // scores ready [2], probabilities handed over [2] (one arrive per
+      // softmax warp), a piece's O complete, all MMAs drained, query rows
+      // ready (per softmax warp), a P.V complete
+      const uint32_t tb = bars + 8 * (2 * S + (int)L.q_slots);
+      const uint32_t counts[kTmemBars] = {1, 1, kTmemWarps, kTmemWarps, 1, 1, kTmemWarps, 1};
+      for (int j = 0; j < kTmemBars; ++j) mbar_init(tb + 8 * j, counts[j]);
+    }
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -1462,7 +1594,8 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 1) * 32
                             flags);
       uint32_t bytes = 0;
       if ((flags & kData) && !(flags & kGathered)) bytes += 2 * L.kv_bytes;
-      if (flags & kHasQ) bytes += L.q_bytes;
+      const bool ring_q = MMA != kMmaTmem && (flags & kHasQ);  // the TMEM form reads q itself
+      if (ring_q) bytes += L.q_bytes;
       if (bytes == 0) {
         mbar_arrive(full);
       } else {
@@ -1483,14 +1616,14 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 1) * 32
             bulk_g2s(base + L.kv_bytes, vp + off, L.kv_bytes, full, pol);
           }
         }
-        if (flags & kHasQ) {
+        if (ring_q) {
           const uint32_t qbase = smem_u32(smem + L.off_q + qslot * L.q_slot_bytes);
           for (int jq = 0; jq < NQ; ++jq)
             bulk_g2s(qbase + jq * q_slice, qp + (((size_t)row * NQ + jq) * p.heads + qh0) * D,
                      q_slice, full, pol);
         }
       }
-      if (flags & kHasQ) {
+      if (ring_q) {
         if (++qnext == L.q_slots) {
           qnext = 0;
           ++qphase;
@@ -1500,7 +1633,7 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 1) * 32
     };
     auto emit = [&](int row, int flags, int phys) -> bool {
       if (!wait_free()) return false;
-      if ((flags & kHasQ) && !wait_q()) return false;
+      if (MMA != kMmaTmem && (flags & kHasQ) && !wait_q()) return false;
       publish(row, flags, phys, 0xffff);
       return true;
     };
@@ -1511,7 +1644,7 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 1) * 32
     const long long pool_slots = p.pool_blocks * kBlock;
     auto gather = [&](int row, int blk, int flags) -> bool {
       bool ok2 = true;
-      if (lane == 0) ok2 = wait_free() && (!(flags & kHasQ) || wait_q());
+      if (lane == 0) ok2 = wait_free() && (MMA == kMmaTmem || !(flags & kHasQ) || wait_q());
       ok2 = __shfl_sync(kFull, ok2, 0);
       if (!ok2) return false;
       const uint32_t s = __shfl_sync(kFull, n, 0) % S;
@@ -1602,19 +1735,27 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 1) * 32
 
   // -------------------------------------------------------------------- consumers
   if constexpr (MMA == kMmaTmem) {
-    if (warp > kTmemWarps) return;
+    if (warp > kTmemWarps + 1) return;
     const uint32_t tmem = *s_tmem;
-    consume_tmem<D>(p, smem, L, s_meta, bars, s_prefix, s_abort, N, U, nhg, nvec, warp, lane,
-                    tmem);
-    // Free the tensor memory once every consumer is done with it and the
-    // tensor core has finished every MMA (bounded wait on a last commit).
+    const TmemBars tb{bars + 8 * (2 * S + (int)L.q_slots)};
+    if (warp == kTmemWarps + 1) {
+      // the MMA warp; on a timeout the softmax warps time out too
+      if (!tmem_mma_warp<D>(p, smem, L, s_meta, bars, tmem, lane)) {
+        if (lane == 0) atomicOr(p.status, (uint32_t)NSV_DEV_TIMEOUT);
+        *s_abort = 1;
+      }
+      umma_commit_warp(tb.drained(), lane == 0);  // arrives once every MMA it issued is done
+    } else {
+      consume_tmem<D>(p, smem, L, s_meta, bars, s_prefix, s_abort, N, U, nhg, nvec, warp, lane,
+                      tmem);
+    }
+    // Free the tensor memory once every role is done with it and the
+    // tensor core has finished every MMA (bounded wait on the last commit).
     tc_fence_before();
-    consumer_sync(kTmemWarps * 32);
+    asm volatile("bar.sync 2, %0;" ::"r"((kTmemWarps + 1) * 32) : "memory");
     tc_fence_after();
     if (warp == 1) {
-      const uint32_t fbar = bars + 8 * (2 * S + (int)L.q_slots + 2);
-      if (lane == 0) umma_commit(fbar);
-      (void)mbar_wait(fbar, 0);
+      (void)mbar_wait(tb.drained(), 0);
       tc_fence_after();
       tmem_dealloc(tmem, tmem_ncols);
     }

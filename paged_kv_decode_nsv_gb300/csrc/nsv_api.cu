@@ -133,11 +133,15 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   if (consumer == NSV_CONSUMER_AUTO) {
     // The tensor cores pay off once several query vectors share a K/V tile,
     // where the CUDA cores repeat the work per vector.  Up to 8 vectors the
-    // tokens are the MMA rows (one warp per KV head); beyond, the vectors
-    // (16 per warp), which measured faster than 8 per warp with tokens as rows.
+    // tokens are the MMA rows (one warp per KV head); 9 to 16, the vectors
+    // (16 per warp), which measured faster than 8 per warp with tokens as
+    // rows; beyond, tcgen05 into tensor memory when the KV heads split into
+    // its groups (17-64 vectors: 1.0-1.9x the vectors-as-rows form's speed).
     consumer = !(tensor_ok && qw <= 0) ? kConsumerCuda
                : vpk <= 8              ? kConsumerTensor
-                                       : kConsumerTensorVectorRows;
+               : (vpk > kMmaRows && s->num_kv_heads % tmem_heads(vpk) == 0)
+                   ? kConsumerTensorTmem
+                   : kConsumerTensorVectorRows;
   } else if (consumer == kConsumerTensor || consumer == kConsumerTensorVectorRows ||
              consumer == kConsumerTensorTmem) {
     if (!tensor_ok || qw > 1) return NSV_ERR_RANGE;
@@ -198,7 +202,7 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   }
   if (L.total > (uint32_t)kSmemPerCta) return NSV_ERR_RANGE;
   const int threads =
-      (tmem_form ? kTmemWarps + 1 : cta_warps(form_of(consumer), s->head_dim, hg * wpk)) * 32;
+      (tmem_form ? kTmemWarps + 2 : cta_warps(form_of(consumer), s->head_dim, hg * wpk)) * 32;
   int fit = kSmemPerSm / (int)(L.total + kSmemReserved);
   // CTAs one SM holds by threads and by registers (each kernel variant's
   // register count is fixed at compile time)

@@ -181,11 +181,12 @@ constexpr int kTmemRows = 128;
 __host__ __device__ constexpr int tmem_rows_per_head(int vpk) { return vpk <= 32 ? 32 : 64; }
 __host__ __device__ constexpr int tmem_heads(int vpk) { return kTmemRows / tmem_rows_per_head(vpk); }
 // Tensor-memory columns a CTA allocates (a power of two, at least 32): the
-// output accumulator (head_dim columns) and the scores (16 per KV head).
+// output accumulator (head_dim columns) and two score buffers (16 columns
+// per KV head each).
 __host__ __device__ constexpr int tmem_cols(int head_dim, int vpk) {
-  return head_dim + tmem_heads(vpk) * kBlock <= 128 ? 128
-         : head_dim + tmem_heads(vpk) * kBlock <= 256 ? 256
-                                                     : 512;
+  return head_dim + 2 * tmem_heads(vpk) * kBlock <= 128 ? 128
+         : head_dim + 2 * tmem_heads(vpk) * kBlock <= 256 ? 256
+                                                         : 512;
 }
 
 // Whether a variant keeps its consumer warps off the producer's SM
@@ -222,6 +223,7 @@ __host__ __device__ constexpr bool fixed_q_slot(int form, int qw) {
 // price of a wait for segments shorter than the ring of stages, and one for
 // the variants that read a fixed slot.
 __host__ __device__ inline int q_slots_for(uint32_t q_bytes, int stages, int form, int qw) {
+  if (form == kFormTmem) return 0;  // it reads its query rows from global memory
   return (!fixed_q_slot(form, qw) && q_bytes <= 8192u) ? stages : 1;
 }
 
@@ -245,13 +247,14 @@ __host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int he
   L.off_bars = align_up(off, 8);
   // mbarriers: full[stages], empty[stages], qfree[q_slots]; the TMEM form
   // adds three (scores ready, output ready, drained)
-  off = L.off_bars + (uint32_t)(2 * stages + (int)L.q_slots + (form == kFormTmem ? 3 : 0)) * 8;
+  off = L.off_bars + (uint32_t)(2 * stages + (int)L.q_slots + (form == kFormTmem ? 8 : 0)) * 8;
   if (form == kFormTmem) {
     // its MMA operands: the query rows (128 x head_dim, 128-byte swizzle,
-    // 1024-byte aligned) and the probabilities (128 x the group's tokens)
+    // 1024-byte aligned) and two probability buffers (128 x the group's
+    // tokens each)
     L.off_pbuf = align_up(off, 1024);
     off = L.off_pbuf + (uint32_t)(kTmemRows * head_dim * 2) +
-          (uint32_t)(kTmemRows * heads_per_cta * kBlock * 2);
+          2u * (uint32_t)(kTmemRows * heads_per_cta * kBlock * 2);
   } else {
     L.off_pbuf = align_up(off, 16);
     off = L.off_pbuf + (form == kFormCuda ? (uint32_t)(nvec * kBlock * 4) : 0u);

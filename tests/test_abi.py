@@ -60,6 +60,8 @@ def _cta_warps(nsv, consumer, consumer_warps, head_dim=128):
     """Warps of a planned CTA: the producer and the consumers, plus, with the
     vectors as the MMA rows at head_dim 128, an idle warp at each multiple of
     4 the consumers pass (none shares the producer's sub-partition)."""
+    if consumer == nsv.CONSUMER_TENSOR_TMEM:
+        return 6      # a producer, four softmax warps and an MMA warp
     if consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS and head_dim == 128:
         return consumer_warps + 1 + (consumer_warps - 1) // 3
     return consumer_warps + 1
@@ -137,7 +139,11 @@ def test_plan_refuses_too_many_query_vectors(nsv, heads, kv_heads, qlen, dtype):
 
 
 def test_odd_vector_counts_above_15_run_on_the_tensor_cores(nsv):
+    # 32 KV heads split into the TMEM form's groups of 4 (17 vectors each)
     p = nsv.plan_split(_shape(nsv, query_len=17), num_sms=152)
+    assert p.consumer == nsv.CONSUMER_TENSOR_TMEM and p.kv_heads_per_cta == 4
+    # 6 KV heads do not: two vectors-as-rows warps per KV head
+    p = nsv.plan_split(_shape(nsv, num_heads=6, num_kv_heads=6, query_len=17), num_sms=152)
     assert p.consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS
     assert p.threads == _cta_warps(nsv, p.consumer, p.kv_heads_per_cta * 2) * 32
 
@@ -147,14 +153,14 @@ def test_odd_vector_counts_above_15_run_on_the_tensor_cores(nsv):
     (8, 8, 17, 128, 4, 1), (32, 8, 8, 64, 4, 2), (64, 8, 8, 64, 2, 2)])
 def test_plan_tmem_form(nsv, heads, kv_heads, qlen, head_dim, group, cps):
     """NSV_CONSUMER_TENSOR_TMEM: one 128-row MMA group per CTA (4 KV heads of
-    up to 32 vectors, 2 of up to 64), a producer and four consumer warps; two
-    CTAs per SM (each with a 2-stage ring) where their shared memory fits, as
-    their 256 (head_dim 128) or 128 tensor-memory columns do."""
+    up to 32 vectors, 2 of up to 64), a producer, four softmax warps and an
+    MMA warp; two CTAs per SM where their shared memory fits, as their 256
+    (head_dim 128) or 128 tensor-memory columns do."""
     p = nsv.plan_custom(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen,
                                head_dim=head_dim),
                         num_sms=152, consumer=nsv.CONSUMER_TENSOR_TMEM)
     assert p.consumer == nsv.CONSUMER_TENSOR_TMEM and p.kv_heads_per_cta == group
-    assert p.threads == 5 * 32 and p.vectors_per_warp == 1
+    assert p.threads == 6 * 32 and p.vectors_per_warp == 1
     assert p.ctas_per_sm == cps and p.grid == 152 * cps
     assert cps == 1 or 2 * (p.smem_bytes + 1024) <= 228 * 1024
 
@@ -174,14 +180,18 @@ def test_plan_vector_rows_form(nsv, qlen, warps):
     (32, 32, 4, "bf16", 2, 8, 8),    # 4 query tokens
     (32, 32, 3, "bf16", 2, 8, 8),
     (16, 1, 1, "bf16", 3, 1, 1),     # 16 vectors: one warp, vectors as the MMA rows
-    (32, 8, 8, "bf16", 3, 4, 8),     # 32 vectors: two warps per KV head
-    (32, 8, 5, "bf16", 3, 4, 8),     # 20 vectors
+    (32, 8, 8, "bf16", 4, 4, 6),     # 32 vectors: tcgen05, 4 KV heads of 32 rows
+    (32, 8, 5, "bf16", 4, 4, 6),     # 20 vectors
+    (64, 8, 8, "bf16", 4, 2, 6),     # 64 vectors: 2 KV heads of 64 rows
+    (24, 6, 5, "bf16", 3, 2, 4),     # 20 vectors, 6 KV heads: no 4-head groups
     (32, 8, 1, "f32", 1, 4, 8),      # fp32 stays on the CUDA cores
 ])
 def test_plan_consumer_choice(nsv, heads, kv_heads, qlen, dtype, consumer, hg, warps):
     """The default plan runs bf16 shapes with 2 or more query vectors per KV
     head on the tensor cores: up to 8 with the tokens as the MMA rows (one
-    warp per KV head), beyond with the vectors as the rows (16 per warp)."""
+    warp per KV head), 9 to 16 with the vectors as the rows (16 per warp),
+    beyond with tcgen05 into tensor memory where the KV heads split into its
+    groups (else the vectors as the rows)."""
     p = nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen,
                               dtype=nsv.BF16 if dtype == "bf16" else nsv.F32), num_sms=152)
     assert p.consumer == consumer and p.kv_heads_per_cta == hg
@@ -359,9 +369,15 @@ def test_every_plan_round_trips(nsv):
                                                  (32, 8, 10), (128, 2, 1)])
 def test_bf16_takes_up_to_64_vectors_per_kv_head(nsv, heads, kv_heads, qlen):
     """Beyond 32 query vectors per KV head only the tensor cores serve the
-    read: vectors as the MMA rows, one warp per 16 of them."""
+    read: tcgen05 into tensor memory, 2 KV heads of 64 rows per MMA, or with
+    an odd KV-head count the vectors as the rows, one warp per 16 of them."""
     p = nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen),
                        num_sms=152)
     vpk = heads // kv_heads * qlen
-    assert vpk > 32 and p.consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS
-    assert p.threads == _cta_warps(nsv, p.consumer, p.kv_heads_per_cta * -(-vpk // 16)) * 32
+    assert vpk > 32
+    if kv_heads % 2 == 0:
+        assert p.consumer == nsv.CONSUMER_TENSOR_TMEM and p.kv_heads_per_cta == 2
+        assert p.threads == 6 * 32
+    else:
+        assert p.consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS
+        assert p.threads == _cta_warps(nsv, p.consumer, p.kv_heads_per_cta * -(-vpk // 16)) * 32
