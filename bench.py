@@ -108,7 +108,8 @@ def recorded_traffic(consumer, read_bytes):
             sha = hashlib.sha256(f.read()).hexdigest()
         if d.get("decode_cu_sha256") != sha:
             return None
-        cap = d["captures"][{1: "cuda", 2: "tensor", 3: "tensor_vector_rows"}[consumer]]
+        cap = d["captures"][{1: "cuda", 2: "tensor", 3: "tensor_vector_rows",
+                             4: "tensor_tmem"}[consumer]]
         return cap["traffic_over_algorithmic"] * read_bytes
     except (OSError, ValueError, KeyError):
         return None
@@ -425,7 +426,8 @@ def run_nsv(args, wl):
                      if peak_kind == "measured" else "fallback",
                      "kernel": "decode read (decode_kernel, %s consumer)"
                                % {1: "CUDA-core", 2: "tensor-core",
-                                  3: "tensor-core, vectors as rows"}[plan.consumer],
+                                  3: "tensor-core, vectors as rows",
+                                  4: "tcgen05, tensor-memory accumulators"}[plan.consumer],
                      "bytes_per_launch": wl.read_bytes(), "us_per_launch": ms_read * 1e3,
                      "traffic": recorded_traffic(plan.consumer, wl.read_bytes())},
         "e2e": {"value": whole_job_gbs(step_bytes, ws, e2e_ms), "unit": "GB/s",

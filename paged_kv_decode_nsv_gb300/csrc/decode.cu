@@ -807,8 +807,9 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
 // the softmax warps; K as staged by TMA (K-major); P in 8x16-byte core
 // matrices (zeros outside the row's head); V as staged (MN-major).
 // Barriers beyond the ring's: scores ready [2], probabilities handed over
-// [2], a piece's O complete, every MMA drained, query rows ready, a P.V
-// complete.
+// [2], a piece's O complete, every MMA drained, query rows ready.  (A stage's
+// empty barrier, which its P.V's commit completes, also tells the softmax
+// warps that this P.V is done.)
 struct TmemBars {
   uint32_t base;
   __device__ uint32_t scores(uint32_t b) const { return base + 8 * b; }
@@ -816,9 +817,8 @@ struct TmemBars {
   __device__ uint32_t out() const { return base + 32; }
   __device__ uint32_t drained() const { return base + 40; }
   __device__ uint32_t qready() const { return base + 48; }
-  __device__ uint32_t pv() const { return base + 56; }
 };
-constexpr int kTmemBars = 8;
+constexpr int kTmemBars = 7;
 
 // The MMA warp.  The d-th stage with data has its scores in buffer d & 1,
 // stage n's probabilities are in buffer n & 1; every barrier completes once
@@ -907,7 +907,6 @@ __device__ __forceinline__ bool tmem_mma_warp(const DecodeParams& p, unsigned ch
                        !fresh || k > 0, lead);
       fresh = false;
       umma_commit_warp(bars + 8 * (S + s), lead);  // the stage is free once P.V has read it
-      umma_commit_warp(tb.pv(), lead);
     } else if (lead) {
       mbar_arrive(bars + 8 * (S + s));
     }
@@ -981,6 +980,7 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
 
   float m = -INFINITY, l = 0.f;
   bool fresh = true;   // no P.V yet in this piece: O holds nothing of it
+  uint32_t pv_s = 0, pv_ph = 0;  // stage and phase of the last P.V handed over
   uint32_t npv = 0;    // P.V products handed over so far (all pieces); also
                        // the count of stages with data, whose scores
                        // alternate between two buffers
@@ -1076,8 +1076,9 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
       }
       if (!fresh && __any_sync(kFull, raise)) {
         // O holds earlier blocks of the piece: once the last P.V handed over
-        // is complete, rescale the warp's rows (1 where the max did not move)
-        if (!mbar_wait(tb.pv(), (npv - 1) & 1)) {
+        // is complete (its commit completes that stage's empty barrier),
+        // rescale the warp's rows (1 where the max did not move)
+        if (!mbar_wait(bars + 8 * (S + pv_s), pv_ph)) {
           failed = true;
           break;
         }
@@ -1115,6 +1116,8 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
       *reinterpret_cast<uint4*>(pr + 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       fence_proxy_async_smem();
       ++npv;
+      pv_s = s;
+      pv_ph = ph;
       fresh = false;
     }
     // hand the stage over: P (and zeroed V rows, rescaled O) are in place, or
@@ -1478,9 +1481,9 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
     if (MMA == kMmaTmem) {
       // scores ready [2], probabilities handed over [2] (one arrive per
       // softmax warp), a piece's O complete, all MMAs drained, query rows
-      // ready (per softmax warp), a P.V complete
+      // ready (per softmax warp)
       const uint32_t tb = bars + 8 * (2 * S + (int)L.q_slots);
-      const uint32_t counts[kTmemBars] = {1, 1, kTmemWarps, kTmemWarps, 1, 1, kTmemWarps, 1};
+      const uint32_t counts[kTmemBars] = {1, 1, kTmemWarps, kTmemWarps, 1, 1, kTmemWarps};
       for (int j = 0; j < kTmemBars; ++j) mbar_init(tb + 8 * j, counts[j]);
     }
     *s_abort = 0;

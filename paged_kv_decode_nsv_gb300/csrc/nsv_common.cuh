@@ -247,7 +247,7 @@ __host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int he
   L.off_bars = align_up(off, 8);
   // mbarriers: full[stages], empty[stages], qfree[q_slots]; the TMEM form
   // adds three (scores ready, output ready, drained)
-  off = L.off_bars + (uint32_t)(2 * stages + (int)L.q_slots + (form == kFormTmem ? 8 : 0)) * 8;
+  off = L.off_bars + (uint32_t)(2 * stages + (int)L.q_slots + (form == kFormTmem ? 7 : 0)) * 8;
   if (form == kFormTmem) {
     // its MMA operands: the query rows (128 x head_dim, 128-byte swizzle,
     // 1024-byte aligned) and two probability buffers (128 x the group's

@@ -240,6 +240,28 @@ def headline_spec4_bf16(seed=4):
                  block_size=16, max_blocks=512, dtype="bf16", lens=lens, rng=rng, query_len=4)
 
 
+def headline_gqa8_spec8_bf16(seed=4):
+    """The headline batch with both: 64 query heads share 8 KV heads (8 per
+    group) and each row verifies 8 speculative tokens, so 64 query vectors
+    read every K/V tile; same lengths (which count the 8 new tokens) and pool
+    recipe."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(512, 8192, size=256, endpoint=True)
+    return _make("headline_gqa8_spec8_bf16", seed, rows=256, heads=64, kv_heads=8, head_dim=128,
+                 block_size=16, max_blocks=512, dtype="bf16", lens=lens, rng=rng, query_len=8)
+
+
+def manyrow_gqa8_spec8_bf16(seed=3):
+    """The many-row batch with 64 query vectors per KV tile (64 query heads
+    over 8 KV heads, 8 query tokens): a 0.7 GB case for a full ncu capture."""
+    rng = np.random.default_rng(seed)
+    real = np.concatenate([[2048], _log_uniform(rng, 239, 128, 2048)])
+    lens = np.concatenate([real, np.zeros(16, dtype=np.int64)])
+    return _make("manyrow_gqa8_spec8_bf16", seed, rows=256, heads=64, kv_heads=8, head_dim=128,
+                 block_size=16, max_blocks=128, dtype="bf16", lens=lens, free_frac=0.10, rng=rng,
+                 query_len=8)
+
+
 def manyrow_gqa4_bf16(seed=3):
     """The many-row batch with 8 KV heads shared by 32 query heads: a 0.7 GB
     grouped-query case small enough for a full ncu capture."""
@@ -259,6 +281,8 @@ WORKLOADS = {
     "headline_gqa4_bf16": headline_gqa4_bf16,
     "headline_spec4_bf16": headline_spec4_bf16,
     "manyrow_gqa4_bf16": manyrow_gqa4_bf16,
+    "headline_gqa8_spec8_bf16": headline_gqa8_spec8_bf16,
+    "manyrow_gqa8_spec8_bf16": manyrow_gqa8_spec8_bf16,
 }
 
 

@@ -407,10 +407,13 @@ def test_multi_query_plans(nsv, kw):
     assert_parity("bf16", gpu_out_f64(out), oracle_step(wl, host))
 
 
-@pytest.mark.parametrize("name", ["headline_spec4_bf16", "headline_gqa4_bf16"])
+@pytest.mark.parametrize("name", ["headline_spec4_bf16", "headline_gqa4_bf16",
+                                  "headline_gqa8_spec8_bf16"])
 def test_headline_variants_sampled(nsv, name):
-    """Full-size headline batches with 4 query tokens per row, and with 4
-    query heads per KV head, in the benchmark's default plan; sampled rows."""
+    """Full-size headline batches with 4 query tokens per row, with 4 query
+    heads per KV head, and with both grouped heads and speculative tokens (64
+    query vectors per KV head, tcgen05), in the benchmark's default plan;
+    sampled rows."""
     wl = W.WORKLOADS[name]()
     inp = device_inputs(wl)
     ctx = wl.context_lens
