@@ -184,3 +184,52 @@ def test_tensor_consumer_slot_gather(nsv, form, heads, kv_heads, head_dim):
     ref = oracle.paged_decode_slots(host["q"], host["k_pool"], host["v_pool"], table, width,
                                     wl.context_lens, wl.scale)
     assert_parity("bf16", gpu_out_f64(out), ref)
+
+
+@pytest.mark.parametrize("consumer", [3, 4], ids=["vectors_as_rows", "tmem"])
+def test_tensor_forms_ignore_poisoned_padding(nsv, consumer):
+    """NaN in every pool slot no row addresses (past a row's length inside
+    its last block, and all unused blocks) and garbage in the table's padding
+    give the same bits as the clean run: masked scores and zeroed V rows keep
+    NaN out of the MMAs (32 vectors per KV head)."""
+    import torch
+    wl = _case(32, 8, 8, 128, lens=[3, 16, 200, 1, 0, 999, 513, 40], seed=23, free_frac=0.5)
+    inp = device_inputs(wl)
+    host = host_copy(inp)
+    plan = _plan(nsv, inp, consumer=consumer)
+    clean = gpu_read(wl, inp, plan=plan).clone()
+    used = np.zeros((wl.num_blocks + 1, 16), dtype=bool)
+    for r, c in enumerate(wl.context_lens):
+        for t in range(int(c)):
+            used[wl.block_tables[r, t // 16], t % 16] = True
+    mask = torch.from_numpy(~used).cuda()[:, None, :, None]
+    nan = torch.tensor(float("nan"), dtype=inp["k_pool"].dtype, device="cuda")
+    inp["k_pool"] = torch.where(mask, nan, inp["k_pool"])
+    inp["v_pool"] = torch.where(mask, nan, inp["v_pool"])
+    bt = wl.block_tables.copy()
+    bt[bt < 0] = 2 ** 30
+    inp["block_tables"] = torch.from_numpy(bt).cuda()
+    poisoned = gpu_read(wl, inp, plan=plan)
+    assert status()[0] == 0
+    assert torch.equal(poisoned, clean)
+    assert_parity("bf16", gpu_out_f64(poisoned), oracle_read(wl, host))
+
+
+@pytest.mark.parametrize("consumer", [3, 4], ids=["vectors_as_rows", "tmem"])
+def test_tensor_forms_skip_a_bad_block_mid_row(nsv, consumer):
+    """A walked block id outside the pool in the middle of a row: that stage
+    carries no data, the status flags it, and every other row stays exact."""
+    import torch
+    wl = _case(32, 8, 8, 128, lens=[40, 600, 300, 17], seed=29)
+    inp = device_inputs(wl)
+    host = host_copy(inp)
+    ref = oracle_read(wl, host)
+    bt = wl.block_tables.copy()
+    bt[1, 5] = wl.num_blocks + 5
+    inp["block_tables"] = torch.from_numpy(bt).cuda()
+    status()
+    out = gpu_out_f64(gpu_read(wl, inp, plan=_plan(nsv, inp, consumer=consumer)))
+    st, _ = status()
+    assert st & nsv.DEV_BAD_BLOCK
+    keep = [0, 2, 3]
+    assert_parity("bf16", out[keep], ref[keep])
