@@ -180,17 +180,18 @@ typedef struct nsv_plan {
  *  NSV_CONSUMER_TENSOR_TMEM: bf16 only, on the 5th-generation tensor cores
  *                       (tcgen05.mma with the accumulators in tensor
  *                       memory).  The MMA's 128 rows are the query vectors
- *                       of 4 KV heads (up to 32 vectors each) or 2 (up to
- *                       64), padded with zero rows; so kv_heads_per_cta is
- *                       4 or 2, and num_kv_heads must be a multiple of it.
+ *                       of a group of 4, 2 or 1 KV heads (128 / group rows
+ *                       each, zero past the vectors): kv_heads_per_cta is
+ *                       the group, which must divide num_kv_heads; by
+ *                       default the largest that fits.
  *                       Four softmax warps (one thread per row) and an MMA
  *                       warp that issues the next block's scores while the
  *                       softmax warps work; K/V tiles by 2-D TMA as above.
  * The default plan takes NSV_CONSUMER_TENSOR for bf16 shapes with 2 to 8
  * query vectors per KV head, NSV_CONSUMER_TENSOR_VECTOR_ROWS for 9 to 16,
- * NSV_CONSUMER_TENSOR_TMEM for 17 to 64 (NSV_CONSUMER_TENSOR_VECTOR_ROWS
- * when num_kv_heads is not a multiple of its group), and the CUDA-core one
- * otherwise. */
+ * NSV_CONSUMER_TENSOR_TMEM for 17 to 64 when its group can be 2 or 4 KV
+ * heads (NSV_CONSUMER_TENSOR_VECTOR_ROWS otherwise, for example for an odd
+ * num_kv_heads), and the CUDA-core one otherwise. */
 enum {
     NSV_CONSUMER_AUTO = 0,
     NSV_CONSUMER_CUDA = 1,

@@ -792,7 +792,7 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
 
 // The TMEM form (bf16) on the 5th-generation tensor cores: tcgen05.mma from
 // shared-memory operands into tensor-memory accumulators.  The MMA has 128
-// rows: the group's KV heads take R = 32 or 64 rows each (their query
+// rows: the group's KV heads take R = 128 / group rows each (their query
 // vectors, zero rows past them), so one MMA over the stage's tokens (16 per
 // head) gives every row its scores, and each row keeps only its own head's
 // 16 columns.  Roles:
@@ -943,7 +943,7 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
   constexpr int kNcw = kTmemWarps;
   const int G = p.group, NQ = p.query_len, HG = p.heads_per_cta, S = p.stages;
   const int vpk = G * NQ;
-  const int R = tmem_rows_per_head(vpk);    // rows per KV head; HG * R == 128
+  const int R = kTmemRows / HG;             // rows per KV head of the group
   const int cw = warp - 1;
   const int q4 = warp & 3;                  // the TMEM lane quadrant this warp reaches
   const int r = q4 * 32 + lane;             // this thread's MMA row
@@ -1466,7 +1466,7 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // the TMEM form's tensor-memory columns and their base address
-  const uint32_t tmem_ncols = MMA == kMmaTmem ? (uint32_t)tmem_cols(D, G * NQ) : 0u;
+  const uint32_t tmem_ncols = MMA == kMmaTmem ? (uint32_t)tmem_cols(D, HG) : 0u;
   uint32_t* const s_tmem = reinterpret_cast<uint32_t*>(smem + L.off_flag + 8);
 
   if (tid == 0) {

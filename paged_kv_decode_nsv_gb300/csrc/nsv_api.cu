@@ -139,7 +139,7 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
     // its groups (17-64 vectors: 1.0-1.9x the vectors-as-rows form's speed).
     consumer = !(tensor_ok && qw <= 0) ? kConsumerCuda
                : vpk <= 8              ? kConsumerTensor
-               : (vpk > kMmaRows && s->num_kv_heads % tmem_heads(vpk) == 0)
+               : (vpk > kMmaRows && tmem_group(s->num_kv_heads, vpk) >= 2)
                    ? kConsumerTensorTmem
                    : kConsumerTensorVectorRows;
   } else if (consumer == kConsumerTensor || consumer == kConsumerTensorVectorRows ||
@@ -170,11 +170,12 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   const int tile = kBlock * s->head_dim * elem;
   const bool tmem_form = consumer == kConsumerTensorTmem;
   if (tmem_form) {
-    // one 128-row MMA group per CTA: 4 KV heads of up to 32 vectors, or 2
-    // of up to 64
-    const int gh = tmem_heads(vpk);
-    if (s->num_kv_heads % gh != 0 || (hg > 0 && hg != gh)) return NSV_ERR_RANGE;
-    hg = gh;
+    // one 128-row MMA group per CTA: 4, 2 or 1 KV heads, each with 128 /
+    // group rows for its vectors
+    if (hg <= 0)
+      hg = tmem_group(s->num_kv_heads, vpk);
+    else if (!tmem_group_ok(hg, s->num_kv_heads, vpk))
+      return NSV_ERR_RANGE;
   } else if (hg <= 0) {
     // Largest KV-head group whose K+V stage stays within 64 KiB and whose
     // query vectors fill at most 8 consumer warps: big bulk copies, few CTAs.
@@ -213,7 +214,7 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   // that allocates tensor memory, however few columns it takes; two CTAs of
   // 256 columns do run side by side: the 64-vector read takes 929 us with two
   // per SM against 1540 us with one, on GB300.)
-  if (tmem_form) fit_threads = std::min(fit_threads, 512 / tmem_cols(s->head_dim, vpk));
+  if (tmem_form) fit_threads = std::min(fit_threads, 512 / tmem_cols(s->head_dim, hg));
   if (tmem_form && auto_stages && cps <= 0 && fit < 2 && fit_threads >= 2 && stages > 2) {
     // Two CTAs with a 2-stage ring each beat one CTA with a deep one: each
     // CTA's stage is a chain of dependent steps (MMA, softmax, MMA) that the

@@ -171,22 +171,28 @@ __host__ __device__ constexpr int form_of(int consumer) {
 }
 
 // The TMEM form (tcgen05.mma, accumulators in tensor memory).  Its MMA has
-// 128 rows: each KV head of the group takes R = 32 or 64 of them (its query
-// vectors, the rest zero), so a group is 4 or 2 KV heads, and one MMA over
-// the group's tokens serves them all (each row uses its own head's 16
-// columns).  Four consumer warps, one per TMEM lane quadrant; a thread owns
-// one row.
+// 128 rows: each KV head of the CTA's group takes 128 / group of them (its
+// query vectors, the rest zero), and one MMA over the group's tokens serves
+// them all (each row uses its own head's 16 columns).  Four softmax warps,
+// one per TMEM lane quadrant; a thread owns one row.
 constexpr int kTmemWarps = 4;
 constexpr int kTmemRows = 128;
-__host__ __device__ constexpr int tmem_rows_per_head(int vpk) { return vpk <= 32 ? 32 : 64; }
-__host__ __device__ constexpr int tmem_heads(int vpk) { return kTmemRows / tmem_rows_per_head(vpk); }
+// Whether `group` KV heads of `vpk` query vectors each can share the MMA.
+__host__ __device__ constexpr bool tmem_group_ok(int group, int kv_heads, int vpk) {
+  return (group == 1 || group == 2 || group == 4) && kv_heads % group == 0 &&
+         group * vpk <= kTmemRows;
+}
+// The default group: the largest of 4, 2 and 1 that fits.
+__host__ __device__ constexpr int tmem_group(int kv_heads, int vpk) {
+  return tmem_group_ok(4, kv_heads, vpk) ? 4 : tmem_group_ok(2, kv_heads, vpk) ? 2 : 1;
+}
 // Tensor-memory columns a CTA allocates (a power of two, at least 32): the
 // output accumulator (head_dim columns) and two score buffers (16 columns
-// per KV head each).
-__host__ __device__ constexpr int tmem_cols(int head_dim, int vpk) {
-  return head_dim + 2 * tmem_heads(vpk) * kBlock <= 128 ? 128
-         : head_dim + 2 * tmem_heads(vpk) * kBlock <= 256 ? 256
-                                                         : 512;
+// per KV head of the group each).
+__host__ __device__ constexpr int tmem_cols(int head_dim, int group) {
+  return head_dim + 2 * group * kBlock <= 128 ? 128
+         : head_dim + 2 * group * kBlock <= 256 ? 256
+                                               : 512;
 }
 
 // Whether a variant keeps its consumer warps off the producer's SM

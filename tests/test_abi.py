@@ -142,20 +142,22 @@ def test_odd_vector_counts_above_15_run_on_the_tensor_cores(nsv):
     # 32 KV heads split into the TMEM form's groups of 4 (17 vectors each)
     p = nsv.plan_split(_shape(nsv, query_len=17), num_sms=152)
     assert p.consumer == nsv.CONSUMER_TENSOR_TMEM and p.kv_heads_per_cta == 4
-    # 6 KV heads do not: two vectors-as-rows warps per KV head
-    p = nsv.plan_split(_shape(nsv, num_heads=6, num_kv_heads=6, query_len=17), num_sms=152)
+    # 5 KV heads split into no group of 2 or 4: two vectors-as-rows warps per KV head
+    p = nsv.plan_split(_shape(nsv, num_heads=5, num_kv_heads=5, query_len=17), num_sms=152)
     assert p.consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS
     assert p.threads == _cta_warps(nsv, p.consumer, p.kv_heads_per_cta * 2) * 32
 
 
 @pytest.mark.parametrize("heads,kv_heads,qlen,head_dim,group,cps", [
     (32, 8, 8, 128, 4, 1), (64, 8, 8, 128, 2, 2), (32, 8, 1, 128, 4, 1), (32, 8, 9, 128, 2, 2),
-    (8, 8, 17, 128, 4, 1), (32, 8, 8, 64, 4, 2), (64, 8, 8, 64, 2, 2)])
+    (8, 8, 17, 128, 4, 1), (32, 8, 8, 64, 4, 2), (64, 8, 8, 64, 2, 2), (24, 6, 5, 128, 2, 2),
+    (64, 1, 1, 128, 1, 2), (20, 5, 5, 64, 1, 2)])
 def test_plan_tmem_form(nsv, heads, kv_heads, qlen, head_dim, group, cps):
-    """NSV_CONSUMER_TENSOR_TMEM: one 128-row MMA group per CTA (4 KV heads of
-    up to 32 vectors, 2 of up to 64), a producer, four softmax warps and an
-    MMA warp; two CTAs per SM where their shared memory fits, as their 256
-    (head_dim 128) or 128 tensor-memory columns do."""
+    """NSV_CONSUMER_TENSOR_TMEM: one 128-row MMA group per CTA (the largest of
+    4, 2 or 1 KV heads that divides the KV heads and leaves each head rows for
+    its vectors), a producer, four softmax warps and an MMA warp; two CTAs per
+    SM where their shared memory fits, as their 256 (head_dim 128) or 128
+    tensor-memory columns do."""
     p = nsv.plan_custom(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen,
                                head_dim=head_dim),
                         num_sms=152, consumer=nsv.CONSUMER_TENSOR_TMEM)
@@ -183,7 +185,8 @@ def test_plan_vector_rows_form(nsv, qlen, warps):
     (32, 8, 8, "bf16", 4, 4, 6),     # 32 vectors: tcgen05, 4 KV heads of 32 rows
     (32, 8, 5, "bf16", 4, 4, 6),     # 20 vectors
     (64, 8, 8, "bf16", 4, 2, 6),     # 64 vectors: 2 KV heads of 64 rows
-    (24, 6, 5, "bf16", 3, 2, 4),     # 20 vectors, 6 KV heads: no 4-head groups
+    (24, 6, 5, "bf16", 4, 2, 6),     # 20 vectors, 6 KV heads: groups of 2 (64 rows each)
+    (20, 5, 5, "bf16", 3, 1, 2),     # 20 vectors, 5 KV heads: no group of 2 or 4
     (32, 8, 1, "f32", 1, 4, 8),      # fp32 stays on the CUDA cores
 ])
 def test_plan_consumer_choice(nsv, heads, kv_heads, qlen, dtype, consumer, hg, warps):
@@ -207,7 +210,8 @@ def test_plan_consumer_choice(nsv, heads, kv_heads, qlen, dtype, consumer, hg, w
     (dict(num_kv_heads=8, dtype=0), dict(consumer=2)),              # fp32
     (dict(num_kv_heads=8), dict(consumer=5)),                       # no such consumer
     (dict(num_kv_heads=8, dtype=0), dict(consumer=4)),              # fp32
-    (dict(num_heads=24, num_kv_heads=6), dict(consumer=4)),         # 4-head groups do not divide 6
+    (dict(num_heads=24, num_kv_heads=6), dict(consumer=4, kv_heads_per_cta=4)),  # 4 does not divide 6
+    (dict(num_kv_heads=8, query_len=9), dict(consumer=4, kv_heads_per_cta=4)),   # 4 x 36 rows > 128
     (dict(num_kv_heads=8), dict(consumer=4, kv_heads_per_cta=8)),   # its group is 4 heads
     (dict(num_kv_heads=8, dtype=0), dict(consumer=3)),              # fp32
     (dict(num_kv_heads=8, num_blocks=(1 << 24)), dict(consumer=2)), # TMA row index overflows

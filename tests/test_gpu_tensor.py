@@ -45,20 +45,8 @@ def _case(heads, kv_heads, qlen, head_dim, lens=LENS, seed=5, free_frac=0.3):
                     free_frac=free_frac, query_len=qlen)
 
 
-def _tmem_unfit(shape):
-    """The TMEM form groups 4 KV heads (up to 32 vectors each) or 2 (up to 64)."""
-    vpk = shape.num_heads // shape.num_kv_heads * max(1, shape.query_len)
-    return shape.num_kv_heads % (4 if vpk <= 32 else 2) != 0
-
-
 def _plan(nsv, inp, **kw):
-    shape = nsv.shape_of(inp["q"], inp["k_pool"], inp["block_tables"])
-    try:
-        return nsv.plan_custom(shape, **kw)
-    except nsv.NsvError as e:
-        if kw.get("consumer") == nsv.CONSUMER_TENSOR_TMEM and e.code == -5 and _tmem_unfit(shape):
-            pytest.skip("the TMEM form's KV-head groups do not divide this shape's KV heads")
-        raise
+    return nsv.plan_custom(nsv.shape_of(inp["q"], inp["k_pool"], inp["block_tables"]), **kw)
 
 
 @pytest.mark.parametrize("heads,kv_heads,qlen,head_dim", [
