@@ -211,7 +211,7 @@ NSV_API int nsv_plan_split(const nsv_shape *shape, int num_sms, nsv_plan *plan);
 /*
  * The same planner with some choices fixed (any argument <= 0 is chosen by
  * the heuristic): kv_heads_per_cta (must divide num_kv_heads), stages (2..8),
- * ctas_per_sm (1..4), grid (persistent CTAs; default num_sms * ctas_per_sm)
+ * ctas_per_sm (1..8), grid (persistent CTAs; default num_sms * ctas_per_sm)
  * vectors_per_warp (1, 2 or 4, dividing the query vectors per KV head;
  * at most 16 consumer warps for 1 or 2, 8 for 4; CUDA-core consumer only)
  * and consumer (NSV_CONSUMER_*; AUTO picks as the default plan does).

@@ -27,6 +27,8 @@ constexpr int kSmemPerSm = 228 * 1024;     // shared memory per SM on sm_103
 constexpr int kSmemPerCta = 227 * 1024;    // opt-in maximum per CTA
 constexpr int kSmemReserved = 1024;        // per-CTA system reservation
 constexpr int kThreadsPerSm = 2048;
+constexpr int kMaxCtasPerSm = 8;        // resident CTAs per SM a plan may ask for
+constexpr int kEnoughWarpsPerSm = 16;   // consumer warps per SM that keep HBM busy
 
 struct DeviceState {
   bool ready = false;
@@ -177,16 +179,34 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
     else if (!tmem_group_ok(hg, s->num_kv_heads, vpk))
       return NSV_ERR_RANGE;
   } else if (hg <= 0) {
-    // Largest KV-head group whose K+V stage stays within 64 KiB and whose
-    // query vectors fill at most 8 consumer warps: big bulk copies, few CTAs.
-    hg = 1;
-    const int cands[4] = {8, 4, 2, 1};
-    for (int c : cands) {
-      if (s->num_kv_heads % c == 0 && c * wpk <= 8 && 2 * c * tile <= 64 * 1024) {
-        hg = c;
-        break;
+    // Among 1 and the KV-head groups whose K+V stage stays within 64 KiB and
+    // whose query vectors fill at most 8 consumer warps, the one whose plan keeps
+    // the most consumer warps resident per SM, counted up to 16, the larger
+    // group on a tie (big bulk copies, few CTAs).  A consumer warp's chain of
+    // dependent steps per tile, not the bytes in flight, bounds one CTA's
+    // rate once its stages are small: a deeper ring leaves the read time
+    // unchanged, more warps per SM shorten it until HBM is the bound, which
+    // 12 to 16 reach.
+    int best_warps = 0;
+    nsv_plan best{};
+    int best_rc = NSV_ERR_RANGE;
+    for (int c : {8, 4, 2, 1}) {
+      if (c > 1 && (s->num_kv_heads % c != 0 || c * wpk > 8 || 2 * c * tile > 64 * 1024)) continue;
+      nsv_plan cand;
+      const int rc_c = make_plan(s, num_sms, c, stages, cps, grid, qw, consumer, &cand);
+      if (rc_c != NSV_OK) {
+        if (best_warps == 0) best_rc = rc_c;
+        continue;
+      }
+      const int warps = std::min(cand.ctas_per_sm * c * wpk, kEnoughWarpsPerSm);
+      if (warps > best_warps) {
+        best_warps = warps;
+        best = cand;
       }
     }
+    if (best_warps == 0) return best_rc;
+    *p = best;
+    return NSV_OK;
   } else if (s->num_kv_heads % hg != 0 || hg * wpk > max_warps) {
     return NSV_ERR_RANGE;
   }
@@ -241,10 +261,11 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
     fit = kSmemPerSm / (int)(L.total + kSmemReserved);
   }
   if (cps <= 0) {
-    cps = fit < 2 ? fit : 2;
+    // As many as fit: up to 8, or 2 for the TMEM form (measured no further)
+    cps = std::min(fit, tmem_form ? 2 : kMaxCtasPerSm);
     if (cps > fit_threads) cps = fit_threads;
     if (cps < 1) cps = 1;
-  } else if (cps > 4 || cps > fit || cps > fit_threads) {
+  } else if (cps > kMaxCtasPerSm || cps > fit || cps > fit_threads) {
     return NSV_ERR_RANGE;
   }
   if (grid <= 0) {

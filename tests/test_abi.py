@@ -113,7 +113,7 @@ def test_plan_shapes_of_every_workload(nsv):
 
 @pytest.mark.parametrize("heads,kv_heads,qlen,qw,warps", [
     (32, 32, 1, 1, 8), (32, 8, 1, 2, 8), (32, 32, 4, 2, 8), (32, 32, 2, 2, 8),
-    (32, 32, 3, 1, 6), (16, 1, 1, 2, 8), (32, 8, 8, 2, 16), (8, 8, 5, 1, 5),
+    (32, 32, 3, 1, 3), (16, 1, 1, 2, 8), (32, 8, 8, 2, 16), (8, 8, 5, 1, 5),
 ])
 def test_plan_query_vectors(nsv, heads, kv_heads, qlen, qw, warps):
     """On the CUDA cores a consumer warp serves two query vectors by default
@@ -124,6 +124,28 @@ def test_plan_query_vectors(nsv, heads, kv_heads, qlen, qw, warps):
     assert p.consumer == nsv.CONSUMER_CUDA
     assert p.vectors_per_warp == qw
     assert p.threads == (warps + 1) * 32
+
+
+@pytest.mark.parametrize("heads,kv_heads,qlen,head_dim,consumer,group,cps", [
+    (32, 32, 1, 128, 1, 8, 1),   # 64 KiB stages: one CTA of 8 warps per SM
+    (32, 8, 1, 128, 2, 8, 1),
+    (1, 1, 1, 128, 1, 1, 7),     # one KV head: as many small CTAs as fit
+    (2, 2, 1, 128, 1, 2, 4),
+    (16, 4, 1, 128, 2, 2, 3),    # 3 CTAs of 2 warps beat 1 of 4
+    (8, 2, 2, 64, 2, 2, 4),
+    (8, 8, 1, 64, 1, 8, 2),      # 16 warps either way: the larger group
+    (8, 1, 1, 128, 2, 1, 6),
+])
+def test_plan_keeps_consumer_warps_resident(nsv, heads, kv_heads, qlen, head_dim, consumer,
+                                            group, cps):
+    """The default group is the one whose plan keeps the most consumer warps
+    resident per SM (counted up to 16), the larger on a tie, and the default
+    CTAs per SM are as many as fit (up to 8)."""
+    p = nsv.plan_split(_shape(nsv, rows=512, num_blocks=200000, num_heads=heads,
+                              num_kv_heads=kv_heads, query_len=qlen, head_dim=head_dim),
+                       num_sms=152)
+    assert (p.consumer, p.kv_heads_per_cta, p.ctas_per_sm) == (consumer, group, cps)
+    assert p.grid == 152 * cps
 
 
 @pytest.mark.parametrize("heads,kv_heads,qlen,dtype", [
@@ -269,7 +291,8 @@ def test_block_size_refusal(nsv):
 
 
 @pytest.mark.parametrize("kw", [dict(kv_heads_per_cta=3), dict(stages=1), dict(stages=9),
-                                dict(ctas_per_sm=5), dict(kv_heads_per_cta=32, stages=8),
+                                dict(ctas_per_sm=9), dict(kv_heads_per_cta=8, ctas_per_sm=2),
+                                dict(kv_heads_per_cta=32, stages=8),
                                 dict(kv_heads_per_cta=8, stages=4), dict(grid=70000)])
 def test_plan_custom_refusals(nsv, kw):
     with pytest.raises(nsv.NsvError) as e:
