@@ -155,7 +155,8 @@ typedef struct nsv_plan {
                                  that share a KV head) one consumer warp
                                  serves from each K/V tile: 1, 2 or 4
                                  (CUDA-core consumer; 1 for the tensor one) */
-    int32_t consumer;         /* NSV_CONSUMER_CUDA, _TENSOR or _TENSOR_VECTOR_ROWS */
+    int32_t consumer;         /* NSV_CONSUMER_CUDA, _TENSOR, _TENSOR_VECTOR_ROWS
+                                 or _TENSOR_TMEM */
     int32_t reserved;         /* 0 */
     int64_t workspace_bytes;  /* device scratch the read needs */
 } nsv_plan;
@@ -191,7 +192,13 @@ typedef struct nsv_plan {
  * query vectors per KV head, NSV_CONSUMER_TENSOR_VECTOR_ROWS for 9 to 16,
  * NSV_CONSUMER_TENSOR_TMEM for 17 to 64 when its group can be 2 or 4 KV
  * heads (NSV_CONSUMER_TENSOR_VECTOR_ROWS otherwise, for example for an odd
- * num_kv_heads), and the CUDA-core one otherwise. */
+ * num_kv_heads), and the CUDA-core one otherwise.  Outside the TMEM form
+ * the default kv_heads_per_cta is, among 1 and the groups whose K+V stage
+ * is at most 64 KiB and whose vectors need at most 8 consumer warps, the
+ * one whose plan keeps the most consumer warps resident per SM (counted up
+ * to 16; the larger group on a tie), and the default ctas_per_sm is as many
+ * as shared memory, threads and registers allow, up to 8 (2 for the TMEM
+ * form). */
 enum {
     NSV_CONSUMER_AUTO = 0,
     NSV_CONSUMER_CUDA = 1,

@@ -128,6 +128,7 @@ MEDIUM_LENS = [1, 0, 17, 256, 1000, 333, 16, 15, 1024, 47]
     dict(kv_heads_per_cta=1),
     dict(kv_heads_per_cta=2, ctas_per_sm=2),
     dict(kv_heads_per_cta=4, ctas_per_sm=1, grid=100),
+    dict(kv_heads_per_cta=1, ctas_per_sm=4),  # four small CTAs per SM
 ])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_plan_variants(nsv, kw, dtype):
@@ -139,6 +140,27 @@ def test_plan_variants(nsv, kw, dtype):
     out = gpu_read(wl, inp, plan=plan)
     assert status()[0] == 0
     assert_parity(dtype, gpu_out_f64(out), oracle_read(wl, host))
+
+
+@pytest.mark.parametrize("kw", [
+    dict(kv_heads_per_cta=1, ctas_per_sm=8),
+    dict(kv_heads_per_cta=1, ctas_per_sm=7, stages=2),
+    dict(kv_heads_per_cta=2, ctas_per_sm=3),
+    dict(consumer=2, kv_heads_per_cta=1, ctas_per_sm=6),
+])
+def test_many_small_ctas_per_sm(nsv, kw):
+    """Plans with up to 8 resident CTAs per SM (small stages, one or two KV
+    heads per CTA) read as the oracle does; with 2 query heads per KV head
+    the tensor-core consumer is covered too."""
+    wl = _custom("many_ctas", MEDIUM_LENS, heads=16 if kw.get("consumer") else 8)
+    inp = device_inputs(wl)
+    host = host_copy(inp)
+    shape = nsv.shape_of(inp["q"], inp["k_pool"], inp["block_tables"])
+    plan = nsv.plan_custom(shape, **kw)
+    assert plan.ctas_per_sm == kw["ctas_per_sm"]
+    out = gpu_read(wl, inp, plan=plan)
+    assert status()[0] == 0
+    assert_parity("bf16", gpu_out_f64(out), oracle_read(wl, host))
 
 
 @pytest.mark.parametrize("dtype,head_dim", [("bf16", 64), ("f32", 64), ("f32", 128)])
