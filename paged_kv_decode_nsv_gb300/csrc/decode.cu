@@ -1428,7 +1428,7 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
     __maxnreg__(decode_regs(MMA == kMmaTokenRows    ? kConsumerTensor
                             : MMA == kMmaVectorRows ? kConsumerTensorVectorRows
                             : MMA == kMmaTmem       ? kConsumerTensorTmem
-                                                    : kConsumerCuda, QW))
+                                                    : kConsumerCuda, QW, D))
     decode_kernel(const __grid_constant__ DecodeParams p) {
   using E = Elem<T>;
   constexpr int kDpl = E::kDpl;           // dims per lane per 16-byte load

@@ -227,7 +227,7 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   int fit = kSmemPerSm / (int)(L.total + kSmemReserved);
   // CTAs one SM holds by threads and by registers (each kernel variant's
   // register count is fixed at compile time)
-  const int regs = decode_regs(consumer, qw);
+  const int regs = decode_regs(consumer, qw, s->head_dim);
   int fit_threads = std::min(kThreadsPerSm / threads, ctas_by_registers(threads, regs));
   // The TMEM form's CTAs also share the SM's 512 tensor-memory columns.
   // (The device's occupancy calculator answers one CTA per SM for a kernel

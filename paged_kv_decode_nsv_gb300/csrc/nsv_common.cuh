@@ -40,15 +40,21 @@ constexpr int kMaxThreadsMulti = (kMaxConsumerWarpsMulti + 1) * 32;
 // (__maxnreg__) so that the planner can size the grid to the CTAs that are
 // really resident: CUDA-core consumer with 1 or 2 vectors per warp (96: a
 // 17-warp CTA fits, 5 warps of it per sub-partition, and two 9-warp CTAs
-// do), and every other variant (4 vectors per warp, both tensor-core forms,
-// at most 9 warps a CTA).
+// do), the two mma.sync forms at head_dim 64 (what they use without
+// spilling: 112 with tokens as rows, 128 with vectors as rows, which lets
+// 4 warps share a sub-partition instead of 3), and every other variant
+// (4 vectors per warp, the mma.sync forms at head_dim 128, the TMEM form).
 constexpr int kRegsNarrow = 96;
 constexpr int kRegsWide = 168;
 constexpr int kRegsTmem = 168;
-__host__ __device__ constexpr int decode_regs(int consumer, int qw) {
-  return consumer == kConsumerTensorTmem                ? kRegsTmem
-         : (consumer == kConsumerCuda && qw <= 2) ? kRegsNarrow
-                                                  : kRegsWide;
+constexpr int kRegsTokenRows64 = 112;
+constexpr int kRegsVectorRows64 = 128;
+__host__ __device__ constexpr int decode_regs(int consumer, int qw, int head_dim) {
+  return consumer == kConsumerTensorTmem                      ? kRegsTmem
+         : (consumer == kConsumerCuda && qw <= 2)             ? kRegsNarrow
+         : (consumer == kConsumerTensor && head_dim == 64)    ? kRegsTokenRows64
+         : (consumer == kConsumerTensorVectorRows && head_dim == 64) ? kRegsVectorRows64
+                                                              : kRegsWide;
 }
 // CTAs of `threads` threads at `regs` registers each that one SM's
 // registers hold: 4 sub-partitions of 16 K registers, each holding whole

@@ -132,7 +132,7 @@ def test_plan_query_vectors(nsv, heads, kv_heads, qlen, qw, warps):
     (1, 1, 1, 128, 1, 1, 7),     # one KV head: as many small CTAs as fit
     (2, 2, 1, 128, 1, 2, 4),
     (16, 4, 1, 128, 2, 2, 3),    # 3 CTAs of 2 warps beat 1 of 4
-    (8, 2, 2, 64, 2, 2, 4),
+    (8, 2, 2, 64, 2, 2, 5),      # head_dim 64 tokens-as-rows warps fit 4 per sub-partition
     (8, 8, 1, 64, 1, 8, 2),      # 16 warps either way: the larger group
     (8, 1, 1, 128, 2, 1, 6),
 ])
