@@ -247,6 +247,26 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
     }
   }
   if (fit_threads < 1) return NSV_ERR_RANGE;  // one CTA would not fit the register file
+  if (!tensor && auto_stages && cps <= 0 && stages == 3 && hg == s->num_kv_heads &&
+      2 * hg * tile <= 16 * 1024) {
+    // CUDA-core consumer whose CTA streams every KV head (one or two of
+    // them) in stages of at most 16 KiB: where shared memory alone holds the
+    // CTAs per SM below what registers allow and their consumer warps stay
+    // under 16, a 2-stage ring that fits more CTAs reads faster (one KV head
+    // of one query head: 7 CTAs of 3 stages 222 us, 8 of 2 stages 206 us on
+    // GB300).  The tensor-core forms lost 4-14 % with 2 stages, so they keep
+    // 3, and so do shapes with more KV heads, whose larger groups were not
+    // measured against it.
+    const int warps_cta = threads / 32 - 1;
+    const int now = std::min({fit, fit_threads, kMaxCtasPerSm});
+    const SmemLayout L2 = make_layout(elem, s->head_dim, hg, nvec, 2, rows_for_layout, form, qw);
+    const int fit2 = kSmemPerSm / (int)(L2.total + kSmemReserved);
+    if (now * warps_cta < kEnoughWarpsPerSm && std::min({fit2, fit_threads, kMaxCtasPerSm}) > now) {
+      stages = 2;
+      L = L2;
+      fit = fit2;
+    }
+  }
   if (tensor && auto_stages && cps <= 0 && std::min(fit, fit_threads) < 2) {
     // One CTA per SM either way: spend the rest of its shared memory on a
     // deeper ring (up to 6 stages), which keeps more bytes in flight for

@@ -129,8 +129,8 @@ def test_plan_query_vectors(nsv, heads, kv_heads, qlen, qw, warps):
 @pytest.mark.parametrize("heads,kv_heads,qlen,head_dim,consumer,group,cps", [
     (32, 32, 1, 128, 1, 8, 1),   # 64 KiB stages: one CTA of 8 warps per SM
     (32, 8, 1, 128, 2, 8, 1),
-    (1, 1, 1, 128, 1, 1, 7),     # one KV head: as many small CTAs as fit
-    (2, 2, 1, 128, 1, 2, 4),
+    (1, 1, 1, 128, 1, 1, 8),     # one KV head: as many small CTAs as fit (2 stages)
+    (2, 2, 1, 128, 1, 2, 5),
     (16, 4, 1, 128, 2, 2, 3),    # 3 CTAs of 2 warps beat 1 of 4
     (8, 2, 2, 64, 2, 2, 5),      # head_dim 64 tokens-as-rows warps fit 4 per sub-partition
     (8, 8, 1, 64, 1, 8, 2),      # 16 warps either way: the larger group
@@ -146,6 +146,20 @@ def test_plan_keeps_consumer_warps_resident(nsv, heads, kv_heads, qlen, head_dim
                        num_sms=152)
     assert (p.consumer, p.kv_heads_per_cta, p.ctas_per_sm) == (consumer, group, cps)
     assert p.grid == 152 * cps
+
+
+@pytest.mark.parametrize("heads,kv_heads,head_dim,stages,cps", [
+    (1, 1, 128, 2, 8), (2, 2, 128, 2, 5),   # every KV head in one small-stage CTA
+    (4, 4, 128, 3, 2),                      # 32 KiB stages keep 3
+    (32, 32, 128, 3, 1),                    # a group of 8 out of 32 keeps 3
+])
+def test_cuda_core_small_stage_ring(nsv, heads, kv_heads, head_dim, stages, cps):
+    """A CUDA-core CTA that streams every KV head in stages of at most 16 KiB
+    takes a 2-stage ring where that fits more CTAs per SM."""
+    p = nsv.plan_split(_shape(nsv, rows=512, num_blocks=200000, num_heads=heads,
+                              num_kv_heads=kv_heads, head_dim=head_dim), num_sms=152)
+    assert p.consumer == nsv.CONSUMER_CUDA
+    assert (p.stages, p.ctas_per_sm) == (stages, cps)
 
 
 @pytest.mark.parametrize("heads,kv_heads,qlen,dtype", [
