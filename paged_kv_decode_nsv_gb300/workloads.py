@@ -272,6 +272,17 @@ def manyrow_gqa4_bf16(seed=3):
                  block_size=16, max_blocks=128, dtype="bf16", lens=lens, free_frac=0.10, rng=rng)
 
 
+def headline_mqa8_bf16(seed=4):
+    """The headline batch as one tensor-parallel shard of a grouped-query
+    model: 8 query heads share the shard's single KV head; same lengths and
+    pool recipe.  Its stages are small (one KV head of one block, 8 KiB), so
+    the read is bound by how many consumer warps an SM keeps resident."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(512, 8192, size=256, endpoint=True)
+    return _make("headline_mqa8_bf16", seed, rows=256, heads=8, kv_heads=1, head_dim=128,
+                 block_size=16, max_blocks=512, dtype="bf16", lens=lens, rng=rng)
+
+
 WORKLOADS = {
     "tiny_f32": tiny_f32,
     "uniform_f32": uniform_f32,
@@ -283,6 +294,7 @@ WORKLOADS = {
     "manyrow_gqa4_bf16": manyrow_gqa4_bf16,
     "headline_gqa8_spec8_bf16": headline_gqa8_spec8_bf16,
     "manyrow_gqa8_spec8_bf16": manyrow_gqa8_spec8_bf16,
+    "headline_mqa8_bf16": headline_mqa8_bf16,
 }
 
 

@@ -98,7 +98,7 @@ def test_plan_shapes_of_every_workload(nsv):
         assert p.grid == 152 * p.ctas_per_sm
         assert p.smem_bytes <= 227 * 1024
         nvec = p.kv_heads_per_cta * (wl.heads // wl.kv_heads) * wl.query_len
-        assert 0 < p.workspace_bytes < 152 * 4 * 2 * nvec * (wl.head_dim * 4 + 8) + (1 << 16)
+        assert 0 < p.workspace_bytes < p.grid * 2 * nvec * (wl.head_dim * 4 + 8) + (1 << 16)
         assert wl.kv_heads % p.kv_heads_per_cta == 0
         vpk = (wl.heads // wl.kv_heads) * wl.query_len
         if p.consumer != nsv.CONSUMER_CUDA:  # one warp per 8 or per 16 vectors of a KV head

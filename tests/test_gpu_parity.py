@@ -430,12 +430,13 @@ def test_multi_query_plans(nsv, kw):
 
 
 @pytest.mark.parametrize("name", ["headline_spec4_bf16", "headline_gqa4_bf16",
-                                  "headline_gqa8_spec8_bf16"])
+                                  "headline_gqa8_spec8_bf16", "headline_mqa8_bf16"])
 def test_headline_variants_sampled(nsv, name):
     """Full-size headline batches with 4 query tokens per row, with 4 query
-    heads per KV head, and with both grouped heads and speculative tokens (64
-    query vectors per KV head, tcgen05), in the benchmark's default plan;
-    sampled rows."""
+    heads per KV head, with both grouped heads and speculative tokens (64
+    query vectors per KV head, tcgen05), and with 8 query heads on a single
+    KV head (six small CTAs per SM), in the benchmark's default plan; sampled
+    rows."""
     wl = W.WORKLOADS[name]()
     inp = device_inputs(wl)
     ctx = wl.context_lens
