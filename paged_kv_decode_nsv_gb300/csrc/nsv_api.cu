@@ -191,7 +191,8 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
     nsv_plan best{};
     int best_rc = NSV_ERR_RANGE;
     for (int c : {8, 4, 2, 1}) {
-      if (c > 1 && (s->num_kv_heads % c != 0 || c * wpk > 8 || 2 * c * tile > 64 * 1024)) continue;
+      if (c > 1 && (s->num_kv_heads % c != 0 || c * wpk > 8 || 2 * c * tile > 64 * 1024))
+        continue;
       nsv_plan cand;
       const int rc_c = make_plan(s, num_sms, c, stages, cps, grid, qw, consumer, &cand);
       if (rc_c != NSV_OK) {
@@ -261,7 +262,8 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
     const int now = std::min({fit, fit_threads, kMaxCtasPerSm});
     const SmemLayout L2 = make_layout(elem, s->head_dim, hg, nvec, 2, rows_for_layout, form, qw);
     const int fit2 = kSmemPerSm / (int)(L2.total + kSmemReserved);
-    if (now * warps_cta < kEnoughWarpsPerSm && std::min({fit2, fit_threads, kMaxCtasPerSm}) > now) {
+    if (now * warps_cta < kEnoughWarpsPerSm &&
+        std::min({fit2, fit_threads, kMaxCtasPerSm}) > now) {
       stages = 2;
       L = L2;
       fit = fit2;
