@@ -385,13 +385,15 @@ def test_every_plan_round_trips(nsv):
     for dtype in (nsv.F32, nsv.BF16):
         for heads, kv, ql in [(32, 32, 1), (32, 8, 1), (32, 32, 4), (32, 8, 8), (128, 8, 1),
                               (16, 16, 17), (8, 8, 3), (16, 1, 2), (8, 2, 16), (64, 8, 8),
-                              (64, 1, 1), (32, 32, 64)]:
+                              (64, 1, 1), (32, 32, 64), (1, 1, 1), (2, 2, 1), (8, 1, 1),
+                              (24, 6, 5), (20, 5, 5)]:
             for d in (64, 128):
                 shape = nsv.make_shape(num_heads=heads, num_kv_heads=kv, query_len=ql,
                                        dtype=dtype, head_dim=d, **base)
                 for extra in (dict(), dict(consumer=1), dict(consumer=2), dict(consumer=3),
                               dict(consumer=1, vectors_per_warp=4), dict(kv_heads_per_cta=1),
-                              dict(kv_heads_per_cta=2, ctas_per_sm=2), dict(stages=2)):
+                              dict(kv_heads_per_cta=2, ctas_per_sm=2), dict(stages=2),
+                              dict(consumer=4), dict(consumer=4, kv_heads_per_cta=1)):
                     try:
                         p = nsv.plan_custom(shape, num_sms=152, **extra)
                     except nsv.NsvError:
