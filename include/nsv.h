@@ -198,7 +198,10 @@ typedef struct nsv_plan {
  * one whose plan keeps the most consumer warps resident per SM (counted up
  * to 16; the larger group on a tie), and the default ctas_per_sm is as many
  * as shared memory, threads and registers allow, up to 8 (2 for the TMEM
- * form). */
+ * form).  The default ring is 3 stages; a tensor-core CTA alone on its SM
+ * deepens it to fill shared memory (up to 6), and a CUDA-core CTA that
+ * streams all of one or two KV heads in stages of at most 16 KiB takes 2
+ * where that fits more CTAs per SM. */
 enum {
     NSV_CONSUMER_AUTO = 0,
     NSV_CONSUMER_CUDA = 1,
