@@ -137,11 +137,13 @@ def pin_brute_force(orc):
 
 
 def pin_gqa_brute_force(orc):
-    cs = small_case(7, "f32", rows=3, heads=8, kv_heads=2, head_dim=8, block_size=4,
-                    lens=[5, 13, 9])
-    got = _decode(orc, cs)
-    ref = brute_force(cs["q"], cs["k"], cs["v"], cs["bt"], cs["ctx"], cs["scale"], cs["B"])
-    assert np.max(np.abs(got - ref)) <= 1e-12
+    # 4 query heads per KV head, and every query head on a single KV head
+    for seed, heads, kv_heads in ((7, 8, 2), (8, 8, 1)):
+        cs = small_case(seed, "f32", rows=3, heads=heads, kv_heads=kv_heads, head_dim=8,
+                        block_size=4, lens=[5, 13, 9])
+        got = _decode(orc, cs)
+        ref = brute_force(cs["q"], cs["k"], cs["v"], cs["bt"], cs["ctx"], cs["scale"], cs["B"])
+        assert np.max(np.abs(got - ref)) <= 1e-12, (heads, kv_heads)
 
 
 def _mq_case(seed, nq, dtype="f32", lens=None, heads=2, kv_heads=2):
