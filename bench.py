@@ -3,10 +3,12 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl nsv|reference]
                     [--workload headline_bf16]
 
-Prints ONE JSON line (rank 0).  A step is the whole hot path over one batch:
-nsv_kv_write then the decode read (one kernel), on the
-headline workload by default (256 rows, 32 heads, head_dim 128, block 16,
-width 8192, lengths uniform in [512, 8192], bf16, seeded synthetic data).
+Prints ONE JSON line (rank 0).  A step is the whole hot path over one batch,
+through the fused entry point nsv_decode_step: the KV append (one kernel,
+which also zeroes the read's merge counters) then the decode read (one
+kernel, launched programmatically dependent on the append), on the headline
+workload by default (256 rows, 32 heads, head_dim 128, block 16, width 8192,
+lengths uniform in [512, 8192], bf16, seeded synthetic data).
 
 value     = algorithmic bytes of a step (unique K+V read + q + out + the
             append's read and write) x ranks / max-over-ranks seconds per
@@ -18,10 +20,14 @@ e2e       = the same metric through the C ABI with the step's inputs in
             in one staging buffer, one copy) and the output device->host
             inside the timed region (the KV pool is the resident cache and
             stays on the device).
-roofline  = the decode read alone: read bytes (K+V + q + out) / its
-            CUDA-event time, against the measured HBM copy bandwidth in
-            MEASURED_PEAKS.json.  Workloads smaller than 4x L2 flush L2
-            (a 256 MB write) before every step, outside the timed spans.
+roofline  = the decode read alone, timed in a separate loop of
+            nsv_paged_decode_ws calls (a 4 KiB counter memset + the kernel,
+            each between its own CUDA events): read bytes (K+V + q + out) /
+            its time, against the measured HBM copy bandwidth in
+            MEASURED_PEAKS.json (a read+write copy, which a read-only
+            stream such as this one can exceed).  Workloads smaller than 4x L2
+            flush L2 (a 256 MB write) before every step and every read,
+            outside the timed spans.
 cpu_baseline = the oracle (plain C, fp64) timed on this host's cores on a
             time-bounded sample of rows of the same workload.
 
@@ -294,7 +300,10 @@ def run_nsv(args, wl):
     shape = nsv.shape_of(q, kp, bt)
     plan = nsv.plan_split(shape)
     wsp = nsv.workspace_for(plan)
-    launches_per_step = 2  # kv_write_kernel, decode_kernel (plus one counter memset)
+    # nsv_decode_step launches two kernels per step: kv_write_kernel (which
+    # also zeroes the read's merge counters) and decode_kernel, the read
+    # launched programmatically dependent on the append.  No memset.
+    launches_per_step = 2
     small_l2 = wl.step_bytes() <= 4 * 129e6
     # L2 flush for small workloads: write a buffer larger than L2, then read
     # another one, so that L2 holds clean lines and no write-back of the
@@ -302,22 +311,35 @@ def run_nsv(args, wl):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if small_l2 else None
     flush_rd = torch.ones(32 << 20, dtype=torch.int64, device="cuda") if small_l2 else None
 
-    def step(ev_s=None, ev_a=None, ev_b=None):
+    def flush_l2():
         if flush is not None:
             flush.zero_()
             flush_rd.sum()
+
+    def step(ev_s=None, ev_e=None):
+        """One serving step through the fused entry point (the timed unit)."""
+        flush_l2()
         if ev_s is not None:
             ev_s.record(stream)
-        nsv.kv_write(kn, vn, slots, kp, vp)
-        if ev_a is not None:
-            ev_a.record(stream)
+        nsv.decode_step(q, kn, vn, slots, kp, vp, bt, ctx, wl.scale, out, workspace=wsp,
+                        plan=plan)
+        if ev_e is not None:
+            ev_e.record(stream)
+
+    def read(ev_s=None, ev_e=None):
+        """The decode read alone (its counter memset and its kernel), for the
+        roofline of the dominant kernel."""
+        flush_l2()
+        if ev_s is not None:
+            ev_s.record(stream)
         nsv.paged_decode_ws(q, kp, vp, bt, ctx, wl.scale, out, workspace=wsp, plan=plan)
-        if ev_b is not None:
-            ev_b.record(stream)
+        if ev_e is not None:
+            ev_e.record(stream)
 
     nsv.device_status(clear=True)
     for _ in range(max(3, args.warmup)):
         step()
+        read()
     torch.cuda.synchronize()
     st, _ = nsv.device_status(clear=True)
     if st:
@@ -333,23 +355,36 @@ def run_nsv(args, wl):
     sampler.start()
 
     K = args.steps
-    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
+    # The timed region: K fused steps.  Without a flush the events bracket
+    # the whole loop; with one, each step has its own pair and the flushes
+    # sit between the timed spans.
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2)) for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
     start.record(stream)
     for k in range(K):
-        step(*ev[k])
+        if flush is None:
+            step()
+        else:
+            step(*ev[k])
     end.record(stream)
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     if flush is None:
         total_ms = start.elapsed_time(end)
-    else:  # the flushes sit between the timed spans
-        total_ms = sum(s0.elapsed_time(b) for s0, _, b in ev)
-    read_ms = [a.elapsed_time(b) for _, a, b in ev]
+    else:
+        total_ms = sum(a.elapsed_time(b) for a, b in ev)
+
+    # The read alone, each launch between its own pair of events on the
+    # launching stream (the roofline's kernel time).
+    rev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2)) for _ in range(K)]
+    for k in range(K):
+        read(*rev[k])
+    torch.cuda.synchronize()
+    read_ms = [a.elapsed_time(b) for a, b in rev]
 
     # end to end through the C ABI from pinned host buffers.  The step's
     # inputs are packed into one pinned staging buffer and copied to one
@@ -422,7 +457,9 @@ def run_nsv(args, wl):
         "data": "synthetic (seeded N(0,1) values, seeded lengths and block permutation)",
         "config": dict(workload_config(wl), plan=plan.as_dict()),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
+                     "frac": achieved / peak,
+                     "peak_source": (peak_kind + " (MEASURED_PEAKS.json hbm_gbs: a read+write "
+                                     "copy's bandwidth; a read-only stream can exceed it)")
                      if peak_kind == "measured" else "fallback",
                      "kernel": "decode read (decode_kernel, %s consumer)"
                                % {1: "CUDA-core", 2: "tensor-core",
@@ -433,6 +470,9 @@ def run_nsv(args, wl):
         "e2e": {"value": whole_job_gbs(step_bytes, ws, e2e_ms), "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": K * launches_per_step,
+        "gpu_launches_note": "timed region = K nsv_decode_step calls: kv_write_kernel + "
+                             "decode_kernel each; the roofline's read-only loop is timed "
+                             "separately (a 4 KiB counter memset + decode_kernel per launch)",
         "clocks": clocks,
     }
     if cpu is not None:

@@ -29,6 +29,12 @@
  * be device memory of the current CUDA device.  All calls are asynchronous
  * on the given stream unless stated otherwise.
  *
+ * Per-device state: on its first call on a device the library looks up the
+ * device addresses of its status word and scratch buffers and sets kernel
+ * attributes; it redoes this when it finds a different CUDA context current
+ * on that device (after cudaDeviceReset, say).  The library-owned workspace
+ * of the old context is dropped with it, not freed (its context is gone).
+ *
  * Layouts (all C-contiguous, no strides; element type from nsv_shape.dtype):
  *   q, out          [rows][query_len][num_heads][head_dim]
  *   k_pool, v_pool  [num_blocks + 1][num_kv_heads][block_size][head_dim]
@@ -215,12 +221,27 @@ enum {
  * current device's count).  Host-only apart from that optional device query;
  * deterministic; depends on the shape alone.  Returns NSV_OK or
  * NSV_ERR_{NULLPTR, DTYPE, SHAPE, UNSUPPORTED, CUDA}.
+ *
+ * Why the shape alone: the streamed read's saving over the rectangle is a
+ * property of the width axis only, rows and heads cancelling out of it
+ * (Day 59, "Why it matters", first paragraph), and a read that accumulates
+ * tile by tile has no width to specialise on, so the shapes a server
+ * presents are its batch sizes (Day 59, "What I learned" item 7).  A step
+ * recorded into a CUDA graph is bound to what it was launched with, and it
+ * is recorded on a batch whose rows are all padding (Day 55, "the capture
+ * list moved to startup, and the dummy batch was all padding", "Why it
+ * matters"): a plan chosen from the lengths would differ between that warm
+ * batch and the real ones.  How the work is split (stream-K over a
+ * persistent grid, with the pieces of a cut row merged flash-decoding
+ * style) is this library's design; the pages' kernel runs one program per
+ * (row, query head).
  */
 NSV_API int nsv_plan_split(const nsv_shape *shape, int num_sms, nsv_plan *plan);
 
 /*
- * The same planner with some choices fixed (any argument <= 0 is chosen by
- * the heuristic): kv_heads_per_cta (must divide num_kv_heads), stages (2..8),
+ * The same planner with some choices fixed, for sweeps and tests (the pages
+ * have no counterpart; every plan it returns is one the read runs
+ * correctly).  Any argument <= 0 is chosen by the heuristic: kv_heads_per_cta (must divide num_kv_heads), stages (2..8),
  * ctas_per_sm (1..8), grid (persistent CTAs; default num_sms * ctas_per_sm)
  * vectors_per_warp (1, 2 or 4, dividing the query vectors per KV head;
  * at most 16 consumer warps for 1 or 2, 8 for 4; CUDA-core consumer only)
@@ -281,6 +302,17 @@ NSV_API int nsv_paged_decode(const nsv_shape *shape, const void *q, const void *
  * `stream` before its kernel.  Two calls that overlap on the GPU need two
  * workspaces.  A plan passed in must be one nsv_plan_split/nsv_plan_custom
  * returned for this shape (NSV_ERR_RANGE otherwise).
+ *
+ * The workspace is the read's only intermediate in device memory: one
+ * arrival counter per (row, KV-head group) and, per CTA, at most two partial
+ * softmax states (running max, denominator, weighted sum of V) of the query
+ * vectors it serves.  It stands where the gather read's [rows, heads, 1,
+ * width] score rectangle stood (Day 59, "What I added today": 268.4 MB at
+ * 256 rows, 32 heads and width 8192, against one tile and three
+ * accumulators for the streamed read), and it is sized by the grid, not by
+ * rows x width (1.27 MB at that shape).  A workspace at a fixed caller
+ * address is what a captured step replays against (Day 55, "Why it
+ * matters": a graph is bound to the addresses it was launched with).
  */
 NSV_API int nsv_paged_decode_ws(const nsv_shape *shape, const nsv_plan *plan,
                                 const void *q, const void *k_pool, const void *v_pool,
@@ -290,8 +322,11 @@ NSV_API int nsv_paged_decode_ws(const nsv_shape *shape, const nsv_plan *plan,
 
 /*
  * One serving step: nsv_kv_write then the decode read on the same stream.
- * context_lens already count the appended token (its write slot is the
- * row's last real position).  plan/workspace as in nsv_paged_decode_ws;
+ * context_lens already count the appended token: the write slot is the
+ * row's last real entry (Day 51, "the read rectangle stopped being built",
+ * "What I learned" item 2), so the read must see what the append wrote, and
+ * a padded row writes the sink slot and reads nothing (Day 55, "Why it
+ * matters").  plan/workspace as in nsv_paged_decode_ws;
  * workspace NULL with workspace_bytes 0 uses the library-owned workspace.
  * Both halves' arguments are checked before either is launched: on an
  * error return nothing was launched.  The append's launch also zeroes the
@@ -320,7 +355,9 @@ NSV_API int nsv_decode_step(const nsv_shape *shape, const nsv_plan *plan, const 
  * a device looks up the buffer's device address (cudaGetSymbolAddress, no
  * allocation); make that first call before any stream capture.  Calls share
  * the buffer: two calls whose kernels overlap on the GPU race on it.  The
- * buffer needs no clearing between calls.
+ * caller never clears it: the part that must start at zero (the read's
+ * arrival counters) is zeroed by each call with a cudaMemsetAsync on
+ * `stream`, and each call writes the rest before reading it.
  */
 #define NSV_NOALLOC_SCRATCH_BYTES (4u << 20)
 
@@ -362,10 +399,13 @@ NSV_API int nsv_paged_decode_slots(const nsv_shape *shape, const nsv_plan *plan,
  * that gives up sets NSV_DEV_TIMEOUT and the kernel returns, leaving the
  * context usable.  This call runs that same wait routine in a one-thread
  * kernel, with limit_ns (1 us .. 2 s), on an mbarrier phase that nothing
- * completes, so it must give up.  Synchronous on `stream`; touches neither
- * the device status word nor any caller memory.  On NSV_OK, *gave_up is 1
- * when the wait gave up (the expected outcome) and *waited_ns is how long it
- * waited.  Returns NSV_ERR_{NULLPTR, RANGE, CUDA}.
+ * completes, so it must give up; when it does, it sets NSV_DEV_TIMEOUT in
+ * the device status word exactly as a decode kernel's wait would, so the
+ * whole signalling path (nsv_device_status, nsv_status_async) can be
+ * checked without a fault.  Synchronous on `stream`; touches no caller
+ * memory.  On NSV_OK, *gave_up is 1 when the wait gave up (the expected
+ * outcome) and *waited_ns is how long it waited.  Returns
+ * NSV_ERR_{NULLPTR, RANGE, CUDA}.
  */
 NSV_API int nsv_selftest_bounded_wait(uint64_t limit_ns, int *gave_up, uint64_t *waited_ns,
                                       cudaStream_t stream);
@@ -379,13 +419,31 @@ NSV_API int nsv_selftest_bounded_wait(uint64_t limit_ns, int *gave_up, uint64_t 
  */
 NSV_API int nsv_device_status(uint32_t *status, uint64_t *blocks_walked, int clear);
 
+/*
+ * The status word without a device-wide synchronisation, for a serving loop
+ * that must learn of NSV_DEV_TIMEOUT or a flagged bad value before it uses a
+ * step's output (the pages have no counterpart: Day 59, "What I added
+ * today", has the kernel make every refusal the oracle makes, and this is
+ * how a caller hears of one).  Enqueues on `stream` a 4-byte copy of the
+ * current device's status word into `dst`, which is device memory or
+ * page-locked host memory of at least 4 bytes, 4-byte aligned, owned by the
+ * caller; with clear != 0 it then zeroes the status word, also on `stream`.
+ * Nothing waits: `dst` holds the bits raised by all work ordered before the
+ * copy once `stream` reaches it (for pinned host memory, after the caller
+ * synchronises `stream` or an event recorded after this call).  The status
+ * word is one per device and sticky: bits raised by work on other streams
+ * show up too, and a clear can drop a bit that such work raises between the
+ * copy and the clear.  Returns NSV_ERR_{NULLPTR, ALIGN, CUDA}.
+ */
+NSV_API int nsv_status_async(uint32_t *dst, int clear, cudaStream_t stream);
+
 /* Static description of a return code. */
 NSV_API const char *nsv_strerror(int code);
 
 /* ABI version of this header (major * 100 + minor). */
 NSV_API int nsv_abi_version(void);
 
-#define NSV_ABI_VERSION 101
+#define NSV_ABI_VERSION 102
 
 #ifdef __cplusplus
 }

@@ -144,8 +144,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 
 // Self-test of the bounded wait: one thread waits, with limit_ns, for a
 // phase of a fresh mbarrier that nothing completes.  result[0] = 1 when the
-// wait gave up, result[1] = the nanoseconds it waited.
-__global__ void bounded_wait_probe(unsigned long long limit_ns, unsigned long long* result) {
+// wait gave up, result[1] = the nanoseconds it waited; a wait that gave up
+// sets NSV_DEV_TIMEOUT in *status, as the decode kernel's waits do.
+__global__ void bounded_wait_probe(unsigned long long limit_ns, unsigned long long* result,
+                                   uint32_t* status) {
   __shared__ __align__(8) unsigned long long bar_word;
   if (threadIdx.x != 0) return;
   const uint32_t bar = smem_u32(&bar_word);
@@ -155,6 +157,7 @@ __global__ void bounded_wait_probe(unsigned long long limit_ns, unsigned long lo
   const bool completed = mbar_wait_slow(bar, 0, limit_ns);
   result[1] = global_ns() - t0;
   result[0] = completed ? 0ull : 1ull;
+  if (!completed) atomicOr(status, (uint32_t)NSV_DEV_TIMEOUT);
 }
 
 // Programmatic dependent launch: wait until the grid this launch depends on
@@ -2086,8 +2089,8 @@ cudaError_t decode_occupancy(int dtype, int head_dim, int qw, int consumer, int 
 }
 
 cudaError_t launch_wait_probe(unsigned long long limit_ns, unsigned long long* result,
-                              cudaStream_t stream) {
-  bounded_wait_probe<<<1, 32, 0, stream>>>(limit_ns, result);
+                              uint32_t* status, cudaStream_t stream) {
+  bounded_wait_probe<<<1, 32, 0, stream>>>(limit_ns, result, status);
   return cudaGetLastError();
 }
 

@@ -15,11 +15,17 @@
 // library holds NSV_NOALLOC_SCRATCH_BYTES of it until the process exits.
 // Host code cannot use the array's name as a device pointer; its device
 // address is looked up with cudaGetSymbolAddress once per device (on the
-// first call made with that device current) and cached.
+// first call made with that device current) and cached, and looked up again
+// if a different CUDA context has become current on the device since.
 //
-// All calls on one device share the buffer.  Nothing in it has to start at
-// zero: each call writes every partial it later reads.  Calls whose kernels
-// overlap on the GPU (different streams, no ordering) race on it.
+// All calls on one device share the buffer.  Its first part holds the read's
+// arrival counters (one per row and KV-head group), which must be zero when
+// the kernel starts: nsv_paged_decode_ws clears them with a cudaMemsetAsync
+// on the caller's stream before every launch (no allocation).  Everything
+// else in it (the partial softmax states of rows cut between CTAs) each call
+// writes before it reads it.  So a caller never clears the buffer, whatever
+// an earlier call left there; but calls whose kernels overlap on the GPU
+// (different streams, no ordering between them) race on it.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -36,6 +42,7 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 void* g_scratch_addr[kMaxDevices];
+void* g_scratch_ctx[kMaxDevices];  // the context each address belongs to
 std::mutex g_scratch_mu;
 
 // Device address of the scratch array on the current device.
@@ -47,6 +54,10 @@ int scratch_address(void** out) {
   }
   if (dev < 0 || dev >= kMaxDevices) return NSV_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_addr[dev] != nullptr) {
+    void* now = nsv::current_cuda_context();
+    if (now != nullptr && now != g_scratch_ctx[dev]) g_scratch_addr[dev] = nullptr;
+  }
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
@@ -54,6 +65,7 @@ int scratch_address(void** out) {
       return NSV_ERR_CUDA;
     }
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = nsv::current_cuda_context();
   }
   *out = g_scratch_addr[dev];
   return NSV_OK;

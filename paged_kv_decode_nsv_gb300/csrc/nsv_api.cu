@@ -32,6 +32,7 @@ constexpr int kEnoughWarpsPerSm = 16;   // consumer warps per SM that keep HBM b
 
 struct DeviceState {
   bool ready = false;
+  void* ctx = nullptr;  // the CUDA context the addresses below belong to
   uint32_t* status = nullptr;
   unsigned long long* walked = nullptr;
   int num_sms = 0;
@@ -55,14 +56,50 @@ int cuda_fail() {
   return NSV_ERR_CUDA;
 }
 
+// cuCtxGetCurrent, reached like cuTensorMapEncodeTiled below (loaded once).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn g_ctx_current = nullptr;
+std::once_flag g_ctx_once;
+
+}  // namespace
+
+void* current_cuda_context() {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess && fn)
+      g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    else
+      (void)cudaGetLastError();
+  });
+  CUcontext c = nullptr;
+  if (!g_ctx_current || g_ctx_current(&c) != CUDA_SUCCESS) return nullptr;
+  return reinterpret_cast<void*>(c);
+}
+
+namespace {
+
 // Per-device set-up on first use: symbol addresses of the status words,
-// kernel attributes, SM count.  Needs the device current.
+// kernel attributes, SM count.  Needs the device current.  Done again when
+// a different context is current on the device than the one the addresses
+// were taken in (the old one was destroyed, by cudaDeviceReset for one): its
+// workspace went with it and is dropped, not freed.
 int device_state(DeviceState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail();
   if (dev < 0 || dev >= kMaxDevices) return NSV_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState& d = g_dev[dev];
+  if (d.ready) {
+    void* now = current_cuda_context();
+    if (now != nullptr && now != d.ctx) {
+      d.ready = false;
+      d.ws = nullptr;
+      d.ws_bytes = 0;
+    }
+  }
   if (!d.ready) {
     if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status) != cudaSuccess)
       return cuda_fail();
@@ -80,6 +117,7 @@ int device_state(DeviceState** out) {
         return cuda_fail();
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
+    d.ctx = current_cuda_context();  // bound by the runtime calls above
     d.ready = true;
   }
   *out = &d;
@@ -587,13 +625,27 @@ NSV_API int nsv_selftest_bounded_wait(uint64_t limit_ns, int* gave_up, uint64_t*
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&res), g_probe) != cudaSuccess)
     return cuda_fail();
   if (cudaMemsetAsync(res, 0xff, sizeof(g_probe), stream) != cudaSuccess) return cuda_fail();
-  if (launch_wait_probe(limit_ns, res, stream) != cudaSuccess) return cuda_fail();
+  if (launch_wait_probe(limit_ns, res, d->status, stream) != cudaSuccess) return cuda_fail();
   unsigned long long h[2] = {0, 0};
   if (cudaMemcpyAsync(h, res, sizeof h, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
     return cuda_fail();
   if (cudaStreamSynchronize(stream) != cudaSuccess) return cuda_fail();
   *gave_up = h[0] == 1ull ? 1 : 0;
   *waited_ns = (uint64_t)h[1];
+  return NSV_OK;
+}
+
+NSV_API int nsv_status_async(uint32_t* dst, int clear, cudaStream_t stream) {
+  if (!dst) return NSV_ERR_NULLPTR;
+  if (reinterpret_cast<uintptr_t>(dst) & 3u) return NSV_ERR_ALIGN;
+  DeviceState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(dst, d->status, sizeof(uint32_t), cudaMemcpyDefault, stream) !=
+      cudaSuccess)
+    return cuda_fail();
+  if (clear && cudaMemsetAsync(d->status, 0, sizeof(uint32_t), stream) != cudaSuccess)
+    return cuda_fail();
   return NSV_OK;
 }
 

@@ -291,8 +291,12 @@ cudaError_t prepare_decode_kernels();
 // (cudaOccupancyMaxActiveBlocksPerMultiprocessor).
 cudaError_t decode_occupancy(int dtype, int head_dim, int qw, int consumer, int threads,
                              int smem, int* ctas);
-// The bounded-wait self-test kernel (result: device [gave_up, waited_ns]).
+// The bounded-wait self-test kernel (result: device [gave_up, waited_ns]);
+// a wait that gives up also sets NSV_DEV_TIMEOUT in *status.
 cudaError_t launch_wait_probe(unsigned long long limit_ns, unsigned long long* result,
-                              cudaStream_t stream);
+                              uint32_t* status, cudaStream_t stream);
+// The CUDA context current on the calling thread (null when there is none or
+// it cannot be read): per-device state is keyed on it.
+void* current_cuda_context();
 
 }  // namespace nsv

@@ -30,7 +30,7 @@ if not os.path.exists(LIB_PATH):
 
 _lib = ctypes.CDLL(LIB_PATH)
 
-ABI_VERSION = 101  # the layout of Shape and Plan below
+ABI_VERSION = 102  # the layout of Shape and Plan below
 F32, BF16 = 0, 1
 (CONSUMER_AUTO, CONSUMER_CUDA, CONSUMER_TENSOR, CONSUMER_TENSOR_VECTOR_ROWS,
  CONSUMER_TENSOR_TMEM) = 0, 1, 2, 3, 4
@@ -93,6 +93,8 @@ _lib.nsv_paged_decode_noalloc.argtypes = [_SP, _vp, _vp, _vp, _vp, _vp, _f, _vp,
 _lib.nsv_device_status.restype = _i32
 _lib.nsv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32),
                                    ctypes.POINTER(ctypes.c_uint64), _i32]
+_lib.nsv_status_async.restype = _i32
+_lib.nsv_status_async.argtypes = [_vp, _i32, _vp]
 _lib.nsv_selftest_bounded_wait.restype = _i32
 _lib.nsv_selftest_bounded_wait.argtypes = [ctypes.c_uint64, ctypes.POINTER(ctypes.c_int),
                                            ctypes.POINTER(ctypes.c_uint64), _vp]
@@ -316,6 +318,21 @@ def selftest_bounded_wait(limit_ns, stream=None):
                                           ctypes.byref(waited), _stream(stream)),
            "nsv_selftest_bounded_wait")
     return gave_up.value, waited.value
+
+
+def status_async(dst, clear=True, stream=None):
+    """Enqueue a copy of the device status word into `dst` (a uint32/int32
+    tensor of at least one element, on the device or in pinned host memory)
+    and, with `clear`, zero the word, both on `stream`; no synchronisation.
+    Read `dst` once the stream has reached the copy."""
+    import torch
+    if dst.dtype not in (torch.int32, torch.uint32) or dst.numel() < 1:
+        raise ValueError("dst must be an int32 or uint32 tensor of at least one element")
+    if not dst.is_cuda and not dst.is_pinned():
+        raise ValueError("dst must be device memory or pinned host memory")
+    _check(_lib.nsv_status_async(dst.data_ptr(), 1 if clear else 0, _stream(stream)),
+           "nsv_status_async")
+    return dst
 
 
 def device_status(clear=True):

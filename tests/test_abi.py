@@ -50,7 +50,7 @@ def test_library_exports_nothing_else(nsv):
 
 
 def test_abi_version_and_strerror(nsv):
-    assert nsv.abi_version() == nsv.ABI_VERSION == 101
+    assert nsv.abi_version() == nsv.ABI_VERSION == 102
     for code in (0, -1, -2, -3, -4, -5, -6, -7, -8, -10):
         assert nsv.strerror(code) and "unknown" not in nsv.strerror(code)
     assert "unknown" in nsv.strerror(-99)
@@ -329,6 +329,12 @@ def test_null_and_misaligned_pointers_refused_before_any_device_call(nsv):
     assert rc == -4
     rc = lib.nsv_kv_write(None, fake, fake, fake, fake, fake, None)
     assert rc == -1
+
+
+def test_status_async_refuses_null_and_misaligned_destinations(nsv):
+    lib = nsv._lib
+    assert lib.nsv_status_async(None, 1, None) == -1
+    assert lib.nsv_status_async(ctypes.c_void_p(0x100002), 1, None) == -4
 
 
 def test_tampered_plan_refused_before_any_device_call(nsv):
