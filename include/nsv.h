@@ -163,7 +163,8 @@ typedef struct nsv_plan {
                                  (CUDA-core consumer; 1 for the tensor one) */
     int32_t consumer;         /* NSV_CONSUMER_CUDA, _TENSOR, _TENSOR_VECTOR_ROWS
                                  or _TENSOR_TMEM */
-    int32_t reserved;         /* 0 */
+    int32_t blocks_per_stage; /* consecutive blocks of one row a stage holds:
+                                 1 to 4 for NSV_CONSUMER_TENSOR_TMEM, else 1 */
     int64_t workspace_bytes;  /* device scratch the read needs */
 } nsv_plan;
 
@@ -188,11 +189,14 @@ typedef struct nsv_plan {
  *                       (tcgen05.mma with the accumulators in tensor
  *                       memory).  The MMA's 128 rows are the query vectors
  *                       of a group of 4, 2 or 1 KV heads (128 / group rows
- *                       each, zero past the vectors): kv_heads_per_cta is
- *                       the group, which must divide num_kv_heads; by
- *                       default the largest that fits.
+ *                       each, zero past the vectors; group x head_dim at
+ *                       most 256): kv_heads_per_cta is the group, which must
+ *                       divide num_kv_heads; by default the largest that
+ *                       fits.  A stage holds blocks_per_stage consecutive
+ *                       blocks of one row (fewer at a segment's end), and
+ *                       one scores MMA per 16 dims covers all of them.
  *                       Four softmax warps (one thread per row) and an MMA
- *                       warp that issues the next block's scores while the
+ *                       warp that issues the next stage's scores while the
  *                       softmax warps work; K/V tiles by 2-D TMA as above.
  * The default plan takes NSV_CONSUMER_TENSOR for bf16 shapes with 2 to 8
  * query vectors per KV head, NSV_CONSUMER_TENSOR_VECTOR_ROWS for 9 to 16,
@@ -244,15 +248,17 @@ NSV_API int nsv_plan_split(const nsv_shape *shape, int num_sms, nsv_plan *plan);
  * correctly).  Any argument <= 0 is chosen by the heuristic: kv_heads_per_cta (must divide num_kv_heads), stages (2..8),
  * ctas_per_sm (1..8), grid (persistent CTAs; default num_sms * ctas_per_sm)
  * vectors_per_warp (1, 2 or 4, dividing the query vectors per KV head;
- * at most 16 consumer warps for 1 or 2, 8 for 4; CUDA-core consumer only)
- * and consumer (NSV_CONSUMER_*; AUTO picks as the default plan does).
- * Returns NSV_ERR_RANGE when a fixed choice does not fit the shape or the
- * shared-memory limit, or asks for the tensor consumer where it does not
+ * at most 16 consumer warps for 1 or 2, 8 for 4; CUDA-core consumer only),
+ * consumer (NSV_CONSUMER_*; AUTO picks as the default plan does) and
+ * blocks_per_stage (1 to 4, NSV_CONSUMER_TENSOR_TMEM only; its scores
+ * product is at most 256 tokens wide and its tensor-memory columns at most
+ * 512).  Returns NSV_ERR_RANGE when a fixed choice does not fit the shape or
+ * the shared-memory limit, or asks for the tensor consumer where it does not
  * apply.
  */
 NSV_API int nsv_plan_custom(const nsv_shape *shape, int num_sms, int kv_heads_per_cta,
                             int stages, int ctas_per_sm, int grid, int vectors_per_warp,
-                            int consumer, nsv_plan *plan);
+                            int consumer, int blocks_per_stage, nsv_plan *plan);
 
 /*
  * How many CTAs of `plan`'s kernel one SM of the current device holds at the

@@ -99,6 +99,14 @@ __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
       : "memory");
 }
 
+// Add `bytes` to the transaction count the current phase of `bar` waits
+// for (no arrival): the TMEM form arms a stage block by block and arrives
+// once when the stage is complete.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -183,6 +191,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Prefetch `bytes` (a multiple of 16) at a 16-byte aligned global address
+// into L2, without waiting.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // One 2-D TMA tile load global -> this CTA's shared memory (the tensor map's
 // box, with its swizzle), completing on `bar`.  x is the innermost coordinate.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
@@ -191,6 +205,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// The same with a 4-D tensor map (coordinates x innermost, y, z, w).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int x, int y, int z,
+                                            int w, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// The same with a 3-D tensor map (coordinates x innermost, y, z).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z,
+                                            uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
       : "memory");
 }
 
@@ -236,6 +270,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // or V tile set staged by 128-byte-swizzled TMA loads: the dims are split in
 // 64-dim halves of half_bytes each, a row of a half is 128 bytes, and chunk c
 // of row r sits at position c ^ (r % 8).
+// Byte offset of 16-byte chunk dc of token row r in the TMEM form's K
+// layout: rows in groups of 8, each group's 64-dim halves one 1024-byte
+// atom after the other ([group][half][8 rows][128 bytes], 128-byte swizzle).
+template <int D>
+__device__ __forceinline__ uint32_t swz_grouped(int r, int dc) {
+  return (uint32_t)(r >> 3) * (D / 64) * 1024u + (uint32_t)(dc >> 3) * 1024u +
+         (uint32_t)(r & 7) * 128u + ((uint32_t)((dc & 7) ^ (r & 7)) << 4);
+}
+
 __device__ __forceinline__ uint32_t swz(int r, int dc, uint32_t half_bytes) {
   return (uint32_t)(dc >> 3) * half_bytes + (uint32_t)r * 128u +
          ((uint32_t)((dc & 7) ^ (r & 7)) << 4);
@@ -352,6 +395,16 @@ __device__ __forceinline__ void umma_bf16_warp(uint32_t d_tmem, uint64_t a, uint
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u), "r"(lead ? 1u : 0u)
       : "memory");
 }
+// The same with the A operand in tensor memory (`a_tmem`: its rows in the
+// lanes, two bf16 of a row's K to a 32-bit column).
+__device__ __forceinline__ void umma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                                  uint32_t idesc, bool accumulate, bool lead) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %4, 0;\n\tsetp.ne.u32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u), "r"(lead ? 1u : 0u)
+      : "memory");
+}
 // One arrive on `bar` once every MMA the `lead` lane issued so far is
 // complete (executed by the whole warp).
 __device__ __forceinline__ void umma_commit_warp(uint32_t bar, bool lead) {
@@ -386,7 +439,13 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
-// 16 or 32 consecutive fp32 columns of this thread's TMEM lane (warp-wide).
+// 8, 16 or 32 consecutive fp32 columns of this thread's TMEM lane (warp-wide).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -406,6 +465,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
@@ -558,6 +626,17 @@ __device__ __forceinline__ void finish_cut_row(const DecodeParams& p, int row, i
       }
     }
   }
+}
+
+// finish_cut_row for the TMEM form, out of line: it runs once per piece of a
+// cut row, and inlined into the softmax warps' stage loop its registers
+// pushed that loop's working set into local memory.
+template <typename T, int D>
+__device__ __noinline__ void finish_cut_row_call(const DecodeParams& p, int row, int kv0,
+                                                 const int* s_prefix, int N, long long U,
+                                                 int nhg, int nvec, int v0, int nv, int ncw,
+                                                 int cw, int lane, volatile int* s_merge) {
+  finish_cut_row<T, D>(p, row, kv0, s_prefix, N, U, nhg, nvec, v0, nv, ncw, cw, lane, s_merge);
 }
 
 // Tensor-core consumer (bf16) with the query vectors as the MMA rows: a KV
@@ -796,19 +875,28 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
 // The TMEM form (bf16) on the 5th-generation tensor cores: tcgen05.mma from
 // shared-memory operands into tensor-memory accumulators.  The MMA has 128
 // rows: the group's KV heads take R = 128 / group rows each (their query
-// vectors, zero rows past them), so one MMA over the stage's tokens (16 per
-// head) gives every row its scores, and each row keeps only its own head's
-// 16 columns.  Roles:
+// vectors, zero rows past them).  A stage holds up to `blocks_per_stage`
+// consecutive blocks of one segment, so one scores MMA per 16 dims covers
+// all of them (N = blocks x group x 16 tokens) and each row keeps its own
+// head's 16 columns of every block.  The P.V product of a block is one MMA
+// of N = group x head_dim: every row's probabilities (for its own head's
+// tokens) times every head's V of the block, of which each row keeps its own
+// head's columns.  Roles:
 //   * an MMA warp (one lane issues) runs S = Q.K^T for stage n + 1 while the
 //     softmax warps work on stage n (two score buffers in tensor memory, two
 //     probability buffers in shared memory), then O += P.V for stage n once
 //     they hand P over, committed to the stage's empty barrier;
 //   * four softmax warps, one per TMEM lane quadrant: thread r owns row r
-//     (its online-softmax state in registers), reads its head's 16 scores
-//     with tcgen05.ld and writes its probabilities (bf16) into P.
-// Operands: Q (128 x D, 128-byte swizzle, K-major) copied from the q ring by
-// the softmax warps; K as staged by TMA (K-major); P in 8x16-byte core
-// matrices (zeros outside the row's head); V as staged (MN-major).
+//     (its online-softmax state in registers), reads its head's 16 scores of
+//     each block with tcgen05.ld and writes its probabilities (bf16) into P.
+// Shared-memory operands: Q (128 x D, 128-byte swizzle, K-major) copied
+// from global memory by the softmax warps; K as staged by TMA, the stage's
+// token rows (block, head, token) in order within each 64-dim half
+// (K-major); P in 8x16-byte core matrices, 16 tokens per block; V as
+// staged, block by block, each block's 64-dim chunks (half, head) 2 KiB
+// apart (MN-major).  Tensor memory: O in columns [0, group x D), the chunk
+// (half h, head k) at columns (h x group + k) x 64; then two score buffers
+// of blocks x group x 16 columns.
 // Barriers beyond the ring's: scores ready [2], probabilities handed over
 // [2], a piece's O complete, every MMA drained, query rows ready.  (A stage's
 // empty barrier, which its P.V's commit completes, also tells the softmax
@@ -823,6 +911,11 @@ struct TmemBars {
 };
 constexpr int kTmemBars = 7;
 
+// Token mask of block b of a TMEM stage (its second metadata word).
+__device__ __forceinline__ int tmem_block_mask(const int4& mm, int b) {
+  return ((b < 2 ? mm.x : mm.y) >> (16 * (b & 1))) & 0xffff;
+}
+
 // The MMA warp.  The d-th stage with data has its scores in buffer d & 1,
 // stage n's probabilities are in buffer n & 1; every barrier completes once
 // per use and never runs more than one phase ahead of a wait on it, so
@@ -831,35 +924,42 @@ template <int D>
 __device__ __forceinline__ bool tmem_mma_warp(const DecodeParams& p, unsigned char* smem,
                                               const SmemLayout& L, const int4* s_meta,
                                               uint32_t bars, uint32_t tmem, int lane) {
-  const int HG = p.heads_per_cta, S = p.stages;
-  const int ntok = HG * kBlock;
-  const int pch = ntok / 8;
-  const uint32_t half_bytes = (uint32_t)HG * kBlock * 128;
+  const int HG = p.heads_per_cta, S = p.stages, NB = p.blocks_per_stage;
+  const int ntok = NB * HG * kBlock;               // a full stage's token rows
+  // K: the stage's token rows in groups of 8, a group's 64-dim halves one
+  // 1024-byte atom apart: within a half, groups are D / 64 atoms apart
+  constexpr uint32_t kGroupBytes = (uint32_t)(D / 64) * 1024u;
+  const uint32_t k_area = (uint32_t)NB * L.kv_bytes;
   const TmemBars tb{bars + 8 * (2 * S + (int)L.q_slots)};
   const bool lead = lane == 0;
   const uint32_t stage0 = smem_u32(smem);
-  const uint32_t qa_s = smem_u32(smem + L.off_pbuf);
-  const uint32_t pb_s = qa_s + (uint32_t)(kTmemRows * D * 2);
-  const uint32_t pbuf_bytes = (uint32_t)(kTmemRows * ntok * 2);
+  const uint32_t pb_s = smem_u32(smem + L.off_pbuf);
+  const uint32_t pbuf_bytes = (uint32_t)(kTmemRows * NB * kBlock * 2);
+  const int pch = NB * 2;  // 16-byte chunks of a P row
+  // the query rows in tensor memory after the score buffers: 16 dims of K
+  // are 8 columns
+  const uint32_t q_col = (uint32_t)(HG * D + 2 * ntok);
   // descriptors are linear in the start address: a base plus an offset
-  const uint64_t dq0 = umma_desc(qa_s, 16, 1024, kUmmaSwizzle128);
-  const uint64_t dk0 = umma_desc(0u, 16, 1024, kUmmaSwizzle128);
+  const uint64_t dk0 = umma_desc(0u, 16, kGroupBytes, kUmmaSwizzle128);
   const uint64_t dp0 = umma_desc(pb_s, 128, (uint32_t)pch * 128, kUmmaSwizzleNone);
-  const uint64_t dv0 = umma_desc(0u, half_bytes, 1024, kUmmaSwizzle128);
-  const uint32_t idesc_s = umma_idesc_bf16(kTmemRows, ntok, false);
-  const uint32_t idesc_o = umma_idesc_bf16(kTmemRows, D, true);
+  // V, MN-major: the leading offset steps the block's 64-dim chunks (half,
+  // head), 2 KiB apart; the stride offset steps 8 tokens
+  const uint64_t dv0 = umma_desc(0u, 2048, 1024, kUmmaSwizzle128);
+  const uint32_t idesc_o = umma_idesc_bf16(kTmemRows, HG * D, true);
+  const uint32_t s_col = (uint32_t)(HG * D);  // the score buffers follow O
 
   uint32_t nd = 0;  // stages with data whose scores were issued
-  auto issue_scores = [&](uint32_t stage) {
+  auto issue_scores = [&](uint32_t stage, int nb) {
     tc_fence_after();
     const uint32_t st_s = stage0 + stage * L.stage_bytes;
-    const uint32_t sb = tmem + (uint32_t)(D + (int)(nd & 1) * ntok);
+    const uint32_t sb = tmem + s_col + (nd & 1) * (uint32_t)ntok;
+    const uint32_t idesc_s = umma_idesc_bf16(kTmemRows, nb * HG * kBlock, false);
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      // 16 dims: 64-dim half ks / 4, 32 bytes into its 128-byte rows
-      const uint32_t qoff = (uint32_t)(ks >> 2) * (kTmemRows * 128) + (uint32_t)(ks & 3) * 32;
-      const uint32_t koff = st_s + (uint32_t)(ks >> 2) * half_bytes + (uint32_t)(ks & 3) * 32;
-      umma_bf16_warp(sb, dq0 + (qoff >> 4), dk0 + (koff >> 4), idesc_s, ks > 0, lead);
+      // 16 dims: K's 64-dim half ks / 4, 32 bytes into its 128-byte rows
+      const uint32_t koff = st_s + (uint32_t)(ks >> 2) * 1024u + (uint32_t)(ks & 3) * 32;
+      umma_bf16_ts_warp(sb, tmem + q_col + (uint32_t)ks * 8, dk0 + (koff >> 4), idesc_s, ks > 0,
+                        lead);
     }
     umma_commit_warp(tb.scores(nd & 1), lead);
     ++nd;
@@ -870,6 +970,7 @@ __device__ __forceinline__ bool tmem_mma_warp(const DecodeParams& p, unsigned ch
   // stage 0
   if (!mbar_wait(bars, 0)) return false;
   int4 meta = s_meta[0];
+  int nb = s_meta[1].z;
   // every stage that brings query rows has them handed over (even one with
   // no data), so the hand-over barrier's phases match the waits
   if (!(meta.w & kEnd)) {
@@ -877,7 +978,7 @@ __device__ __forceinline__ bool tmem_mma_warp(const DecodeParams& p, unsigned ch
       if (!mbar_wait(tb.qready(), nq & 1)) return false;
       ++nq;
     }
-    if (meta.w & kData) issue_scores(0);
+    if (meta.w & kData) issue_scores(0, nb);
   }
   uint32_t s = 0, ph = 0;
   for (uint32_t n = 0;; ++n) {
@@ -885,29 +986,39 @@ __device__ __forceinline__ bool tmem_mma_warp(const DecodeParams& p, unsigned ch
     if (flags & kEnd) break;
     const uint32_t s1 = (s + 1 == (uint32_t)S) ? 0u : s + 1;
     const uint32_t ph1 = (s + 1 == (uint32_t)S) ? ph ^ 1u : ph;
-    // Look ahead: if stage n + 1 is already in and needs no new query rows,
-    // its scores go to the tensor core before this stage's P.V.
-    bool have_next = mbar_test_wait(bars + 8 * s1, ph1);
+    // Wait (bounded) for stage n's probabilities.  Meanwhile, as soon as
+    // stage n + 1 is in and needs no new query rows, its scores go to the
+    // tensor core ahead of this stage's P.V.  (A phase that one lane sees
+    // complete is complete for all: the tests are made warp-uniform.)
+    bool have_next = false, scored1 = false;
     int4 meta1 = make_int4(0, 0, 0, 0);
-    bool scored1 = false;
-    if (have_next) {
-      meta1 = s_meta[s1];
-      if ((meta1.w & kData) && !(meta1.w & kEnd) && !(meta1.w & kHasQ)) {
-        issue_scores(s1);
-        scored1 = true;
+    int nb1 = 0;
+    {
+      const uint32_t hbar = tb.handed(n & 1), hph = (n >> 1) & 1;
+      const unsigned long long t0 = global_ns();
+      for (uint32_t spin = 0;; ++spin) {
+        if (!have_next && __any_sync(kFull, mbar_test_wait(bars + 8 * s1, ph1))) {
+          have_next = true;
+          meta1 = s_meta[2 * s1];
+          nb1 = s_meta[2 * s1 + 1].z;
+          if ((meta1.w & kData) && !(meta1.w & kEnd) && !(meta1.w & kHasQ)) {
+            issue_scores(s1, nb1);
+            scored1 = true;
+          }
+        }
+        if (__any_sync(kFull, mbar_test_wait(hbar, hph))) break;
+        if ((spin & 63) == 63 && __any_sync(kFull, global_ns() - t0 > kWaitLimitNs)) return false;
       }
     }
-    // Stage n: wait for the probabilities, then P.V (or just release it)
-    if (!mbar_wait(tb.handed(n & 1), (n >> 1) & 1)) return false;
     tc_fence_after();
     if (flags & kFirst) fresh = true;
     if (flags & kData) {
-      const uint32_t vb = stage0 + s * L.stage_bytes + L.kv_bytes;
+      const uint32_t vb = stage0 + s * L.stage_bytes + k_area;
       const uint32_t pb = (n & 1) * pbuf_bytes;
-      for (int k = 0; k < HG; ++k)  // one MMA of K = 16 tokens per head
-        umma_bf16_warp(tmem, dp0 + ((pb + (uint32_t)k * 256) >> 4),
-                       dv0 + ((vb + (uint32_t)k * (kBlock * 128)) >> 4), idesc_o,
-                       !fresh || k > 0, lead);
+      for (int b = 0; b < nb; ++b)  // one MMA of K = 16 tokens per block
+        umma_bf16_warp(tmem, dp0 + ((pb + (uint32_t)b * 256) >> 4),
+                       dv0 + ((vb + (uint32_t)b * L.kv_bytes) >> 4), idesc_o, !fresh || b > 0,
+                       lead);
       fresh = false;
       umma_commit_warp(bars + 8 * (S + s), lead);  // the stage is free once P.V has read it
     } else if (lead) {
@@ -917,25 +1028,33 @@ __device__ __forceinline__ bool tmem_mma_warp(const DecodeParams& p, unsigned ch
     // stage n + 1
     if (!have_next) {
       if (!mbar_wait(bars + 8 * s1, ph1)) return false;
-      meta1 = s_meta[s1];
+      meta1 = s_meta[2 * s1];
+      nb1 = s_meta[2 * s1 + 1].z;
     }
     if (!scored1 && !(meta1.w & kEnd)) {
       if (meta1.w & kHasQ) {
         if (!mbar_wait(tb.qready(), nq & 1)) return false;
         ++nq;
       }
-      if (meta1.w & kData) issue_scores(s1);
+      if (meta1.w & kData) issue_scores(s1, nb1);
     }
     meta = meta1;
+    nb = nb1;
     s = s1;
     ph = ph1;
   }
   return true;
 }
 
-// The four softmax warps of the TMEM form (warps 1-4; warp w reaches TMEM
-// lanes 32 (w % 4) .. + 31).  Thread r owns MMA row r.  The query rows of a
-// piece come straight from global memory (the form keeps no q ring).
+// The eight softmax warps of the TMEM form (warps 1-8; warp w reaches TMEM
+// lanes 32 (w % 4) .. + 31, so warps w and w + 4 share a quadrant).  Thread
+// r of either warp of a pair owns MMA row r: the pair splits each stage's
+// blocks (the first warp takes the first half), exchanges the rows' maxima
+// through shared memory, keeps the same running max and rescale decisions,
+// and splits the output columns for the rescale and the epilogue; each warp
+// keeps its own part of the running sum.  The query rows of a piece come
+// straight from global memory (the form keeps no q ring; the producer
+// prefetches them into L2 when it opens the piece).
 template <int D>
 __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned char* smem,
                                              const SmemLayout& L, const int4* s_meta,
@@ -944,26 +1063,40 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
                                              int nvec, int warp, int lane, uint32_t tmem) {
   using T = __nv_bfloat16;
   constexpr int kNcw = kTmemWarps;
+  constexpr int kPieces = D / 64;           // 32-column pieces of a row's O each warp owns
   const int G = p.group, NQ = p.query_len, HG = p.heads_per_cta, S = p.stages;
+  const int NB = p.blocks_per_stage;
   const int vpk = G * NQ;
   const int R = kTmemRows / HG;             // rows per KV head of the group
   const int cw = warp - 1;
   const int q4 = warp & 3;                  // the TMEM lane quadrant this warp reaches
+  const int hf = cw >> 2;                   // which half of the pair
   const int r = q4 * 32 + lane;             // this thread's MMA row
   const int kvl = r / R, v = r - kvl * R;   // its KV head within the group, its vector
   const bool rok = v < vpk;
   const int qhl = kvl * G + (rok ? v / NQ : 0);  // query head within the group
   const int jq = rok ? v % NQ : 0;               // query token
-  const int ntok = HG * kBlock;
-  const int pch = ntok / 8;                 // 16-byte chunks of a P row
-  const uint32_t pbuf_bytes = (uint32_t)(kTmemRows * ntok * 2);
-  const uint32_t half_bytes = (uint32_t)HG * kBlock * 128;
+  const int ntok = NB * HG * kBlock;
+  const int pch = NB * 2;                   // 16-byte chunks of a P row
+  const uint32_t pbuf_bytes = (uint32_t)(kTmemRows * NB * kBlock * 2);
+  const uint32_t k_area = (uint32_t)NB * L.kv_bytes;
+  const uint32_t vhalf = (uint32_t)HG * kBlock * 128;  // a block's V: one 64-dim half
   volatile int* s_merge = s_abort + 1;
   const TmemBars tb{bars + 8 * (2 * S + (int)L.q_slots)};
-  unsigned char* const qa = smem + L.off_pbuf;     // Q: 128 x D, swizzled
-  unsigned char* const pb = qa + kTmemRows * D * 2;  // P: two buffers of 128 x ntok
+  unsigned char* const pb = smem + L.off_pbuf;     // P: two buffers of 128 x NB*16
+  // the pairs' exchanges: maxima [stage parity][half][row], sums [piece parity][half][row]
+  float* const s_xmax = reinterpret_cast<float*>(pb + 2 * pbuf_bytes);
+  float* const s_xl = s_xmax + 4 * kTmemRows;
   const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-  const uint32_t t_o = tmem + lane_base;  // O: columns [0, D)
+  const uint32_t t_o = tmem + lane_base;
+  const uint32_t s_col = (uint32_t)(HG * D);
+  // this warp's 32-column pieces of the row's O: piece c covers the row's
+  // own columns [32c, 32c + 32), i.e. chunk (c / 2, kvl) at offset c % 2
+  auto o_col = [&](int c) { return (uint32_t)(((c >> 1) * HG + kvl) * 64 + (c & 1) * 32); };
+  const int pc0 = hf * kPieces;
+  auto pair_sync = [&]() {
+    asm volatile("bar.sync %0, 64;" ::"r"(3 + q4) : "memory");
+  };
 
   // Empty rows see nothing: zeros for all their (token, head) vectors.
   constexpr int kChunks = D * 2 / 16;
@@ -974,14 +1107,10 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
         reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)rr * NQ * p.heads + vh) * D)[c] =
             make_uint4(0u, 0u, 0u, 0u);
   }
-  // P rows hold zeros outside their own head's two 16-byte chunks, for good
-  for (int b = 0; b < 2; ++b)
-    for (int kc = 0; kc < pch; ++kc)
-      *reinterpret_cast<uint4*>(pb + b * pbuf_bytes + (r >> 3) * (pch * 128) + kc * 128 +
-                                (r & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-  unsigned char* const prow = pb + (r >> 3) * (pch * 128) + (2 * kvl) * 128 + (r & 7) * 16;
+  // this row's P: block b's tokens in 16-byte chunks 2b and 2b + 1
+  unsigned char* const prow = pb + (r >> 3) * (pch * 128) + (r & 7) * 16;
 
-  float m = -INFINITY, l = 0.f;
+  float m = -INFINITY, l = 0.f;  // l: this warp's part of the running sum
   bool fresh = true;   // no P.V yet in this piece: O holds nothing of it
   uint32_t pv_s = 0, pv_ph = 0;  // stage and phase of the last P.V handed over
   uint32_t npv = 0;    // P.V products handed over so far (all pieces); also
@@ -995,11 +1124,12 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
       failed = true;
       break;
     }
-    const int4 meta = s_meta[s];
+    const int4 meta = s_meta[2 * s];
+    const int4 mm = s_meta[2 * s + 1];
     const int flags = meta.w;
     if (flags & kEnd) break;
+    const int nb = mm.z;
     unsigned char* st = smem + s * L.stage_bytes;
-    const int tmask = meta.y & 0xffff;
     const int qh0 = (flags >> 16) * G;
     const uint32_t b = n & 1;
 
@@ -1008,36 +1138,53 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
       l = 0.f;
       fresh = true;
       if (flags & kHasQ) {
-        // this row's query vector -> row r of the Q operand: 16-byte chunk c
-        // of a 64-dim half at chunk c ^ (r & 7).  Every earlier scores MMA is
+        // this row's query vector -> lane r of the Q operand in tensor
+        // memory, two dims to a column (as they lie in memory); each warp of
+        // the pair copies half of the dims.  Every earlier scores MMA is
         // complete (each was waited for below).
         const uint4* src = reinterpret_cast<const uint4*>(
-            static_cast<const T*>(p.q) + (((size_t)meta.x * NQ + jq) * p.heads + qh0 + qhl) * D);
-        uint4 vals[D / 8];
+            static_cast<const T*>(p.q) + (((size_t)meta.x * NQ + jq) * p.heads + qh0 + qhl) * D) +
+            hf * (D / 16);
+        constexpr int kWords = D / 4;  // this warp's columns: D / 2 dims
+        uint32_t w[kWords];
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) vals[c] = rok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c)
-          *reinterpret_cast<uint4*>(qa + (c >> 3) * (kTmemRows * 128) + r * 128 +
-                                    (((c & 7) ^ (r & 7)) * 16)) = vals[c];
-        fence_proxy_async_smem();
+        for (int c = 0; c < kWords / 4; ++c) {
+          const uint4 v4 = rok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * c] = v4.x;
+          w[4 * c + 1] = v4.y;
+          w[4 * c + 2] = v4.z;
+          w[4 * c + 3] = v4.w;
+        }
+        const uint32_t qt = tmem + lane_base + s_col + 2u * (uint32_t)ntok + (uint32_t)(hf * kWords);
+        if constexpr (kWords == 32) {
+          tmem_st32(qt, w);
+        } else {
+          tmem_st16(qt, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tb.qready());
       }
     }
 
     if (flags & kData) {
-      const int rem = flags & 0xff;
-      const int nvalid = min(kBlock, rem);
+      const int rem0 = flags & 0xff;  // the row's positions from the stage's first block on
       // V rows that hold no data become zeros (P is 0 there, but 0 * NaN is
       // not); the MMA warp reads V only after the hand-over below.
-      if (nvalid < kBlock || tmask != 0xffff) {
-        for (int c = cw * 32 + lane; c < ntok * kChunks; c += kNcw * 32) {
-          const int tr = c / kChunks, dc = c - tr * kChunks;
-          const int t = tr % kBlock;
-          if (!(t < nvalid && ((tmask >> t) & 1)))
-            *reinterpret_cast<uint4*>(st + L.kv_bytes + swz(tr, dc, half_bytes)) =
-                make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int bb = 0; bb < kTmemMaxBlocks; ++bb) {
+        if (bb >= nb) break;
+        const int mask = tmem_block_mask(mm, bb);
+        const int nvalid = min(kBlock, rem0 - bb * kBlock);
+        if (nvalid < kBlock || mask != 0xffff) {
+          unsigned char* vblk = st + k_area + bb * L.kv_bytes;
+          for (int c = cw * 32 + lane; c < HG * kBlock * kChunks; c += kNcw * 32) {
+            const int tr = c / kChunks, dc = c - tr * kChunks;
+            const int t = tr % kBlock;
+            if (!(t < nvalid && ((mask >> t) & 1)))
+              *reinterpret_cast<uint4*>(vblk + swz(tr, dc, vhalf)) = make_uint4(0u, 0u, 0u, 0u);
+          }
         }
       }
       if (!mbar_wait(tb.scores(npv & 1), (npv >> 1) & 1)) {
@@ -1045,31 +1192,74 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
         break;
       }
       tc_fence_after();
-      uint32_t sr[16];
-      tmem_ld16(tmem + lane_base + (uint32_t)(D + (int)(npv & 1) * ntok + kvl * kBlock), sr);
+      // This warp's share of the stage: blocks [b0, b0 + nw), at most two
+      // (the first warp of the pair takes the first half, rounded up).
+      // Their raw scores are read from tensor memory once, by two loads that
+      // are always issued (past the warp's share they read the stage's last
+      // block again), so that the registers they fill are always defined.
+      const int lo_n = (nb + 1) >> 1;
+      const int b0 = hf ? lo_n : 0;
+      const int nw = hf ? nb - lo_n : lo_n;
+      const uint32_t sbase = tmem + lane_base + s_col + (npv & 1) * (uint32_t)ntok;
+      const float qs = p.qscale;
+      uint32_t sr[2][16];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        tmem_ld16(sbase + (uint32_t)((min(b0 + i, nb - 1) * HG + kvl) * kBlock), sr[i]);
       tmem_wait_ld();
-      // Online softmax of this row's 16 scores; the running max is raised
-      // lazily (by more than kRescaleSlack), as in the other tensor forms.
-      // A block every query token sees in full needs no masks.
-      const bool dense = nvalid == kBlock && tmask == 0xffff && rem - (NQ - 1) >= kBlock;
-      float x[16];
+      // Whether block b0 + i is seen in full by every query token of every
+      // row (warp-uniform): then it needs no per-token masks.  Rows past the
+      // vector count (zero queries) may then compute finite garbage: their
+      // state is never written anywhere.
+      auto dense = [&](int i) {
+        const int bb = b0 + i;
+        return tmem_block_mask(mm, bb) == 0xffff && rem0 - bb * kBlock - (NQ - 1) >= kBlock;
+      };
+      // the tokens of block b0 + i this row's query sees (bit t: token t)
+      auto visible = [&](int i) {
+        const int bb = b0 + i;
+        const int nv = rem0 - bb * kBlock - (NQ - 1 - jq);
+        const int upto = nv <= 0 ? 0 : nv >= kBlock ? 0xffff : (1 << nv) - 1;
+        return rok ? tmem_block_mask(mm, bb) & upto : 0;
+      };
+      float mx = -INFINITY;  // this warp's maximum of the scaled scores
 #pragma unroll
-      for (int t = 0; t < kBlock; ++t) x[t] = __uint_as_float(sr[t]) * p.qscale;
-      if (!dense || !rok) {
-        const int nv = rem - (NQ - 1 - jq);  // positions this row's query sees
+      for (int i = 0; i < 2; ++i) {
+        if (i >= nw) break;
+        if (dense(i)) {
+          // the maximum of scale * s is scale times the largest s (the
+          // smallest for a negative scale)
+          float a8[8];
+          if (qs >= 0.f) {
 #pragma unroll
-        for (int t = 0; t < kBlock; ++t)
-          if (!(rok && t < nv && ((tmask >> t) & 1))) x[t] = -INFINITY;
+            for (int t = 0; t < 8; ++t)
+              a8[t] = fmaxf(__uint_as_float(sr[i][t]), __uint_as_float(sr[i][t + 8]));
+#pragma unroll
+            for (int t = 0; t < 4; ++t) a8[t] = fmaxf(a8[t], a8[t + 4]);
+            mx = fmaxf(mx, fmaxf(fmaxf(a8[0], a8[2]), fmaxf(a8[1], a8[3])) * qs);
+          } else {
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              a8[t] = fminf(__uint_as_float(sr[i][t]), __uint_as_float(sr[i][t + 8]));
+#pragma unroll
+            for (int t = 0; t < 4; ++t) a8[t] = fminf(a8[t], a8[t + 4]);
+            mx = fmaxf(mx, fminf(fminf(a8[0], a8[2]), fminf(a8[1], a8[3])) * qs);
+          }
+        } else {
+          const int vis = visible(i);
+#pragma unroll
+          for (int t = 0; t < kBlock; ++t)
+            if ((vis >> t) & 1) mx = fmaxf(mx, __uint_as_float(sr[i][t]) * qs);
+        }
       }
-      float mx;
-      {
-        float a8[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) a8[t] = fmaxf(x[t], x[t + 8]);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) a8[t] = fmaxf(a8[t], a8[t + 4]);
-        mx = fmaxf(fmaxf(a8[0], a8[2]), fmaxf(a8[1], a8[3]));
-      }
+      // the pair's maximum over the whole stage
+      float* xm = s_xmax + (npv & 1) * (2 * kTmemRows);
+      xm[hf * kTmemRows + r] = mx;
+      pair_sync();
+      mx = fmaxf(xm[r], xm[kTmemRows + r]);
+      // Online softmax; the running max is raised lazily (by more than
+      // kRescaleSlack), as in the other tensor forms.  Both warps of the pair
+      // see the same maximum and take the same decisions.
       float alpha = 1.f;
       const bool raise = mx > m + kRescaleSlack;  // also the first finite max (m = -inf)
       if (raise) {
@@ -1080,43 +1270,62 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
       if (!fresh && __any_sync(kFull, raise)) {
         // O holds earlier blocks of the piece: once the last P.V handed over
         // is complete (its commit completes that stage's empty barrier),
-        // rescale the warp's rows (1 where the max did not move)
+        // rescale this warp's columns of its rows (1 where the max did not move)
         if (!mbar_wait(bars + 8 * (S + pv_s), pv_ph)) {
           failed = true;
           break;
         }
         tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(t_o + (uint32_t)c0, o);
+        for (int c = 0; c < 2 * kPieces; ++c) {
+          const uint32_t col = o_col(pc0 + (c >> 1)) + (uint32_t)(c & 1) * 16;
+          uint32_t o[16];
+          tmem_ld16(t_o + col, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-          tmem_st32(t_o + (uint32_t)c0, o);
+          for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+          tmem_st16(t_o + col, o);
         }
         tmem_wait_st();
       }
-      // probabilities (none while the row has seen no position: m = -inf)
-      uint32_t pk[8];
+      // probabilities 2^(scale * s - m), rounded to bf16 into P (none while
+      // the row has seen no position: m = -inf)
       {
-        float pv[16];
         const bool live = m != -INFINITY;
+        unsigned char* pr = prow + b * pbuf_bytes;
 #pragma unroll
-        for (int t = 0; t < kBlock; ++t) pv[t] = live ? ex2_approx(x[t] - m) : 0.f;
-        float s8[8];
+        for (int i = 0; i < 2; ++i) {
+          if (i >= nw) break;
+          float pv[16];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) s8[t] = pv[t] + pv[t + 8];
+          for (int t = 0; t < kBlock; t += 2) {
+            pv[t] = -m;
+            pv[t + 1] = -m;
+            fma2(pv[t], pv[t + 1], __uint_as_float(sr[i][t]), __uint_as_float(sr[i][t + 1]), qs,
+                 qs);
+          }
+          if (dense(i) && live) {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) s8[t] += s8[t + 4];
-        l += (s8[0] + s8[2]) + (s8[1] + s8[3]);
+            for (int t = 0; t < kBlock; ++t) pv[t] = ex2_approx(pv[t]);
+          } else {
+            const int vis = live ? visible(i) : 0;
 #pragma unroll
-        for (int t2 = 0; t2 < 8; ++t2) pk[t2] = pack_bf16(pv[2 * t2], pv[2 * t2 + 1]);
+            for (int t = 0; t < kBlock; ++t) pv[t] = ((vis >> t) & 1) ? ex2_approx(pv[t]) : 0.f;
+          }
+          float s8[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) s8[t] = pv[t] + pv[t + 8];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) s8[t] += s8[t + 4];
+          l += (s8[0] + s8[2]) + (s8[1] + s8[3]);
+          uint32_t pk[8];
+#pragma unroll
+          for (int t2 = 0; t2 < 8; ++t2) pk[t2] = pack_bf16(pv[2 * t2], pv[2 * t2 + 1]);
+          const int kc = 2 * (b0 + i);
+          *reinterpret_cast<uint4*>(pr + kc * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(pr + (kc + 1) * 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
       }
-      // this row's head's two 8-token chunks of P (the rest stays zero)
-      unsigned char* pr = prow + b * pbuf_bytes;
-      *reinterpret_cast<uint4*>(pr) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      *reinterpret_cast<uint4*>(pr + 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       fence_proxy_async_smem();
       ++npv;
       pv_s = s;
@@ -1136,16 +1345,21 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
         failed = true;
         break;
       }
-      ++nout;
       tc_fence_after();
+      // the row's whole running sum: both warps' parts
+      float* xl = s_xl + (nout & 1) * (2 * kTmemRows);
+      xl[hf * kTmemRows + r] = l;
+      pair_sync();
+      const float lt = xl[r] + xl[kTmemRows + r];
+      ++nout;
       if (flags & kFinal) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
         T* out = static_cast<T*>(p.out) + (((size_t)row * NQ + jq) * p.heads + qh0 + qhl) * D;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c = 0; c < kPieces; ++c) {
           uint32_t o[32];
           if (!fresh) {
-            tmem_ld32(t_o + (uint32_t)c0, o);
+            tmem_ld32(t_o + o_col(pc0 + c), o);
             tmem_wait_ld();
           } else {
 #pragma unroll
@@ -1154,7 +1368,7 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
           if (rok) {
 #pragma unroll
             for (int j = 0; j < 32; j += 8)
-              *reinterpret_cast<uint4*>(out + c0 + j) = make_uint4(
+              *reinterpret_cast<uint4*>(out + (pc0 + c) * 32 + j) = make_uint4(
                   pack_bf16(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv),
                   pack_bf16(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv),
                   pack_bf16(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv),
@@ -1164,17 +1378,17 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
       } else {
         const size_t slot = (size_t)meta.z * nvec + (size_t)(kvl * vpk + v);
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c = 0; c < kPieces; ++c) {
           uint32_t o[32];
           if (!fresh) {
-            tmem_ld32(t_o + (uint32_t)c0, o);
+            tmem_ld32(t_o + o_col(pc0 + c), o);
             tmem_wait_ld();
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] = 0u;
           }
           if (rok) {
-            float* a = p.ws_acc + slot * D + c0;
+            float* a = p.ws_acc + slot * D + (pc0 + c) * 32;
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
               *reinterpret_cast<float4*>(a + j) =
@@ -1182,12 +1396,14 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
                               __uint_as_float(o[j + 2]), __uint_as_float(o[j + 3]));
           }
         }
-        if (rok) p.ws_ml[slot] = make_float2(m, l);
-        // this warp's rows are vectors [vw, vw + 32) of one KV head
+        if (rok && hf == 0) p.ws_ml[slot] = make_float2(m, lt);
+        // this quadrant's rows are vectors [vw, vw + 32) of one KV head; the
+        // pair merges 16 of them each
         const int vw = q4 * 32 - kvl * R;
-        const int nvw = max(0, min(32, vpk - vw));
-        finish_cut_row<T, D>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, kvl * vpk + vw,
-                             nvw, kNcw, cw, lane, s_merge);
+        const int nvq = max(0, min(32, vpk - vw));
+        const int nvw = max(0, min(16, nvq - hf * 16));
+        finish_cut_row_call<T, D>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec,
+                                  kvl * vpk + vw + hf * 16, nvw, kNcw, cw, lane, s_merge);
       }
       tc_fence_before();
     }
@@ -1457,7 +1673,8 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
                   : MMA == kMmaTmem       ? kTmemWarps
                                           : nvec / QW;
   const int S = p.stages;
-  const SmemLayout L = make_layout((int)sizeof(T), D, HG, nvec, S, p.rows, MMA, QW);
+  const int NBS = MMA == kMmaTmem ? p.blocks_per_stage : 1;  // blocks per stage
+  const SmemLayout L = make_layout((int)sizeof(T), D, HG, nvec, S, p.rows, MMA, QW, NBS);
 
   int4* s_meta = reinterpret_cast<int4*>(smem + L.off_meta);
   const uint32_t bars = smem_u32(smem + L.off_bars);  // full[s] at +8s, empty[s] at +8(S+s)
@@ -1469,7 +1686,7 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // the TMEM form's tensor-memory columns and their base address
-  const uint32_t tmem_ncols = MMA == kMmaTmem ? (uint32_t)tmem_cols(D, HG) : 0u;
+  const uint32_t tmem_ncols = MMA == kMmaTmem ? (uint32_t)tmem_cols(D, HG, NBS) : 0u;
   uint32_t* const s_tmem = reinterpret_cast<uint32_t*>(smem + L.off_flag + 8);
 
   if (tid == 0) {
@@ -1643,6 +1860,156 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
       publish(row, flags, phys, 0xffff);
       return true;
     };
+
+    // The TMEM form packs up to NBS consecutive blocks of one segment into a
+    // stage and fills a stage in one pass: every lane issues the copies of
+    // its own unit of the window, lane 0 arms the stage's full barrier once
+    // with their bytes and publishes the stage (metadata, one arrival) when
+    // it is full or its segment ends.  Lane 0 keeps the open stage: its row,
+    // the flags of its first block, its blocks so far and their token masks.
+    int t_open = 0, t_nb = 0, t_row = 0, t_flags = 0, t_mask01 = 0, t_mask23 = 0;
+    bool t_data = false, t_gath = false;
+    const uint32_t t_vhalf = (uint32_t)HG * kBlock * 128;       // a block's V half
+    const uint32_t t_karea = (uint32_t)NBS * L.kv_bytes;
+    auto tmem_close = [&](int last_flags) {  // lane 0
+      const uint32_t s = n % S;
+      int f = t_flags | (last_flags & kLast);
+      if (t_data) f |= kData;
+      if (t_gath) f |= kGathered;
+      s_meta[2 * s] = make_int4(t_row, 0, slot0 + ((f & kSlot1) ? 1 : 0), f);
+      s_meta[2 * s + 1] = make_int4(t_mask01, t_mask23, t_nb, 0);
+      mbar_arrive(bars + 8 * s);
+      ++n;
+      t_open = 0;
+    };
+    // The warp gathers unit (row, blk) token by token (slot mode, a block
+    // whose slots are not one aligned run) into block b of stage slot s, in
+    // the layout the copies write; returns the mask of tokens gathered.
+    auto tmem_gather = [&](uint32_t s, int b, int row, int blk, int flags) -> int {
+      unsigned char* stg = smem + (size_t)s * L.stage_bytes;
+      const int64_t* sp = p.slots + (size_t)row * p.slot_stride + (size_t)blk * kBlock;
+      const int nval = min(kBlock, flags & 0xff);
+      const long long my = lane < nval ? sp[lane] : -1;
+      const bool in_pool = lane < nval && my >= 0 && my < p.pool_blocks * kBlock;
+      if (lane < nval && !in_pool) atomicOr(p.status, (uint32_t)NSV_DEV_BAD_BLOCK);
+      const int mask = (int)(__ballot_sync(kFull, in_pool) & 0xffffu);
+      const int kv0 = flags >> 16;
+      constexpr int kVpr = D * (int)sizeof(T) / 16;  // 16-byte vectors per token row
+      const int items = kBlock * HG * 2 * kVpr;
+      for (int it = lane; it < items; it += 32) {
+        const int vv = it % kVpr;
+        int rest = it / kVpr;
+        const int h = rest % HG;
+        rest /= HG;
+        const int which = rest & 1;  // 0: K, 1: V
+        const int t = rest >> 1;
+        if (!((mask >> t) & 1)) continue;
+        const long long sl = sp[t];
+        const T* src = (which ? vp : kp) +
+                       (((size_t)(sl / kBlock) * p.kv_heads + kv0 + h) * kBlock + sl % kBlock) * D;
+        const uint32_t dst = which ? t_karea + (uint32_t)b * L.kv_bytes +
+                                         swz(h * kBlock + t, vv, t_vhalf)
+                                   : swz_grouped<D>((b * HG + h) * kBlock + t, vv);
+        *reinterpret_cast<uint4*>(stg + dst) = *(reinterpret_cast<const uint4*>(src) + vv);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      return mask;
+    };
+    // One window of units (lane j holds unit w0 + j, nwin of them valid).
+    auto tmem_window = [&](int nwin, int u_row, int u_blk, int u_flags, int u_phys) -> bool {
+      const bool act = lane < nwin;
+      const bool tokw = act && u_phys == kTokenWise;
+      const bool valid = act && !tokw && u_phys >= 0 && (long long)u_phys < p.pool_blocks;
+      if (act && !tokw && !valid) atomicOr(p.status, (uint32_t)NSV_DEV_BAD_BLOCK);
+      const unsigned wk = __ballot_sync(kFull, (valid || tokw) && (u_flags >> 16) == 0);
+      if (lane == 0) walked += (unsigned long long)__popc(wk);
+      // this unit's index within its segment, modulo the stage size: the
+      // blocks before the window of a segment that continues into it are
+      // the open stage's (a closed stage holds NBS blocks)
+      const unsigned fm = __ballot_sync(kFull, act && (u_flags & kFirst));
+      const unsigned upto = fm & (0xffffffffu >> (31 - lane));  // firsts at lanes <= this one
+      const int c0 = __shfl_sync(kFull, t_nb, 0);
+      const int k = upto ? lane - (31 - __clz((int)upto)) : c0 + lane;
+      const bool ends = act && ((k % NBS) == NBS - 1 || (u_flags & kLast));
+      const unsigned em = __ballot_sync(kFull, ends);
+      int pos = 0;
+      while (pos < nwin) {
+        const unsigned rest = em & (0xffffffffu << pos);
+        const int e = rest ? __ffs((int)rest) - 1 : nwin - 1;
+        const int row0 = __shfl_sync(kFull, u_row, pos);
+        const int flags0 = __shfl_sync(kFull, u_flags, pos);
+        const int flags_e = __shfl_sync(kFull, u_flags, e);
+        bool ok2 = true;
+        if (lane == 0 && !t_open) {
+          ok2 = wait_free();
+          if (ok2) {
+            t_open = 1;
+            t_nb = 0;
+            t_row = row0;
+            t_flags = flags0 & ~(kLast | kData | kGathered);
+            t_mask01 = t_mask23 = 0;
+            t_data = t_gath = false;
+            if (flags0 & kHasQ) {
+              // the piece's query rows, which the softmax warps load when it
+              // starts: into L2 now, a few stages ahead of them
+              const int qh0 = (flags0 >> 16) * G;
+              for (int jq = 0; jq < NQ; ++jq)
+                prefetch_l2(qp + (((size_t)row0 * NQ + jq) * p.heads + qh0) * D,
+                            (uint32_t)(HG * G * D * sizeof(T)));
+            }
+          }
+        }
+        if (!__shfl_sync(kFull, ok2, 0)) return false;
+        const uint32_t s = __shfl_sync(kFull, n, 0) % S;
+        const int nb0 = __shfl_sync(kFull, t_nb, 0);
+        const bool mine = lane >= pos && lane <= e;
+        const int bl = nb0 + lane - pos;  // this unit's block within the stage
+        int mymask = (mine && valid) ? 0xffff : 0;
+        // copies: each lane its own unit's (K: one box per 64-dim half, V:
+        // one box of both halves)
+        const unsigned vm = __ballot_sync(kFull, mine && valid);
+        const uint32_t full = bars + 8 * s;
+        if (lane == 0 && vm) mbar_expect_tx(full, (uint32_t)__popc(vm) * 2u * L.kv_bytes);
+        if (mine && valid) {
+          const uint32_t base = smem_u32(smem + (size_t)s * L.stage_bytes);
+          const int y = (u_phys * p.kv_heads + (u_flags >> 16)) * kBlock;
+          tma_load_4d(base + (uint32_t)bl * L.kv_bytes, &p.tmap_k, 0, 0, 0, y >> 3, full, pol);
+          tma_load_3d(base + t_karea + (uint32_t)bl * L.kv_bytes, &p.tmap_v, 0, y, 0, full,
+                      pol);
+        }
+        // gathered units, one at a time with the whole warp
+        unsigned gm = __ballot_sync(kFull, mine && tokw);
+        while (gm) {
+          const int g = __ffs((int)gm) - 1;
+          gm &= gm - 1;
+          const int msk = tmem_gather(s, nb0 + g - pos, __shfl_sync(kFull, u_row, g),
+                                      __shfl_sync(kFull, u_blk, g),
+                                      __shfl_sync(kFull, u_flags, g));
+          if (lane == g) mymask = msk;
+        }
+        // the blocks' token masks, into lane 0's open stage
+        for (int j = pos; j <= e; ++j) {
+          const int mj = __shfl_sync(kFull, mymask, j);
+          if (lane == 0) {
+            const int bj = nb0 + j - pos;
+            if (bj < 2)
+              t_mask01 |= mj << (16 * bj);
+            else
+              t_mask23 |= mj << (16 * (bj - 2));
+            if (mj) t_data = true;
+          }
+        }
+        if (lane == 0) t_nb = nb0 + e - pos + 1;
+        const bool any_gath = __ballot_sync(kFull, mine && tokw) != 0;
+        if (lane == 0) {
+          if (any_gath) t_gath = true;
+          if (rest) tmem_close(flags_e);  // full, or the segment ends here
+        }
+        pos = e + 1;
+      }
+      return true;
+    };
     // Slot mode, a block whose slots are not one aligned run: the whole warp
     // gathers the block's tokens (every head of the group, K and V) into the
     // next stage with 16-byte loads and stores, then lane 0 publishes it with
@@ -1699,7 +2066,8 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
       int n_row = 0, n_blk = 0, n_flags = 0, n_phys = -1;
       if (nw0 + lane < end) unit_at(nw0 + lane, n_row, n_blk, n_flags, n_phys);
       const int nwin = (int)min(32ll, end - w0);
-      for (int jj = 0; jj < nwin && ok; ++jj) {
+      if constexpr (MMA == kMmaTmem) ok = tmem_window(nwin, c_row, c_blk, c_flags, c_phys);
+      for (int jj = 0; MMA != kMmaTmem && jj < nwin && ok; ++jj) {
         const int row = __shfl_sync(kFull, c_row, jj);
         int flags = __shfl_sync(kFull, c_flags, jj);
         const int phys = __shfl_sync(kFull, c_phys, jj);
@@ -1725,7 +2093,19 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
       c_phys = n_phys;
     }
     if (lane == 0) {
-      if (ok) ok = emit(0, kEnd, 0);
+      if constexpr (MMA == kMmaTmem) {
+        // every segment ended with its last unit, which closed its stage
+        if (ok) ok = wait_free();
+        if (ok) {
+          const uint32_t s = n % S;
+          s_meta[2 * s] = make_int4(0, 0, 0, kEnd);
+          s_meta[2 * s + 1] = make_int4(0, 0, 0, 0);
+          mbar_arrive(bars + 8 * s);
+          ++n;
+        }
+      } else {
+        if (ok) ok = emit(0, kEnd, 0);
+      }
       if (!ok) {
         atomicOr(p.status, (uint32_t)NSV_DEV_TIMEOUT);
         *s_abort = 1;

@@ -155,8 +155,53 @@ bool tensor_rows_fit(const nsv_shape* s) {
   return (s->num_blocks + 1) * (int64_t)s->num_kv_heads * kBlock < (int64_t(1) << 31);
 }
 
+// The TMEM form's sizes: its group, blocks per stage, ring and CTAs per SM.
+// One CTA per SM: its eight softmax warps, MMA warp and producer take most
+// of the register file, and a group of two KV heads at head_dim 128 takes
+// all 512 tensor-memory columns.
+int plan_tmem(const nsv_shape* s, int vpk, int* hg, int* bps, int* stages, int* cps) {
+  const int D = s->head_dim;
+  const int rows = s->rows > 0 ? s->rows : 1;
+  if (*hg <= 0)
+    *hg = tmem_group(s->num_kv_heads, vpk, D);
+  else if (!tmem_group_ok(*hg, s->num_kv_heads, vpk, D))
+    return NSV_ERR_RANGE;
+  if (*bps > 0 && !tmem_blocks_ok(D, *hg, *bps)) return NSV_ERR_RANGE;
+  if (*stages > 0 && (*stages < 2 || *stages > 8)) return NSV_ERR_RANGE;
+  if (*cps > 1) return NSV_ERR_RANGE;
+  const int nvec = *hg * vpk;
+  auto fits = [&](int b, int st) {
+    return make_layout(2, D, *hg, nvec, st, rows, kFormTmem, 1, b).total <=
+           (uint32_t)kSmemPerCta;
+  };
+  // By default the largest stage (up to 4 blocks) that still leaves a ring
+  // of 3, with the deepest ring (up to 6) that fits; else 2 stages.
+  const int b_hi = *bps > 0 ? *bps : kTmemMaxBlocks, b_lo = *bps > 0 ? *bps : 1;
+  for (int min_st : {3, 2}) {
+    for (int b = b_hi; b >= b_lo; --b) {
+      if (!tmem_blocks_ok(D, *hg, b)) continue;
+      int st = 0;
+      if (*stages > 0) {
+        st = fits(b, *stages) ? *stages : 0;
+      } else {
+        for (int k = 2; k <= 6; ++k)
+          if (fits(b, k)) st = k;
+        if (st < min_st) st = 0;
+      }
+      if (st) {
+        *bps = b;
+        *stages = st;
+        *cps = 1;
+        return NSV_OK;
+      }
+    }
+    if (*stages > 0) break;  // min_st does not apply to a fixed ring
+  }
+  return NSV_ERR_RANGE;
+}
+
 int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int grid, int qw,
-              int consumer, nsv_plan* p) {
+              int consumer, int bps, nsv_plan* p) {
   int rc = check_shape(s);
   if (rc) return rc;
   if (!p) return NSV_ERR_NULLPTR;
@@ -176,10 +221,15 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
     // tokens are the MMA rows (one warp per KV head); 9 to 16, the vectors
     // (16 per warp), which measured faster than 8 per warp with tokens as
     // rows; beyond, tcgen05 into tensor memory when the KV heads split into
-    // its groups (17-64 vectors: 1.0-1.9x the vectors-as-rows form's speed).
+    // its groups (at head_dim 128, 17-64 vectors: 1.0-1.9x the
+    // vectors-as-rows form's speed), except at head_dim 64 up to 32 vectors,
+    // where a stage's fixed cost weighs on its half-size blocks and the
+    // vectors as the rows measured faster (32 vectors on 8 KV heads: 400
+    // against 498 us).
     consumer = !(tensor_ok && qw <= 0) ? kConsumerCuda
                : vpk <= 8              ? kConsumerTensor
-               : (vpk > kMmaRows && tmem_group(s->num_kv_heads, vpk) >= 2)
+               : (vpk > kMmaRows && tmem_group(s->num_kv_heads, vpk, s->head_dim) >= 2 &&
+                  !(s->head_dim == 64 && vpk <= 32))
                    ? kConsumerTensorTmem
                    : kConsumerTensorVectorRows;
   } else if (consumer == kConsumerTensor || consumer == kConsumerTensorVectorRows ||
@@ -209,13 +259,11 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   const int max_warps = tensor ? kMaxConsumerWarpsMulti : max_consumer_warps(qw);
   const int tile = kBlock * s->head_dim * elem;
   const bool tmem_form = consumer == kConsumerTensorTmem;
+  if (!tmem_form && bps > 1) return NSV_ERR_RANGE;  // one block per stage
   if (tmem_form) {
-    // one 128-row MMA group per CTA: 4, 2 or 1 KV heads, each with 128 /
-    // group rows for its vectors
-    if (hg <= 0)
-      hg = tmem_group(s->num_kv_heads, vpk);
-    else if (!tmem_group_ok(hg, s->num_kv_heads, vpk))
-      return NSV_ERR_RANGE;
+    // one 128-row MMA group per CTA (4, 2 or 1 KV heads, each with 128 /
+    // group rows for its vectors), stages of up to 4 blocks
+    if ((rc = plan_tmem(s, vpk, &hg, &bps, &stages, &cps)) != NSV_OK) return rc;
   } else if (hg <= 0) {
     // Among 1 and the KV-head groups whose K+V stage stays within 64 KiB and
     // whose query vectors fill at most 8 consumer warps, the one whose plan keeps
@@ -232,7 +280,7 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
       if (c > 1 && (s->num_kv_heads % c != 0 || c * wpk > 8 || 2 * c * tile > 64 * 1024))
         continue;
       nsv_plan cand;
-      const int rc_c = make_plan(s, num_sms, c, stages, cps, grid, qw, consumer, &cand);
+      const int rc_c = make_plan(s, num_sms, c, stages, cps, grid, qw, consumer, 1, &cand);
       if (rc_c != NSV_OK) {
         if (best_warps == 0) best_rc = rc_c;
         continue;
@@ -249,16 +297,18 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   } else if (s->num_kv_heads % hg != 0 || hg * wpk > max_warps) {
     return NSV_ERR_RANGE;
   }
+  if (!tmem_form) bps = 1;
   const int nvec = hg * vpk;
   const int rows_for_layout = s->rows > 0 ? s->rows : 1;
-  const bool auto_stages = stages <= 0;
+  const bool auto_stages = stages <= 0 && !tmem_form;
   if (auto_stages) stages = 3;
   if (stages < 2 || stages > 8) return NSV_ERR_RANGE;
   const int form = form_of(consumer);
-  SmemLayout L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout, form, qw);
+  SmemLayout L =
+      make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout, form, qw, bps);
   while (auto_stages && L.total > (uint32_t)kSmemPerCta && stages > 2) {
     --stages;
-    L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout, form, qw);
+    L = make_layout(elem, s->head_dim, hg, nvec, stages, rows_for_layout, form, qw, bps);
   }
   if (L.total > (uint32_t)kSmemPerCta) return NSV_ERR_RANGE;
   const int threads =
@@ -271,20 +321,10 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   // The TMEM form's CTAs also share the SM's 512 tensor-memory columns.
   // (The device's occupancy calculator answers one CTA per SM for a kernel
   // that allocates tensor memory, however few columns it takes; two CTAs of
-  // 256 columns do run side by side: the 64-vector read takes 929 us with two
-  // per SM against 1540 us with one, on GB300.)
-  if (tmem_form) fit_threads = std::min(fit_threads, 512 / tmem_cols(s->head_dim, hg));
-  if (tmem_form && auto_stages && cps <= 0 && fit < 2 && fit_threads >= 2 && stages > 2) {
-    // Two CTAs with a 2-stage ring each beat one CTA with a deep one: each
-    // CTA's stage is a chain of dependent steps (MMA, softmax, MMA) that the
-    // other CTA's chain overlaps.
-    const SmemLayout L2 = make_layout(elem, s->head_dim, hg, nvec, 2, rows_for_layout, form, qw);
-    if (kSmemPerSm / (int)(L2.total + kSmemReserved) >= 2) {
-      stages = 2;
-      L = L2;
-      fit = kSmemPerSm / (int)(L.total + kSmemReserved);
-    }
-  }
+  // 256 columns do run side by side: an earlier one-block-per-stage version
+  // of the form read 64 vectors per KV head in 929 us with two per SM
+  // against 1540 us with one, on GB300.)
+  if (tmem_form) fit_threads = std::min(fit_threads, 512 / tmem_cols(s->head_dim, hg, bps));
   if (fit_threads < 1) return NSV_ERR_RANGE;  // one CTA would not fit the register file
   if (!tensor && auto_stages && cps <= 0 && stages == 3 && hg == s->num_kv_heads &&
       2 * hg * tile <= 16 * 1024) {
@@ -298,7 +338,8 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
     // measured against it.
     const int warps_cta = threads / 32 - 1;
     const int now = std::min({fit, fit_threads, kMaxCtasPerSm});
-    const SmemLayout L2 = make_layout(elem, s->head_dim, hg, nvec, 2, rows_for_layout, form, qw);
+    const SmemLayout L2 =
+        make_layout(elem, s->head_dim, hg, nvec, 2, rows_for_layout, form, qw, 1);
     const int fit2 = kSmemPerSm / (int)(L2.total + kSmemReserved);
     if (now * warps_cta < kEnoughWarpsPerSm &&
         std::min({fit2, fit_threads, kMaxCtasPerSm}) > now) {
@@ -307,13 +348,13 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
       fit = fit2;
     }
   }
-  if (tensor && auto_stages && cps <= 0 && std::min(fit, fit_threads) < 2) {
+  if (tensor && !tmem_form && auto_stages && cps <= 0 && std::min(fit, fit_threads) < 2) {
     // One CTA per SM either way: spend the rest of its shared memory on a
     // deeper ring (up to 6 stages), which keeps more bytes in flight for
     // the consumers that would otherwise wait on HBM latency.
     while (stages < 6) {
       const SmemLayout L2 =
-          make_layout(elem, s->head_dim, hg, nvec, stages + 1, rows_for_layout, form, qw);
+          make_layout(elem, s->head_dim, hg, nvec, stages + 1, rows_for_layout, form, qw, 1);
       if (L2.total > (uint32_t)kSmemPerCta) break;
       ++stages;
       L = L2;
@@ -345,6 +386,7 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
   p->num_sms = num_sms;
   p->vectors_per_warp = qw;
   p->consumer = consumer;
+  p->blocks_per_stage = bps;
   p->workspace_bytes = (int64_t)W.total;
   return NSV_OK;
 }
@@ -353,7 +395,7 @@ int make_plan(const nsv_shape* s, int num_sms, int hg, int stages, int cps, int 
 int check_plan(const nsv_shape* s, const nsv_plan* given, nsv_plan* use) {
   int rc = make_plan(s, given->num_sms, given->kv_heads_per_cta, given->stages,
                      given->ctas_per_sm, given->grid, given->vectors_per_warp,
-                     given->consumer, use);
+                     given->consumer, given->blocks_per_stage, use);
   if (rc) return rc;
   if (memcmp(use, given, sizeof(nsv_plan)) != 0) return NSV_ERR_RANGE;
   return NSV_OK;
@@ -417,7 +459,7 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   DeviceState* d = nullptr;
   if ((rc = device_state(&d)) != NSV_OK) return rc;
   if (!plan_in) {
-    if ((rc = make_plan(s, d->num_sms, 0, 0, 0, 0, 0, 0, &plan)) != NSV_OK) return rc;
+    if ((rc = make_plan(s, d->num_sms, 0, 0, 0, 0, 0, 0, 0, &plan)) != NSV_OK) return rc;
   }
   if (s->rows == 0) return NSV_OK;
   if (library_ws) {
@@ -468,24 +510,58 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
   p.group = s->num_heads / s->num_kv_heads;
   p.query_len = query_len(s);
   p.stages = plan.stages;
+  p.blocks_per_stage = plan.blocks_per_stage;
   p.qscale = scale * 1.4426950408889634f;  // log2(e): the kernels use exp2
   memset(&p.tmap_k, 0, sizeof(p.tmap_k));
   memset(&p.tmap_v, 0, sizeof(p.tmap_v));
   if (plan.consumer != kConsumerCuda) {
     // The pools as [(num_blocks+1)*kv_heads*16 rows][head_dim] bf16; a box is
     // 64 dims (128 bytes, the swizzle span) by the head group's 16-token tiles.
-    const cuuint64_t dims[2] = {(cuuint64_t)s->head_dim,
-                                (cuuint64_t)(s->num_blocks + 1) * s->num_kv_heads * kBlock};
+    const cuuint64_t rows = (cuuint64_t)(s->num_blocks + 1) * s->num_kv_heads * kBlock;
+    const cuuint64_t dims[2] = {(cuuint64_t)s->head_dim, rows};
     const cuuint64_t strides[1] = {(cuuint64_t)s->head_dim * 2};
     const cuuint32_t box[2] = {64u, (cuuint32_t)(plan.kv_heads_per_cta * kBlock)};
-    const cuuint32_t estr[2] = {1u, 1u};
-    for (int i = 0; i < 2; ++i) {
-      if (g_encode(i == 0 ? &p.tmap_k : &p.tmap_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                   const_cast<void*>(i == 0 ? k_pool : v_pool), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    if (plan.consumer == kConsumerTensorTmem) {
+      // K for the TMEM form: the rows seen as [64 dims][8 rows][64-dim
+      // halves][groups of 8 rows], so that one box lands a block's tiles as
+      // [group][half][8 rows][128 bytes], the layout whose groups the scores
+      // MMA steps through at one stride across all blocks of a stage.
+      const cuuint64_t dims4[4] = {64u, 8u, (cuuint64_t)(s->head_dim / 64), rows / 8};
+      const cuuint64_t strides4[3] = {(cuuint64_t)s->head_dim * 2, 128u,
+                                      (cuuint64_t)s->head_dim * 2 * 8};
+      const cuuint32_t box4[4] = {64u, 8u, (cuuint32_t)(s->head_dim / 64),
+                                  (cuuint32_t)(plan.kv_heads_per_cta * kBlock / 8)};
+      const cuuint32_t estr4[4] = {1u, 1u, 1u, 1u};
+      if (g_encode(&p.tmap_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(k_pool),
+                   dims4, strides4, box4, estr4, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return NSV_ERR_CUDA;
+    } else if (g_encode(&p.tmap_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(k_pool),
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      return NSV_ERR_CUDA;
+    }
+    if (plan.consumer == kConsumerTensorTmem) {
+      // V for the TMEM form: the same rows seen as [64 dims][rows][64-dim
+      // halves], so that one box (64 dims x the group's 16-token tiles x
+      // both halves) lands a block as [half][head][token][128 bytes].
+      const cuuint64_t dims3[3] = {64u, rows, (cuuint64_t)(s->head_dim / 64)};
+      const cuuint64_t strides3[2] = {(cuuint64_t)s->head_dim * 2, 128u};
+      const cuuint32_t box3[3] = {64u, (cuuint32_t)(plan.kv_heads_per_cta * kBlock),
+                                  (cuuint32_t)(s->head_dim / 64)};
+      if (g_encode(&p.tmap_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v_pool),
+                   dims3, strides3, box3, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return NSV_ERR_CUDA;
+    } else if (g_encode(&p.tmap_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(v_pool),
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      return NSV_ERR_CUDA;
     }
   }
   // The arrival counters of cut rows start every call at zero: zeroed by
@@ -531,14 +607,14 @@ NSV_API const char* nsv_strerror(int code) {
 }
 
 NSV_API int nsv_plan_split(const nsv_shape* shape, int num_sms, nsv_plan* plan) {
-  return make_plan(shape, num_sms, 0, 0, 0, 0, 0, 0, plan);
+  return make_plan(shape, num_sms, 0, 0, 0, 0, 0, 0, 0, plan);
 }
 
 NSV_API int nsv_plan_custom(const nsv_shape* shape, int num_sms, int kv_heads_per_cta,
                             int stages, int ctas_per_sm, int grid, int vectors_per_warp,
-                            int consumer, nsv_plan* plan) {
+                            int consumer, int blocks_per_stage, nsv_plan* plan) {
   return make_plan(shape, num_sms, kv_heads_per_cta, stages, ctas_per_sm, grid,
-                   vectors_per_warp, consumer, plan);
+                   vectors_per_warp, consumer, blocks_per_stage, plan);
 }
 
 NSV_API int nsv_plan_resident_ctas(const nsv_shape* shape, const nsv_plan* plan,

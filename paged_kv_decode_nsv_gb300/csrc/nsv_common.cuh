@@ -127,6 +127,7 @@ struct DecodeParams {
   int group;          // query heads per KV head
   int query_len;      // query tokens per row
   int stages;
+  int blocks_per_stage;  // blocks a stage holds (the TMEM form; 1 otherwise)
   float qscale;       // scale * log2(e)
 };
 
@@ -178,27 +179,57 @@ __host__ __device__ constexpr int form_of(int consumer) {
 
 // The TMEM form (tcgen05.mma, accumulators in tensor memory).  Its MMA has
 // 128 rows: each KV head of the CTA's group takes 128 / group of them (its
-// query vectors, the rest zero), and one MMA over the group's tokens serves
-// them all (each row uses its own head's 16 columns).  Four softmax warps,
-// one per TMEM lane quadrant; a thread owns one row.
-constexpr int kTmemWarps = 4;
+// query vectors, the rest zero).  A stage holds up to `blocks` consecutive
+// blocks of one segment, and one scores MMA per 16 dims covers all of them
+// (N = blocks x group x 16 tokens; each row uses its own head's columns).
+// The P.V MMA of a block is one instruction with N = group x head_dim: every
+// row's probabilities times every head's V, of which a row keeps its own
+// head's columns.  Eight softmax warps, two per TMEM lane quadrant: a pair
+// shares its quadrant's 32 rows (a thread owns one row) and splits each
+// stage's blocks.
+constexpr int kTmemWarps = 8;
 constexpr int kTmemRows = 128;
-// Whether `group` KV heads of `vpk` query vectors each can share the MMA.
-__host__ __device__ constexpr bool tmem_group_ok(int group, int kv_heads, int vpk) {
+constexpr int kTmemMaxBlocks = 4;  // blocks one stage holds at most
+// Whether `group` KV heads of `vpk` query vectors each can share the MMA:
+// 1, 2 or 4 heads dividing the KV heads, 128 / group rows for each head's
+// vectors, and a P.V product (group x head_dim columns) one MMA wide.
+__host__ __device__ constexpr bool tmem_group_ok(int group, int kv_heads, int vpk,
+                                                 int head_dim) {
   return (group == 1 || group == 2 || group == 4) && kv_heads % group == 0 &&
-         group * vpk <= kTmemRows;
+         group * vpk <= kTmemRows && group * head_dim <= 256;
 }
-// The default group: the largest of 4, 2 and 1 that fits.
-__host__ __device__ constexpr int tmem_group(int kv_heads, int vpk) {
-  return tmem_group_ok(4, kv_heads, vpk) ? 4 : tmem_group_ok(2, kv_heads, vpk) ? 2 : 1;
+// Whether a stage of `blocks` blocks fits the form: its scores MMA at most
+// 256 columns wide and all its columns within the SM's 512.
+__host__ __device__ constexpr bool tmem_blocks_ok(int head_dim, int group, int blocks);
+// The default group: the largest of 4, 2 and 1 that fits with stages of at
+// least 3 blocks (a stage's fixed cost is what bounds the form; see the
+// planner), else the largest that fits.
+__host__ __device__ constexpr int tmem_group(int kv_heads, int vpk, int head_dim) {
+  return (tmem_group_ok(4, kv_heads, vpk, head_dim) && tmem_blocks_ok(head_dim, 4, 3))   ? 4
+         : (tmem_group_ok(2, kv_heads, vpk, head_dim) && tmem_blocks_ok(head_dim, 2, 3)) ? 2
+         : tmem_group_ok(4, kv_heads, vpk, head_dim)                                     ? 4
+         : tmem_group_ok(2, kv_heads, vpk, head_dim)                                     ? 2
+                                                                                         : 1;
 }
-// Tensor-memory columns a CTA allocates (a power of two, at least 32): the
-// output accumulator (head_dim columns) and two score buffers (16 columns
-// per KV head of the group each).
-__host__ __device__ constexpr int tmem_cols(int head_dim, int group) {
-  return head_dim + 2 * group * kBlock <= 128 ? 128
-         : head_dim + 2 * group * kBlock <= 256 ? 256
-                                               : 512;
+// Tensor-memory columns the form uses: the output accumulator (group x
+// head_dim), two score buffers (blocks x group x 16 each) and the query rows
+// (head_dim bf16, two to a column), the scores MMA's A operand.
+__host__ __device__ constexpr int tmem_cols_used(int head_dim, int group, int blocks) {
+  return group * head_dim + 2 * blocks * group * kBlock + head_dim / 2;
+}
+// What a CTA allocates: that, rounded up to a power of two (at least 32).
+__host__ __device__ constexpr int tmem_cols(int head_dim, int group, int blocks) {
+  return tmem_cols_used(head_dim, group, blocks) <= 32    ? 32
+         : tmem_cols_used(head_dim, group, blocks) <= 64  ? 64
+         : tmem_cols_used(head_dim, group, blocks) <= 128 ? 128
+         : tmem_cols_used(head_dim, group, blocks) <= 256 ? 256
+                                                          : 512;
+}
+// Whether a stage of `blocks` blocks fits the form: its scores MMA at most
+// 256 columns wide and all its columns within the SM's 512.
+__host__ __device__ constexpr bool tmem_blocks_ok(int head_dim, int group, int blocks) {
+  return blocks >= 1 && blocks <= kTmemMaxBlocks && blocks * group * kBlock <= 256 &&
+         tmem_cols_used(head_dim, group, blocks) <= 512;
 }
 
 // Whether a variant keeps its consumer warps off the producer's SM
@@ -240,33 +271,38 @@ __host__ __device__ inline int q_slots_for(uint32_t q_bytes, int stages, int for
 }
 
 // The CUDA-core consumer also keeps per-vector probability buffers (the
-// tensor-core forms hold probabilities in registers).
+// tensor-core forms hold probabilities in registers).  `blocks` is the
+// blocks a stage holds (1 outside the TMEM form).
 __host__ __device__ inline SmemLayout make_layout(int elem, int head_dim, int heads_per_cta,
                                                   int nvec, int stages, int rows, int form,
-                                                  int qw) {
+                                                  int qw, int blocks) {
   SmemLayout L;
   L.kv_bytes = (uint32_t)(heads_per_cta * kBlock * head_dim * elem);
   L.q_bytes = (uint32_t)(nvec * head_dim * elem);
   // Stages start on 1024-byte boundaries: 128-byte-swizzled TMA writes
   // need it (the kernel aligns the dynamic shared memory base itself).
-  L.stage_bytes = align_up(2 * L.kv_bytes, 1024);
+  L.stage_bytes = align_up(2 * (uint32_t)blocks * L.kv_bytes, 1024);
   L.q_slots = (uint32_t)q_slots_for(L.q_bytes, stages, form, qw);
   L.q_slot_bytes = align_up(L.q_bytes, 128);
   L.off_q = (uint32_t)stages * L.stage_bytes;
   uint32_t off = L.off_q + L.q_slots * L.q_slot_bytes;
   L.off_meta = off;
-  off += (uint32_t)stages * 16;
+  // an int4 per stage; the TMEM form adds one for its blocks' token masks
+  off += (uint32_t)stages * (form == kFormTmem ? 32 : 16);
   L.off_bars = align_up(off, 8);
   // mbarriers: full[stages], empty[stages], qfree[q_slots]; the TMEM form
-  // adds three (scores ready, output ready, drained)
+  // adds seven (scores ready [2], handed over [2], output ready, drained,
+  // query rows ready)
   off = L.off_bars + (uint32_t)(2 * stages + (int)L.q_slots + (form == kFormTmem ? 7 : 0)) * 8;
   if (form == kFormTmem) {
-    // its MMA operands: the query rows (128 x head_dim, 128-byte swizzle,
-    // 1024-byte aligned) and two probability buffers (128 x the group's
-    // tokens each)
+    // its shared-memory MMA operand: two probability buffers (128 x a
+    // stage's tokens of one head each; the query rows live in tensor
+    // memory); then the softmax warp pairs' exchange of row maxima (two
+    // stages x two warps x 128 rows) and of row sums (two pieces x two warps
+    // x 128 rows)
     L.off_pbuf = align_up(off, 1024);
-    off = L.off_pbuf + (uint32_t)(kTmemRows * head_dim * 2) +
-          2u * (uint32_t)(kTmemRows * heads_per_cta * kBlock * 2);
+    off = L.off_pbuf + 2u * (uint32_t)(kTmemRows * blocks * kBlock * 2) +
+          (4u + 4u) * kTmemRows * 4u;
   } else {
     L.off_pbuf = align_up(off, 16);
     off = L.off_pbuf + (form == kFormCuda ? (uint32_t)(nvec * kBlock * 4) : 0u);

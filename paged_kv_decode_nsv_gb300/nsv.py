@@ -53,7 +53,7 @@ class Plan(ctypes.Structure):
                 ("ctas_per_sm", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("num_sms", ctypes.c_int32), ("vectors_per_warp", ctypes.c_int32),
-                ("consumer", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("consumer", ctypes.c_int32), ("blocks_per_stage", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self):
@@ -73,7 +73,7 @@ _lib.nsv_strerror.argtypes = [_i32]
 _lib.nsv_plan_split.restype = _i32
 _lib.nsv_plan_split.argtypes = [_SP, _i32, _PP]
 _lib.nsv_plan_custom.restype = _i32
-_lib.nsv_plan_custom.argtypes = [_SP, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _PP]
+_lib.nsv_plan_custom.argtypes = [_SP, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _PP]
 _lib.nsv_plan_resident_ctas.restype = _i32
 _lib.nsv_plan_resident_ctas.argtypes = [_SP, _PP, ctypes.POINTER(ctypes.c_int)]
 _lib.nsv_kv_write.restype = _i32
@@ -180,11 +180,12 @@ def plan_split(shape, num_sms=0):
 
 
 def plan_custom(shape, num_sms=0, kv_heads_per_cta=0, stages=0, ctas_per_sm=0, grid=0,
-                vectors_per_warp=0, consumer=CONSUMER_AUTO):
+                vectors_per_warp=0, consumer=CONSUMER_AUTO, blocks_per_stage=0):
     p = Plan()
     _check(_lib.nsv_plan_custom(ctypes.byref(shape), int(num_sms), int(kv_heads_per_cta),
                                 int(stages), int(ctas_per_sm), int(grid), int(vectors_per_warp),
-                                int(consumer), ctypes.byref(p)), "nsv_plan_custom")
+                                int(consumer), int(blocks_per_stage), ctypes.byref(p)),
+           "nsv_plan_custom")
     return p
 
 

@@ -61,7 +61,7 @@ def _cta_warps(nsv, consumer, consumer_warps, head_dim=128):
     vectors as the MMA rows at head_dim 128, an idle warp at each multiple of
     4 the consumers pass (none shares the producer's sub-partition)."""
     if consumer == nsv.CONSUMER_TENSOR_TMEM:
-        return 6      # a producer, four softmax warps and an MMA warp
+        return 10     # a producer, eight softmax warps and an MMA warp
     if consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS and head_dim == 128:
         return consumer_warps + 1 + (consumer_warps - 1) // 3
     return consumer_warps + 1
@@ -175,32 +175,44 @@ def test_plan_refuses_too_many_query_vectors(nsv, heads, kv_heads, qlen, dtype):
 
 
 def test_odd_vector_counts_above_15_run_on_the_tensor_cores(nsv):
-    # 32 KV heads split into the TMEM form's groups of 4 (17 vectors each)
+    # 32 KV heads split into the TMEM form's groups of 2 (17 vectors each; a
+    # group's P.V output, group x head_dim columns, is one MMA wide)
     p = nsv.plan_split(_shape(nsv, query_len=17), num_sms=152)
-    assert p.consumer == nsv.CONSUMER_TENSOR_TMEM and p.kv_heads_per_cta == 4
+    assert p.consumer == nsv.CONSUMER_TENSOR_TMEM and p.kv_heads_per_cta == 2
     # 5 KV heads split into no group of 2 or 4: two vectors-as-rows warps per KV head
     p = nsv.plan_split(_shape(nsv, num_heads=5, num_kv_heads=5, query_len=17), num_sms=152)
     assert p.consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS
     assert p.threads == _cta_warps(nsv, p.consumer, p.kv_heads_per_cta * 2) * 32
 
 
-@pytest.mark.parametrize("heads,kv_heads,qlen,head_dim,group,cps", [
-    (32, 8, 8, 128, 4, 1), (64, 8, 8, 128, 2, 2), (32, 8, 1, 128, 4, 1), (32, 8, 9, 128, 2, 2),
-    (8, 8, 17, 128, 4, 1), (32, 8, 8, 64, 4, 2), (64, 8, 8, 64, 2, 2), (24, 6, 5, 128, 2, 2),
-    (64, 1, 1, 128, 1, 2), (20, 5, 5, 64, 1, 2)])
-def test_plan_tmem_form(nsv, heads, kv_heads, qlen, head_dim, group, cps):
+def _tmem_cols(head_dim, group, blocks):
+    used = group * head_dim + 2 * blocks * group * 16 + head_dim // 2
+    return next(c for c in (32, 64, 128, 256, 512) if used <= c)
+
+
+@pytest.mark.parametrize("heads,kv_heads,qlen,head_dim,group,blocks,stages,cps", [
+    (32, 8, 8, 128, 2, 3, 4, 1), (64, 8, 8, 128, 2, 3, 4, 1), (32, 8, 1, 128, 2, 3, 4, 1),
+    (32, 8, 9, 128, 2, 3, 4, 1), (8, 8, 17, 128, 2, 3, 4, 1), (32, 8, 8, 64, 2, 4, 5, 1),
+    (64, 8, 8, 64, 2, 4, 5, 1), (24, 6, 5, 128, 2, 3, 4, 1), (64, 1, 1, 128, 1, 4, 5, 1),
+    (20, 5, 5, 64, 1, 4, 6, 1)])
+def test_plan_tmem_form(nsv, heads, kv_heads, qlen, head_dim, group, blocks, stages, cps):
     """NSV_CONSUMER_TENSOR_TMEM: one 128-row MMA group per CTA (the largest of
-    4, 2 or 1 KV heads that divides the KV heads and leaves each head rows for
-    its vectors), a producer, four softmax warps and an MMA warp; two CTAs per
-    SM where their shared memory fits, as their 256 (head_dim 128) or 128
-    tensor-memory columns do."""
+    4, 2 or 1 KV heads that divides the KV heads, leaves each head rows for
+    its vectors, keeps group x head_dim within one MMA's 256 columns and
+    leaves tensor memory for stages of 3 blocks), a producer, eight softmax
+    warps and an MMA warp, one CTA per SM; stages of 1 to 4 blocks: the
+    largest that leaves a ring of 3, with the deepest ring (up to 6) that
+    fits.  Tensor memory holds O, two score buffers and the query rows."""
     p = nsv.plan_custom(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen,
                                head_dim=head_dim),
                         num_sms=152, consumer=nsv.CONSUMER_TENSOR_TMEM)
     assert p.consumer == nsv.CONSUMER_TENSOR_TMEM and p.kv_heads_per_cta == group
-    assert p.threads == 6 * 32 and p.vectors_per_warp == 1
+    assert p.threads == 10 * 32 and p.vectors_per_warp == 1
+    assert (p.blocks_per_stage, p.stages) == (blocks, stages)
     assert p.ctas_per_sm == cps and p.grid == 152 * cps
-    assert cps == 1 or 2 * (p.smem_bytes + 1024) <= 228 * 1024
+    assert p.smem_bytes <= 227 * 1024 and cps * (p.smem_bytes + 1024) <= 228 * 1024
+    assert cps * _tmem_cols(head_dim, group, blocks) <= 512
+    assert blocks * group * 16 <= 256 and group * head_dim <= 256
 
 
 @pytest.mark.parametrize("qlen,warps", [(2, 1), (16, 1), (17, 2), (32, 2)])
@@ -218,10 +230,10 @@ def test_plan_vector_rows_form(nsv, qlen, warps):
     (32, 32, 4, "bf16", 2, 8, 8),    # 4 query tokens
     (32, 32, 3, "bf16", 2, 8, 8),
     (16, 1, 1, "bf16", 3, 1, 1),     # 16 vectors: one warp, vectors as the MMA rows
-    (32, 8, 8, "bf16", 4, 4, 6),     # 32 vectors: tcgen05, 4 KV heads of 32 rows
-    (32, 8, 5, "bf16", 4, 4, 6),     # 20 vectors
-    (64, 8, 8, "bf16", 4, 2, 6),     # 64 vectors: 2 KV heads of 64 rows
-    (24, 6, 5, "bf16", 4, 2, 6),     # 20 vectors, 6 KV heads: groups of 2 (64 rows each)
+    (32, 8, 8, "bf16", 4, 2, 10),    # 32 vectors: tcgen05, 2 KV heads of 64 rows
+    (32, 8, 5, "bf16", 4, 2, 10),    # 20 vectors
+    (64, 8, 8, "bf16", 4, 2, 10),    # 64 vectors: 2 KV heads of 64 rows
+    (24, 6, 5, "bf16", 4, 2, 10),    # 20 vectors, 6 KV heads: groups of 2 (64 rows each)
     (20, 5, 5, "bf16", 3, 1, 2),     # 20 vectors, 5 KV heads: no group of 2 or 4
     (32, 8, 1, "f32", 1, 4, 8),      # fp32 stays on the CUDA cores
 ])
@@ -237,7 +249,7 @@ def test_plan_consumer_choice(nsv, heads, kv_heads, qlen, dtype, consumer, hg, w
     assert p.threads == _cta_warps(nsv, consumer, warps) * 32
     if consumer != nsv.CONSUMER_CUDA:
         assert p.vectors_per_warp == 1
-    assert p.reserved == 0
+    assert (p.blocks_per_stage > 1) == (consumer == nsv.CONSUMER_TENSOR_TMEM)
 
 
 @pytest.mark.parametrize("kw,ckw", [
@@ -248,7 +260,13 @@ def test_plan_consumer_choice(nsv, heads, kv_heads, qlen, dtype, consumer, hg, w
     (dict(num_kv_heads=8, dtype=0), dict(consumer=4)),              # fp32
     (dict(num_heads=24, num_kv_heads=6), dict(consumer=4, kv_heads_per_cta=4)),  # 4 does not divide 6
     (dict(num_kv_heads=8, query_len=9), dict(consumer=4, kv_heads_per_cta=4)),   # 4 x 36 rows > 128
-    (dict(num_kv_heads=8), dict(consumer=4, kv_heads_per_cta=8)),   # its group is 4 heads
+    (dict(num_kv_heads=8), dict(consumer=4, kv_heads_per_cta=8)),   # its group is 4 heads at most
+    (dict(num_kv_heads=8, num_heads=64), dict(consumer=4, kv_heads_per_cta=4)),  # 4 x 128 > 256 columns
+    (dict(num_kv_heads=8, num_heads=64), dict(consumer=4, blocks_per_stage=5)),  # at most 4 blocks
+    (dict(num_kv_heads=8, num_heads=64, head_dim=64), dict(consumer=4, kv_heads_per_cta=4,
+                                                          blocks_per_stage=3)),   # 640 TMEM columns
+    (dict(num_kv_heads=8), dict(consumer=2, blocks_per_stage=2)),   # one block per stage
+    (dict(num_kv_heads=8, num_heads=64), dict(consumer=4, ctas_per_sm=2)),  # one CTA per SM
     (dict(num_kv_heads=8, dtype=0), dict(consumer=3)),              # fp32
     (dict(num_kv_heads=8, num_blocks=(1 << 24)), dict(consumer=2)), # TMA row index overflows
 ])
@@ -399,7 +417,10 @@ def test_every_plan_round_trips(nsv):
                 for extra in (dict(), dict(consumer=1), dict(consumer=2), dict(consumer=3),
                               dict(consumer=1, vectors_per_warp=4), dict(kv_heads_per_cta=1),
                               dict(kv_heads_per_cta=2, ctas_per_sm=2), dict(stages=2),
-                              dict(consumer=4), dict(consumer=4, kv_heads_per_cta=1)):
+                              dict(consumer=4), dict(consumer=4, kv_heads_per_cta=1),
+                              dict(consumer=4, blocks_per_stage=1),
+                              dict(consumer=4, blocks_per_stage=2, stages=4),
+                              dict(consumer=4, blocks_per_stage=4)):
                     try:
                         p = nsv.plan_custom(shape, num_sms=152, **extra)
                     except nsv.NsvError:
@@ -408,7 +429,8 @@ def test_every_plan_round_trips(nsv):
                                         kv_heads_per_cta=p.kv_heads_per_cta, stages=p.stages,
                                         ctas_per_sm=p.ctas_per_sm, grid=p.grid,
                                         vectors_per_warp=p.vectors_per_warp,
-                                        consumer=p.consumer)
+                                        consumer=p.consumer,
+                                        blocks_per_stage=p.blocks_per_stage)
                     assert bytes(q) == bytes(p), (heads, kv, ql, dtype, d, extra)
                     checked += 1
     assert checked > 150
@@ -426,7 +448,22 @@ def test_bf16_takes_up_to_64_vectors_per_kv_head(nsv, heads, kv_heads, qlen):
     assert vpk > 32
     if kv_heads % 2 == 0:
         assert p.consumer == nsv.CONSUMER_TENSOR_TMEM and p.kv_heads_per_cta == 2
-        assert p.threads == 6 * 32
+        assert p.threads == 10 * 32
     else:
         assert p.consumer == nsv.CONSUMER_TENSOR_VECTOR_ROWS
         assert p.threads == _cta_warps(nsv, p.consumer, p.kv_heads_per_cta * -(-vpk // 16)) * 32
+
+
+@pytest.mark.parametrize("heads,kv_heads,qlen,consumer", [
+    (32, 8, 8, 3),    # head_dim 64, 32 vectors: the vectors as the MMA rows
+    (16, 4, 5, 3),    # 20 vectors
+    (64, 8, 8, 4),    # 64 vectors: tcgen05 into tensor memory
+    (40, 4, 4, 4),    # 40 vectors
+])
+def test_plan_head_dim_64_tmem_rule(nsv, heads, kv_heads, qlen, consumer):
+    """At head_dim 64 the TMEM form is the default only beyond 32 vectors per
+    KV head: up to 32, its stages' fixed cost on half-size blocks left it
+    behind the vectors-as-rows form."""
+    p = nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen,
+                              head_dim=64), num_sms=152)
+    assert p.consumer == consumer

@@ -8,7 +8,8 @@ columns, 8 per warp (NSV_CONSUMER_TENSOR, the default up to 8 vectors per
 KV head); or the vectors as the rows, 16 per warp
 (NSV_CONSUMER_TENSOR_VECTOR_ROWS, the default beyond); or tcgen05.mma into
 tensor memory with 128 MMA rows shared by 4 KV heads of up to 32 vectors or
-2 of up to 64 (NSV_CONSUMER_TENSOR_TMEM).  Every test runs all three, up to
+2 of up to 64 (NSV_CONSUMER_TENSOR_TMEM), a stage holding up to 4 blocks of a
+row.  Every test runs all three, up to
 64 vectors per KV head; the TMEM form skips shapes whose KV heads do not
 split into its groups."""
 
@@ -221,3 +222,35 @@ def test_tensor_forms_skip_a_bad_block_mid_row(nsv, consumer):
     assert st & nsv.DEV_BAD_BLOCK
     keep = [0, 2, 3]
     assert_parity("bf16", out[keep], ref[keep])
+
+
+@pytest.mark.parametrize("grid", [0, 7], ids=["grid_default", "grid_7"])
+@pytest.mark.parametrize("blocks,stages", [(1, 2), (1, 5), (2, 3), (2, 4), (3, 2), (3, 3),
+                                           (4, 2)])
+@pytest.mark.parametrize("heads,kv_heads,qlen,head_dim", [
+    (64, 8, 8, 128),    # 64 vectors per KV head, groups of 2
+    (32, 8, 5, 128),    # 20 vectors
+    (64, 1, 1, 128),    # one KV head: a group of 1
+    (32, 8, 8, 64),     # head_dim 64, groups of 4
+    (20, 5, 5, 64),     # 5 KV heads: groups of 1
+])
+def test_tmem_stage_sizes(nsv, grid, blocks, stages, heads, kv_heads, qlen, head_dim):
+    """The TMEM form with every stage size (1 to 4 consecutive blocks of a
+    row per stage, fewer where a segment ends) and several ring depths,
+    against the oracle.  The lengths end mid-block, on block and on stage
+    boundaries; a grid of 7 CTAs also cuts rows between CTAs, so pieces start
+    and end inside a stage's reach."""
+    wl = _case(heads, kv_heads, qlen, head_dim, seed=31)
+    inp = device_inputs(wl)
+    host = host_copy(inp)
+    try:
+        plan = _plan(nsv, inp, consumer=nsv.CONSUMER_TENSOR_TMEM, blocks_per_stage=blocks,
+                     stages=stages, grid=grid)
+    except nsv.NsvError as e:   # the stage does not fit shared or tensor memory
+        assert e.code == -5
+        pytest.skip("stage size does not fit this shape")
+    assert plan.blocks_per_stage == blocks and plan.stages == stages
+    out = gpu_read(wl, inp, plan=plan)
+    st, walked = status()
+    assert st == 0 and walked == oracle.walked_tiles(wl.context_lens, 16)
+    assert_parity("bf16", gpu_out_f64(out), oracle_read(wl, host))
