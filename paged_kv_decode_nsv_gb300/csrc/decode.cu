@@ -540,6 +540,8 @@ __device__ __forceinline__ void finish_cut_row(const DecodeParams& p, int row, i
   const int pr = s_prefix[row], nb = s_prefix[row + 1] - pr;
   const long long u0 = (long long)hg * N + pr, u1 = u0 + nb;
   const int c0 = cta_of(u0, U, gridDim.x), c1 = cta_of(u1 - 1, U, gridDim.x);
+  // (The counters are written by the step's append; this comes after the
+  // piece's stages, so after the producer's wait for the append.)
   if (cw == 0 && lane == 0) {
     int pieces = c1 - c0 + 1;
     if (U < gridDim.x) {  // some CTAs have no units and wrote nothing
@@ -2059,6 +2061,14 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
     // Everything so far read only the step's inputs (lengths, block tables
     // or slots).  The pools and the arrival counters may still be being
     // written by the step's append: wait for it before the first copy.
+    // Only this warp waits.  The consumer warps are ordered after it
+    // because everything they read or write that the append writes comes
+    // after data this warp copied following the wait: K/V through the
+    // stages' full barriers, and the arrival counters, which a consumer
+    // touches only in finish_cut_row, after its piece's last stage arrived.
+    // (griddepcontrol.wait makes the prerequisite grid's writes visible to
+    // the whole dependent grid.)  A consumer path that touched the pools or
+    // the counters before its first stage would have to wait as well.
     griddep_wait();
     while (w0 < end && ok) {
       // Prefetch the next window's units while this one is issued.
