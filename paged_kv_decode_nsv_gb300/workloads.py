@@ -272,6 +272,18 @@ def manyrow_gqa4_bf16(seed=3):
                  block_size=16, max_blocks=128, dtype="bf16", lens=lens, free_frac=0.10, rng=rng)
 
 
+def manyrow_gqa16_bf16(seed=3):
+    """The many-row batch with 16 query vectors per KV head: 64 query heads
+    share 4 KV heads.  The default plan
+    runs it with the vectors as the MMA rows (mma.sync), so it is the capture
+    case of that form; 0.35 GB per read."""
+    rng = np.random.default_rng(seed)
+    real = np.concatenate([[2048], _log_uniform(rng, 239, 128, 2048)])
+    lens = np.concatenate([real, np.zeros(16, dtype=np.int64)])
+    return _make("manyrow_gqa16_bf16", seed, rows=256, heads=64, kv_heads=4, head_dim=128,
+                 block_size=16, max_blocks=128, dtype="bf16", lens=lens, free_frac=0.10, rng=rng)
+
+
 def headline_mqa8_bf16(seed=4):
     """The headline batch as one tensor-parallel shard of a grouped-query
     model: 8 query heads share the shard's single KV head; same lengths and
@@ -295,6 +307,7 @@ WORKLOADS = {
     "headline_gqa8_spec8_bf16": headline_gqa8_spec8_bf16,
     "manyrow_gqa8_spec8_bf16": manyrow_gqa8_spec8_bf16,
     "headline_mqa8_bf16": headline_mqa8_bf16,
+    "manyrow_gqa16_bf16": manyrow_gqa16_bf16,
 }
 
 
