@@ -526,8 +526,10 @@ __device__ __forceinline__ int cta_of(long long u, long long U, int G) {
 // lie on CTAs c0..c1).  Count this CTA's piece once it is published; the CTA
 // whose piece arrives last merges every piece, each of its warps for its own
 // query vectors [v0, v0 + nv).  Nobody waits for another CTA: the last
-// arrival finds every partial already written.
-template <typename T, int D>
+// arrival finds every partial already written.  kLanes: lanes per query
+// vector in the merge (32 / kLanes vectors at a time); kChunk: pieces whose
+// loads are in flight together.
+template <typename T, int D, int kLanes, int kChunk>
 __device__ __forceinline__ void finish_cut_row(const DecodeParams& p, int row, int kv0,
                                                const int* s_prefix, int N, long long U, int nhg,
                                                int nvec, int v0, int nv, int ncw, int cw,
@@ -557,75 +559,102 @@ __device__ __forceinline__ void finish_cut_row(const DecodeParams& p, int row, i
   }
   consumer_sync(ncw * 32);
   if (!*s_merge) return;
-  // Lane l owns dims [l*D/32, (l+1)*D/32).
   __threadfence();
-  constexpr int kPer = D / 32;
+  // 32 / kLpv vectors at a time, kLpv lanes each; lane dq of a vector owns
+  // dims [dq*kDl, (dq+1)*kDl).  Every load of a step is independent of the
+  // others, so merging a batch of vectors costs about 1 + ns/kChunk L2 round
+  // trips (the partials were just written by other CTAs: read through L2).
+  constexpr int kLpv = kLanes < D / 4 ? kLanes : D / 4;
+  constexpr int kDl = D / kLpv;
+  constexpr int kF4 = kDl / 4;
   const int ns = c1 - c0 + 1;
   const int qh0 = kv0 * G;
-  for (int k = 0; k < nv; ++k) {
-    const int vv = v0 + k;
+  const int j = lane / kLpv, dq = lane % kLpv;
+  // slot of the k-th CTA's piece, or -1 for a CTA with no units
+  auto slot_of = [&](int kk) {
+    const int c = c0 + kk;
+    const long long sc = (long long)c * U / gridDim.x;
+    if ((long long)(c + 1) * U / gridDim.x == sc) return -1;
+    return c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
+  };
+  // the first kLpv pieces' slots, one per lane of a vector's group; later
+  // pieces (a row cut into many) are found again where they are needed
+  const int sl_own = dq < ns ? slot_of(dq) : -1;
+  const int g0 = lane & ~(kLpv - 1);
+  auto slot_k = [&](int kk) {  // kk is warp-uniform
+    const int sl = __shfl_sync(kFull, sl_own, g0 + (kk & (kLpv - 1)));
+    return kk < kLpv ? sl : slot_of(kk);
+  };
+  for (int k0 = 0; k0 < nv; k0 += 32 / kLpv) {
+    const bool vok = k0 + j < nv;
+    const int vv = v0 + (vok ? k0 + j : 0);
+    // the pieces' combined max and denominator: the vector's lanes take
+    // every eighth piece, then fold their (max, sum) pairs together
+    float M = -INFINITY, Ls = 0.f;
+    for (int kk = dq; kk < ns; kk += kLpv) {
+      const int sl = kk < kLpv ? sl_own : slot_of(kk);
+      if (sl < 0) continue;
+      const float2 ml = __ldcg(&p.ws_ml[(size_t)sl * nvec + vv]);
+      if (ml.x == -INFINITY) continue;
+      const float mn = fmaxf(M, ml.x);
+      Ls = Ls * exp2f(M - mn) + ml.y * exp2f(ml.x - mn);
+      M = mn;
+    }
+#pragma unroll
+    for (int o2 = 1; o2 < kLpv; o2 <<= 1) {
+      const float Mo = __shfl_xor_sync(kFull, M, o2), Lo = __shfl_xor_sync(kFull, Ls, o2);
+      const float mn = fmaxf(M, Mo);
+      if (mn != -INFINITY) {
+        Ls = (M == -INFINITY ? 0.f : Ls * exp2f(M - mn)) + (Mo == -INFINITY ? 0.f : Lo * exp2f(Mo - mn));
+        M = mn;
+      }
+    }
+    float a[kDl];
+#pragma unroll
+    for (int e = 0; e < kDl; ++e) a[e] = 0.f;
+    for (int kk0 = 0; kk0 < ns; kk0 += kChunk) {
+      float2 ml[kChunk];
+      float4 v[kChunk][kF4];
+#pragma unroll
+      for (int u = 0; u < kChunk; ++u) {
+        const int sl = kk0 + u < ns ? slot_k(kk0 + u) : -1;
+        const size_t idx = (size_t)(sl < 0 ? 0 : sl) * nvec + vv;
+        ml[u] = sl < 0 ? make_float2(-INFINITY, 0.f) : __ldcg(&p.ws_ml[idx]);
+        const float4* src = reinterpret_cast<const float4*>(p.ws_acc + idx * D + dq * kDl);
+#pragma unroll
+        for (int f = 0; f < kF4; ++f) v[u][f] = sl < 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldcg(src + f);
+      }
+#pragma unroll
+      for (int u = 0; u < kChunk; ++u) {
+        const float w = ml[u].x == -INFINITY ? 0.f : exp2f(ml[u].x - M);
+#pragma unroll
+        for (int f = 0; f < kF4; ++f) {
+          a[4 * f] = fmaf(w, v[u][f].x, a[4 * f]);
+          a[4 * f + 1] = fmaf(w, v[u][f].y, a[4 * f + 1]);
+          a[4 * f + 2] = fmaf(w, v[u][f].z, a[4 * f + 2]);
+          a[4 * f + 3] = fmaf(w, v[u][f].w, a[4 * f + 3]);
+        }
+      }
+    }
+    if (!vok) continue;
     const int kvl = vv / vpk, rem = vv - kvl * vpk;
     const int qh = qh0 + kvl * G + rem / NQ, jq = rem % NQ;
-    float M = -INFINITY;
-    for (int kk = lane; kk < ns; kk += 32) {
-      const int c = c0 + kk;
-      const long long sc = (long long)c * U / gridDim.x;
-      if ((long long)(c + 1) * U / gridDim.x == sc) continue;  // CTA with no units
-      const int sl = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
-      M = fmaxf(M, __ldcg(&p.ws_ml[(size_t)sl * nvec + vv]).x);
-    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    T* o = static_cast<T*>(p.out) + (((size_t)row * NQ + jq) * p.heads + qh) * D + dq * kDl;
+    if constexpr (sizeof(T) == 4) {
 #pragma unroll
-    for (int o2 = 16; o2 >= 1; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
-    float Lsum = 0.f, a[kPer];
+      for (int f = 0; f < kF4; ++f)
+        reinterpret_cast<float4*>(o)[f] = make_float4(a[4 * f] * inv, a[4 * f + 1] * inv,
+                                                      a[4 * f + 2] * inv, a[4 * f + 3] * inv);
+    } else if constexpr (kDl >= 8) {
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) a[e] = 0.f;
-    for (int base = 0; base < ns; base += 32) {
-      const int c = c0 + base + lane;
-      float w = 0.f;
-      int idx = 0;
-      if (base + lane < ns) {
-        const long long sc = (long long)c * U / gridDim.x;
-        if ((long long)(c + 1) * U / gridDim.x != sc) {
-          const int sl = c * 2 + ((c == c0 && sc < u0) ? 1 : 0);
-          idx = sl * nvec + vv;
-          const float2 ml = __ldcg(&p.ws_ml[idx]);
-          w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-          Lsum = fmaf(w, ml.y, Lsum);
-        }
-      }
-      // Four pieces per step: their loads are independent, so a row cut into
-      // many pieces (a long row of a small batch) does not pay one L2
-      // round trip per piece.
-      const int cnt = min(32, ns - base);
-      for (int k0 = 0; k0 < cnt; k0 += 4) {
-        float wk[4], v[4][kPer];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int kk = (k0 + u) & 31;
-          wk[u] = __shfl_sync(kFull, w, kk);
-          const int ik = __shfl_sync(kFull, idx, kk);
-          if (k0 + u >= cnt) wk[u] = 0.f;
-          const float* src = p.ws_acc + (size_t)(wk[u] != 0.f ? ik : 0) * D + lane * kPer;
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) v[u][e] = wk[u] != 0.f ? __ldcg(src + e) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) a[e] = fmaf(wk[u], v[u][e], a[e]);
-      }
-    }
-#pragma unroll
-    for (int o2 = 16; o2 >= 1; o2 >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, o2);
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    T* o = static_cast<T*>(p.out) + (((size_t)row * NQ + jq) * p.heads + qh) * D + lane * kPer;
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      if constexpr (sizeof(T) == 4) {
-        o[e] = a[e] * inv;
-      } else {
-        o[e] = __float2bfloat16_rn(a[e] * inv);
-      }
+      for (int f = 0; f < kDl / 8; ++f)
+        reinterpret_cast<uint4*>(o)[f] = make_uint4(
+            pack_bf16(a[8 * f] * inv, a[8 * f + 1] * inv), pack_bf16(a[8 * f + 2] * inv, a[8 * f + 3] * inv),
+            pack_bf16(a[8 * f + 4] * inv, a[8 * f + 5] * inv), pack_bf16(a[8 * f + 6] * inv, a[8 * f + 7] * inv));
+    } else {
+      *reinterpret_cast<uint2*>(o) =
+          make_uint2(pack_bf16(a[0] * inv, a[1] * inv), pack_bf16(a[2] * inv, a[3] * inv));
     }
   }
 }
@@ -633,12 +662,13 @@ __device__ __forceinline__ void finish_cut_row(const DecodeParams& p, int row, i
 // finish_cut_row for the TMEM form, out of line: it runs once per piece of a
 // cut row, and inlined into the softmax warps' stage loop its registers
 // pushed that loop's working set into local memory.
-template <typename T, int D>
+template <typename T, int D, int kLanes, int kChunk>
 __device__ __noinline__ void finish_cut_row_call(const DecodeParams& p, int row, int kv0,
                                                  const int* s_prefix, int N, long long U,
                                                  int nhg, int nvec, int v0, int nv, int ncw,
                                                  int cw, int lane, volatile int* s_merge) {
-  finish_cut_row<T, D>(p, row, kv0, s_prefix, N, U, nhg, nvec, v0, nv, ncw, cw, lane, s_merge);
+  finish_cut_row<T, D, kLanes, kChunk>(p, row, kv0, s_prefix, N, U, nhg, nvec, v0, nv, ncw, cw,
+                                       lane, s_merge);
 }
 
 // Tensor-core consumer (bf16) with the query vectors as the MMA rows: a KV
@@ -865,8 +895,8 @@ __device__ __forceinline__ void consume_mma(const DecodeParams& p, unsigned char
             *reinterpret_cast<float2*>(a + nd * 8) = make_float2(o[nd][rh * 2], o[nd][rh * 2 + 1]);
           if (t4 == 0) p.ws_ml[slot] = make_float2(m[rh], lt[rh]);
         }
-        finish_cut_row<T, D>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, vbase, nvw, ncw, cw,
-                             lane, s_merge);
+        finish_cut_row<T, D, 8, 2>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, vbase, nvw,
+                                   ncw, cw, lane, s_merge);
       }
     }
     __syncwarp();
@@ -1404,7 +1434,7 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
         const int vw = q4 * 32 - kvl * R;
         const int nvq = max(0, min(32, vpk - vw));
         const int nvw = max(0, min(16, nvq - hf * 16));
-        finish_cut_row_call<T, D>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec,
+        finish_cut_row_call<T, D, 8, 4>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec,
                                   kvl * vpk + vw + hf * 16, nvw, kNcw, cw, lane, s_merge);
       }
       tc_fence_before();
@@ -1632,8 +1662,8 @@ __device__ __forceinline__ void consume_mma_t(const DecodeParams& p, unsigned ch
           }
           if (g == 0) p.ws_ml[slot] = make_float2(m[c], lt[c]);
         }
-        finish_cut_row<T, D>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, vbase, nvw, ncw, cw,
-                             lane, s_merge);
+        finish_cut_row<T, D, 8, 2>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, vbase, nvw,
+                                   ncw, cw, lane, s_merge);
       }
     }
     __syncwarp();
@@ -2379,8 +2409,8 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
           }
           if (lane == 0) p.ws_ml[slot] = make_float2(m[k], lt[k]);
         }
-        finish_cut_row<T, D>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, v0, QW, ncw, cw, lane,
-                             s_merge);
+        finish_cut_row<T, D, 32 / QW, 2>(p, row, flags >> 16, s_prefix, N, U, nhg, nvec, v0,
+                                              QW, ncw, cw, lane, s_merge);
       }
     }
     __syncwarp();
