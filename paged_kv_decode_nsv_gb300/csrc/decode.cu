@@ -1899,20 +1899,33 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
     // with their bytes and publishes the stage (metadata, one arrival) when
     // it is full or its segment ends.  Lane 0 keeps the open stage: its row,
     // the flags of its first block, its blocks so far and their token masks.
+    // The open stage's bookkeeping is warp-uniform (every lane keeps the
+    // same copy, so a chunk of a window needs no broadcasts): whether a
+    // stage is open, its blocks so far and their token masks, whether any
+    // holds data or was gathered, its row and its first block's flags.
     int t_open = 0, t_nb = 0, t_row = 0, t_flags = 0, t_mask01 = 0, t_mask23 = 0;
     bool t_data = false, t_gath = false;
     const uint32_t t_vhalf = (uint32_t)HG * kBlock * 128;       // a block's V half
     const uint32_t t_karea = (uint32_t)NBS * L.kv_bytes;
-    auto tmem_close = [&](int last_flags) {  // lane 0
-      const uint32_t s = n % S;
-      int f = t_flags | (last_flags & kLast);
-      if (t_data) f |= kData;
-      if (t_gath) f |= kGathered;
-      s_meta[2 * s] = make_int4(t_row, 0, slot0 + ((f & kSlot1) ? 1 : 0), f);
-      s_meta[2 * s + 1] = make_int4(t_mask01, t_mask23, t_nb, 0);
-      mbar_arrive(bars + 8 * s);
+    auto tmem_close = [&](int last_flags) {  // every lane; lane 0 publishes
+      if (lane == 0) {
+        const uint32_t s = n % S;
+        int f = t_flags | (last_flags & kLast);
+        if (t_data) f |= kData;
+        if (t_gath) f |= kGathered;
+        s_meta[2 * s] = make_int4(t_row, 0, slot0 + ((f & kSlot1) ? 1 : 0), f);
+        s_meta[2 * s + 1] = make_int4(t_mask01, t_mask23, t_nb, 0);
+        mbar_arrive(bars + 8 * s);
+      }
       ++n;
       t_open = 0;
+    };
+    auto add_mask = [&](int bj, int mj) {
+      if (bj < 2)
+        t_mask01 |= mj << (16 * bj);
+      else
+        t_mask23 |= mj << (16 * (bj - 2));
+      if (mj) t_data = true;
     };
     // The warp gathers unit (row, blk) token by token (slot mode, a block
     // whose slots are not one aligned run) into block b of stage slot s, in
@@ -1956,13 +1969,14 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
       if (act && !tokw && !valid) atomicOr(p.status, (uint32_t)NSV_DEV_BAD_BLOCK);
       const unsigned wk = __ballot_sync(kFull, (valid || tokw) && (u_flags >> 16) == 0);
       if (lane == 0) walked += (unsigned long long)__popc(wk);
+      const unsigned vmw = __ballot_sync(kFull, valid);  // units copied
+      const unsigned gmw = __ballot_sync(kFull, tokw);   // units gathered token by token
       // this unit's index within its segment, modulo the stage size: the
       // blocks before the window of a segment that continues into it are
       // the open stage's (a closed stage holds NBS blocks)
       const unsigned fm = __ballot_sync(kFull, act && (u_flags & kFirst));
       const unsigned upto = fm & (0xffffffffu >> (31 - lane));  // firsts at lanes <= this one
-      const int c0 = __shfl_sync(kFull, t_nb, 0);
-      const int k = upto ? lane - (31 - __clz((int)upto)) : c0 + lane;
+      const int k = upto ? lane - (31 - __clz((int)upto)) : t_nb + lane;
       const bool ends = act && ((k % NBS) == NBS - 1 || (u_flags & kLast));
       const unsigned em = __ballot_sync(kFull, ends);
       int pos = 0;
@@ -1972,35 +1986,34 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
         const int row0 = __shfl_sync(kFull, u_row, pos);
         const int flags0 = __shfl_sync(kFull, u_flags, pos);
         const int flags_e = __shfl_sync(kFull, u_flags, e);
-        bool ok2 = true;
-        if (lane == 0 && !t_open) {
-          ok2 = wait_free();
-          if (ok2) {
-            t_open = 1;
-            t_nb = 0;
-            t_row = row0;
-            t_flags = flags0 & ~(kLast | kData | kGathered);
-            t_mask01 = t_mask23 = 0;
-            t_data = t_gath = false;
-            if (flags0 & kHasQ) {
-              // the piece's query rows, which the softmax warps load when it
-              // starts: into L2 now, a few stages ahead of them
-              const int qh0 = (flags0 >> 16) * G;
-              for (int jq = 0; jq < NQ; ++jq)
-                prefetch_l2(qp + (((size_t)row0 * NQ + jq) * p.heads + qh0) * D,
-                            (uint32_t)(HG * G * D * sizeof(T)));
-            }
+        if (!t_open) {
+          bool ok2 = true;
+          if (lane == 0) ok2 = wait_free();
+          if (!__shfl_sync(kFull, ok2, 0)) return false;
+          t_open = 1;
+          t_nb = 0;
+          t_row = row0;
+          t_flags = flags0 & ~(kLast | kData | kGathered);
+          t_mask01 = t_mask23 = 0;
+          t_data = t_gath = false;
+          if (flags0 & kHasQ) {
+            // the piece's query rows, which the softmax warps load when it
+            // starts: into L2 now, a few stages ahead of them (a lane per
+            // query token)
+            const int qh0 = (flags0 >> 16) * G;
+            for (int jq = lane; jq < NQ; jq += 32)
+              prefetch_l2(qp + (((size_t)row0 * NQ + jq) * p.heads + qh0) * D,
+                          (uint32_t)(HG * G * D * sizeof(T)));
           }
         }
-        if (!__shfl_sync(kFull, ok2, 0)) return false;
-        const uint32_t s = __shfl_sync(kFull, n, 0) % S;
-        const int nb0 = __shfl_sync(kFull, t_nb, 0);
+        const uint32_t s = n % S;
+        const int nb0 = t_nb;
         const bool mine = lane >= pos && lane <= e;
         const int bl = nb0 + lane - pos;  // this unit's block within the stage
-        int mymask = (mine && valid) ? 0xffff : 0;
-        // copies: each lane its own unit's (K: one box per 64-dim half, V:
-        // one box of both halves)
-        const unsigned vm = __ballot_sync(kFull, mine && valid);
+        const unsigned cm = (0xffffffffu >> (31 - e)) & (0xffffffffu << pos);  // lanes pos..e
+        const unsigned vm = vmw & cm, gm = gmw & cm;
+        // copies: each lane its own unit's (K: one box of both 64-dim
+        // halves, V: one box of both halves)
         const uint32_t full = bars + 8 * s;
         if (lane == 0 && vm) mbar_expect_tx(full, (uint32_t)__popc(vm) * 2u * L.kv_bytes);
         if (mine && valid) {
@@ -2010,34 +2023,25 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
           tma_load_3d(base + t_karea + (uint32_t)bl * L.kv_bytes, &p.tmap_v, 0, y, 0, full,
                       pol);
         }
-        // gathered units, one at a time with the whole warp
-        unsigned gm = __ballot_sync(kFull, mine && tokw);
-        while (gm) {
-          const int g = __ffs((int)gm) - 1;
-          gm &= gm - 1;
-          const int msk = tmem_gather(s, nb0 + g - pos, __shfl_sync(kFull, u_row, g),
-                                      __shfl_sync(kFull, u_blk, g),
-                                      __shfl_sync(kFull, u_flags, g));
-          if (lane == g) mymask = msk;
-        }
-        // the blocks' token masks, into lane 0's open stage
-        for (int j = pos; j <= e; ++j) {
-          const int mj = __shfl_sync(kFull, mymask, j);
-          if (lane == 0) {
-            const int bj = nb0 + j - pos;
-            if (bj < 2)
-              t_mask01 |= mj << (16 * bj);
-            else
-              t_mask23 |= mj << (16 * (bj - 2));
-            if (mj) t_data = true;
+        if (gm == 0) {
+          // a copied block has all its tokens (the consumers mask the
+          // positions past the row's end); a block out of the pool none
+          for (int j = 0; j <= e - pos; ++j) add_mask(nb0 + j, ((vm >> (pos + j)) & 1) ? 0xffff : 0);
+        } else {
+          // gathered units, one at a time with the whole warp
+          int mymask = (mine && valid) ? 0xffff : 0;
+          for (unsigned g2 = gm; g2; g2 &= g2 - 1) {
+            const int g = __ffs((int)g2) - 1;
+            const int msk = tmem_gather(s, nb0 + g - pos, __shfl_sync(kFull, u_row, g),
+                                        __shfl_sync(kFull, u_blk, g),
+                                        __shfl_sync(kFull, u_flags, g));
+            if (lane == g) mymask = msk;
           }
+          for (int j = pos; j <= e; ++j) add_mask(nb0 + j - pos, __shfl_sync(kFull, mymask, j));
+          t_gath = true;
         }
-        if (lane == 0) t_nb = nb0 + e - pos + 1;
-        const bool any_gath = __ballot_sync(kFull, mine && tokw) != 0;
-        if (lane == 0) {
-          if (any_gath) t_gath = true;
-          if (rest) tmem_close(flags_e);  // full, or the segment ends here
-        }
+        t_nb = nb0 + e - pos + 1;
+        if (rest) tmem_close(flags_e);  // full, or the segment ends here
         pos = e + 1;
       }
       return true;
