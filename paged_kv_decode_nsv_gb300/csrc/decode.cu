@@ -1142,6 +1142,41 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
   // this row's P: block b's tokens in 16-byte chunks 2b and 2b + 1
   unsigned char* const prow = pb + (r >> 3) * (pch * 128) + (r & 7) * 16;
 
+  // A segment's query vector of this row -> lane r of the Q operand in
+  // tensor memory, two dims to a column (as they lie in memory); each warp
+  // of the pair copies half of the dims.  Every scores MMA that read the
+  // previous query rows is complete (each was waited for below).
+  auto stage_q = [&](int qrow, int qkv0) {
+    const uint4* src = reinterpret_cast<const uint4*>(
+                           static_cast<const T*>(p.q) +
+                           (((size_t)qrow * NQ + jq) * p.heads + qkv0 * G + qhl) * D) +
+                       hf * (D / 16);
+    constexpr int kWords = D / 4;  // this warp's columns: D / 2 dims
+    uint32_t w[kWords];
+#pragma unroll
+    for (int c = 0; c < kWords / 4; ++c) {
+      const uint4 v4 = rok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      w[4 * c] = v4.x;
+      w[4 * c + 1] = v4.y;
+      w[4 * c + 2] = v4.z;
+      w[4 * c + 3] = v4.w;
+    }
+    const uint32_t qt = tmem + lane_base + s_col + 2u * (uint32_t)ntok + (uint32_t)(hf * kWords);
+    if constexpr (kWords == 32) {
+      tmem_st32(qt, w);
+    } else {
+      tmem_st16(qt, w);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tb.qready());
+  };
+  // whether the next segment's query rows are already in place: a
+  // segment's last stage stages them (once its own scores are done), so
+  // the next segment's first scores can run during this one's epilogue
+  bool q_staged = false;
+
   float m = -INFINITY, l = 0.f;  // l: this warp's part of the running sum
   bool fresh = true;   // no P.V yet in this piece: O holds nothing of it
   uint32_t pv_s = 0, pv_ph = 0;  // stage and phase of the last P.V handed over
@@ -1170,33 +1205,8 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
       l = 0.f;
       fresh = true;
       if (flags & kHasQ) {
-        // this row's query vector -> lane r of the Q operand in tensor
-        // memory, two dims to a column (as they lie in memory); each warp of
-        // the pair copies half of the dims.  Every earlier scores MMA is
-        // complete (each was waited for below).
-        const uint4* src = reinterpret_cast<const uint4*>(
-            static_cast<const T*>(p.q) + (((size_t)meta.x * NQ + jq) * p.heads + qh0 + qhl) * D) +
-            hf * (D / 16);
-        constexpr int kWords = D / 4;  // this warp's columns: D / 2 dims
-        uint32_t w[kWords];
-#pragma unroll
-        for (int c = 0; c < kWords / 4; ++c) {
-          const uint4 v4 = rok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-          w[4 * c] = v4.x;
-          w[4 * c + 1] = v4.y;
-          w[4 * c + 2] = v4.z;
-          w[4 * c + 3] = v4.w;
-        }
-        const uint32_t qt = tmem + lane_base + s_col + 2u * (uint32_t)ntok + (uint32_t)(hf * kWords);
-        if constexpr (kWords == 32) {
-          tmem_st32(qt, w);
-        } else {
-          tmem_st16(qt, w);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tb.qready());
+        if (!q_staged) stage_q(meta.x, flags >> 16);
+        q_staged = false;
       }
     }
 
@@ -1371,6 +1381,10 @@ __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned cha
     if (lane == 0) mbar_arrive(tb.handed(b));
 
     if (flags & kLast) {
+      if (meta.y > 0) {  // the next segment's query rows, while P.V runs
+        stage_q(meta.y - 1, mm.w);
+        q_staged = true;
+      }
       const int row = meta.x;
       // the piece's last P.V is complete
       if (!mbar_wait(tb.out(), nout & 1)) {
@@ -1907,14 +1921,18 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
     bool t_data = false, t_gath = false;
     const uint32_t t_vhalf = (uint32_t)HG * kBlock * 128;       // a block's V half
     const uint32_t t_karea = (uint32_t)NBS * L.kv_bytes;
-    auto tmem_close = [&](int last_flags) {  // every lane; lane 0 publishes
-      if (lane == 0) {
+    // A stage that ends a segment also names the next segment's row and
+    // head group (row + 1 in its first metadata word's y, 0 when this CTA
+    // has none), so the consumers can stage that segment's query rows early.
+    auto tmem_close = [&](int last_flags, int next_row1, int next_flags) {
+      if (lane == 0) {  // every lane keeps the bookkeeping; lane 0 publishes
         const uint32_t s = n % S;
         int f = t_flags | (last_flags & kLast);
         if (t_data) f |= kData;
         if (t_gath) f |= kGathered;
-        s_meta[2 * s] = make_int4(t_row, 0, slot0 + ((f & kSlot1) ? 1 : 0), f);
-        s_meta[2 * s + 1] = make_int4(t_mask01, t_mask23, t_nb, 0);
+        const bool nx = (f & kLast) && next_row1 > 0;
+        s_meta[2 * s] = make_int4(t_row, nx ? next_row1 : 0, slot0 + ((f & kSlot1) ? 1 : 0), f);
+        s_meta[2 * s + 1] = make_int4(t_mask01, t_mask23, t_nb, nx ? next_flags >> 16 : 0);
         mbar_arrive(bars + 8 * s);
       }
       ++n;
@@ -1961,8 +1979,11 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
       __syncwarp();
       return mask;
     };
-    // One window of units (lane j holds unit w0 + j, nwin of them valid).
-    auto tmem_window = [&](int nwin, int u_row, int u_blk, int u_flags, int u_phys) -> bool {
+    // One window of units (lane j holds unit w0 + j, nwin of them valid);
+    // x_row1 / x_flags: the row + 1 and flags of the unit after the window
+    // (x_row1 = 0: none in this CTA's range).
+    auto tmem_window = [&](int nwin, int u_row, int u_blk, int u_flags, int u_phys, int x_row1,
+                           int x_flags) -> bool {
       const bool act = lane < nwin;
       const bool tokw = act && u_phys == kTokenWise;
       const bool valid = act && !tokw && u_phys >= 0 && (long long)u_phys < p.pool_blocks;
@@ -1983,10 +2004,9 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
       while (pos < nwin) {
         const unsigned rest = em & (0xffffffffu << pos);
         const int e = rest ? __ffs((int)rest) - 1 : nwin - 1;
-        const int row0 = __shfl_sync(kFull, u_row, pos);
-        const int flags0 = __shfl_sync(kFull, u_flags, pos);
-        const int flags_e = __shfl_sync(kFull, u_flags, e);
         if (!t_open) {
+          const int row0 = __shfl_sync(kFull, u_row, pos);
+          const int flags0 = __shfl_sync(kFull, u_flags, pos);
           bool ok2 = true;
           if (lane == 0) ok2 = wait_free();
           if (!__shfl_sync(kFull, ok2, 0)) return false;
@@ -2041,7 +2061,13 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
           t_gath = true;
         }
         t_nb = nb0 + e - pos + 1;
-        if (rest) tmem_close(flags_e);  // full, or the segment ends here
+        if (rest) {  // full, or the segment ends here
+          const int src = (e + 1) & 31;
+          const int flags_e = __shfl_sync(kFull, u_flags, e);
+          const int r1 = __shfl_sync(kFull, u_row, src) + 1, f1 = __shfl_sync(kFull, u_flags, src);
+          const bool in_win = e + 1 < nwin;
+          tmem_close(flags_e, in_win ? r1 : x_row1, in_win ? f1 : x_flags);
+        }
         pos = e + 1;
       }
       return true;
@@ -2110,7 +2136,11 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 2) * 32
       int n_row = 0, n_blk = 0, n_flags = 0, n_phys = -1;
       if (nw0 + lane < end) unit_at(nw0 + lane, n_row, n_blk, n_flags, n_phys);
       const int nwin = (int)min(32ll, end - w0);
-      if constexpr (MMA == kMmaTmem) ok = tmem_window(nwin, c_row, c_blk, c_flags, c_phys);
+      if constexpr (MMA == kMmaTmem) {
+        // the unit after this window, if this CTA has one
+        const int x_row = __shfl_sync(kFull, n_row, 0), x_flags = __shfl_sync(kFull, n_flags, 0);
+        ok = tmem_window(nwin, c_row, c_blk, c_flags, c_phys, nw0 < end ? x_row + 1 : 0, x_flags);
+      }
       for (int jj = 0; MMA != kMmaTmem && jj < nwin && ok; ++jj) {
         const int row = __shfl_sync(kFull, c_row, jj);
         int flags = __shfl_sync(kFull, c_flags, jj);
