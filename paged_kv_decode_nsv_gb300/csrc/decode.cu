@@ -561,9 +561,12 @@ __device__ __forceinline__ void finish_cut_row(const DecodeParams& p, int row, i
   if (!*s_merge) return;
   __threadfence();
   // 32 / kLpv vectors at a time, kLpv lanes each; lane dq of a vector owns
-  // dims [dq*kDl, (dq+1)*kDl).  Every load of a step is independent of the
-  // others, so merging a batch of vectors costs about 1 + ns/kChunk L2 round
-  // trips (the partials were just written by other CTAs: read through L2).
+  // the 4-dim groups dq, dq + kLpv, dq + 2 kLpv, ... (dims 4(f kLpv + dq) ..
+  // + 3 for f = 0 .. kF4 - 1), so that one load instruction's lanes read a
+  // vector's partial in whole sectors.  Every load of a step is independent
+  // of the others, so merging a batch of vectors costs about 1 + ns/kChunk
+  // L2 round trips (the partials were just written by other CTAs: read
+  // through L2).
   constexpr int kLpv = kLanes < D / 4 ? kLanes : D / 4;
   constexpr int kDl = D / kLpv;
   constexpr int kF4 = kDl / 4;
@@ -620,9 +623,10 @@ __device__ __forceinline__ void finish_cut_row(const DecodeParams& p, int row, i
         const int sl = kk0 + u < ns ? slot_k(kk0 + u) : -1;
         const size_t idx = (size_t)(sl < 0 ? 0 : sl) * nvec + vv;
         ml[u] = sl < 0 ? make_float2(-INFINITY, 0.f) : __ldcg(&p.ws_ml[idx]);
-        const float4* src = reinterpret_cast<const float4*>(p.ws_acc + idx * D + dq * kDl);
+        const float4* src = reinterpret_cast<const float4*>(p.ws_acc + idx * D) + dq;
 #pragma unroll
-        for (int f = 0; f < kF4; ++f) v[u][f] = sl < 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldcg(src + f);
+        for (int f = 0; f < kF4; ++f)
+          v[u][f] = sl < 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldcg(src + f * kLpv);
       }
 #pragma unroll
       for (int u = 0; u < kChunk; ++u) {
@@ -640,21 +644,17 @@ __device__ __forceinline__ void finish_cut_row(const DecodeParams& p, int row, i
     const int kvl = vv / vpk, rem = vv - kvl * vpk;
     const int qh = qh0 + kvl * G + rem / NQ, jq = rem % NQ;
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-    T* o = static_cast<T*>(p.out) + (((size_t)row * NQ + jq) * p.heads + qh) * D + dq * kDl;
-    if constexpr (sizeof(T) == 4) {
+    T* o = static_cast<T*>(p.out) + (((size_t)row * NQ + jq) * p.heads + qh) * D + 4 * dq;
 #pragma unroll
-      for (int f = 0; f < kF4; ++f)
-        reinterpret_cast<float4*>(o)[f] = make_float4(a[4 * f] * inv, a[4 * f + 1] * inv,
-                                                      a[4 * f + 2] * inv, a[4 * f + 3] * inv);
-    } else if constexpr (kDl >= 8) {
-#pragma unroll
-      for (int f = 0; f < kDl / 8; ++f)
-        reinterpret_cast<uint4*>(o)[f] = make_uint4(
-            pack_bf16(a[8 * f] * inv, a[8 * f + 1] * inv), pack_bf16(a[8 * f + 2] * inv, a[8 * f + 3] * inv),
-            pack_bf16(a[8 * f + 4] * inv, a[8 * f + 5] * inv), pack_bf16(a[8 * f + 6] * inv, a[8 * f + 7] * inv));
-    } else {
-      *reinterpret_cast<uint2*>(o) =
-          make_uint2(pack_bf16(a[0] * inv, a[1] * inv), pack_bf16(a[2] * inv, a[3] * inv));
+    for (int f = 0; f < kF4; ++f) {
+      T* of = o + 4 * f * kLpv;
+      if constexpr (sizeof(T) == 4) {
+        *reinterpret_cast<float4*>(of) = make_float4(a[4 * f] * inv, a[4 * f + 1] * inv,
+                                                     a[4 * f + 2] * inv, a[4 * f + 3] * inv);
+      } else {
+        *reinterpret_cast<uint2*>(of) = make_uint2(pack_bf16(a[4 * f] * inv, a[4 * f + 1] * inv),
+                                                   pack_bf16(a[4 * f + 2] * inv, a[4 * f + 3] * inv));
+      }
     }
   }
 }
