@@ -195,20 +195,25 @@ typedef struct nsv_plan {
  *                       fits.  A stage holds blocks_per_stage consecutive
  *                       blocks of one row (fewer at a segment's end), and
  *                       one scores MMA per 16 dims covers all of them.
- *                       Four softmax warps (one thread per row) and an MMA
- *                       warp that issues the next stage's scores while the
- *                       softmax warps work; K/V tiles by 2-D TMA as above.
+ *                       One CTA per SM: a producer warp, eight softmax
+ *                       warps (one thread per row, two warps per tensor-
+ *                       memory lane quadrant) and an MMA warp that issues
+ *                       the next stage's scores while the softmax warps
+ *                       work; K and V tiles by one multi-dimensional TMA box
+ *                       per block.  At head_dim 64 the default takes it
+ *                       from 33 query vectors per KV head.
  * The default plan takes NSV_CONSUMER_TENSOR for bf16 shapes with 2 to 8
  * query vectors per KV head, NSV_CONSUMER_TENSOR_VECTOR_ROWS for 9 to 16,
- * NSV_CONSUMER_TENSOR_TMEM for 17 to 64 when its group can be 2 or 4 KV
- * heads (NSV_CONSUMER_TENSOR_VECTOR_ROWS otherwise, for example for an odd
- * num_kv_heads), and the CUDA-core one otherwise.  Outside the TMEM form
+ * NSV_CONSUMER_TENSOR_TMEM for 17 to 64 (33 to 64 at head_dim 64) when its
+ * group can be 2 or 4 KV heads (NSV_CONSUMER_TENSOR_VECTOR_ROWS otherwise,
+ * for example for an odd num_kv_heads), and the CUDA-core one otherwise.  Outside the TMEM form
  * the default kv_heads_per_cta is, among 1 and the groups whose K+V stage
  * is at most 64 KiB and whose vectors need at most 8 consumer warps, the
  * one whose plan keeps the most consumer warps resident per SM (counted up
  * to 16; the larger group on a tie), and the default ctas_per_sm is as many
- * as shared memory, threads and registers allow, up to 8 (2 for the TMEM
- * form).  The default ring is 3 stages; a tensor-core CTA alone on its SM
+ * as shared memory, threads and registers allow, up to 8 (1 for the TMEM
+ * form, which takes the largest blocks_per_stage that leaves it a ring of
+ * at least 3 stages, up to 6).  The default ring is 3 stages; a tensor-core CTA alone on its SM
  * deepens it to fill shared memory (up to 6), and a CUDA-core CTA that
  * streams all of one or two KV heads in stages of at most 16 KiB takes 2
  * where that fits more CTAs per SM. */
