@@ -21,7 +21,7 @@ e2e       = the same metric through the C ABI with the step's inputs in
             inside the timed region (the KV pool is the resident cache and
             stays on the device).
 roofline  = the decode read alone, timed in a separate loop of
-            nsv_paged_decode_ws calls (a 4 KiB counter memset + the kernel,
+            nsv_paged_decode_ws calls (the counter-zeroing kernel + the read,
             each between its own CUDA events): read bytes (K+V + q + out) /
             its time, against the measured HBM copy bandwidth in
             MEASURED_PEAKS.json (a read+write copy, which a read-only
@@ -327,7 +327,7 @@ def run_nsv(args, wl):
             ev_e.record(stream)
 
     def read(ev_s=None, ev_e=None):
-        """The decode read alone (its counter memset and its kernel), for the
+        """The decode read alone (its counter-zeroing kernel and the read), for the
         roofline of the dominant kernel."""
         flush_l2()
         if ev_s is not None:
@@ -472,7 +472,7 @@ def run_nsv(args, wl):
         "gpu_launches": K * launches_per_step,
         "gpu_launches_note": "timed region = K nsv_decode_step calls: kv_write_kernel + "
                              "decode_kernel each; the roofline's read-only loop is timed "
-                             "separately (a 4 KiB counter memset + decode_kernel per launch)",
+                             "separately (the counter-zeroing kernel + decode_kernel per launch)",
         "clocks": clocks,
     }
     if cpu is not None:

@@ -309,9 +309,10 @@ NSV_API int nsv_paged_decode(const nsv_shape *shape, const void *q, const void *
  * Decode read with an explicit plan (NULL: the default plan) and a
  * caller-owned device workspace of at least plan->workspace_bytes bytes
  * (256-byte aligned).  The workspace holds no state between calls; each
- * call clears the part that must start at zero with one cudaMemsetAsync on
- * `stream` before its kernel.  Two calls that overlap on the GPU need two
- * workspaces.  A plan passed in must be one nsv_plan_split/nsv_plan_custom
+ * call clears the part that must start at zero on `stream` with a small
+ * kernel of its own (the append kernel given no rows), and launches the
+ * read programmatically dependent on it.  Two calls that overlap on the GPU
+ * need two workspaces.  A plan passed in must be one nsv_plan_split/nsv_plan_custom
  * returned for this shape (NSV_ERR_RANGE otherwise).
  *
  * The workspace is the read's only intermediate in device memory: one
@@ -367,8 +368,8 @@ NSV_API int nsv_decode_step(const nsv_shape *shape, const nsv_plan *plan, const 
  * allocation); make that first call before any stream capture.  Calls share
  * the buffer: two calls whose kernels overlap on the GPU race on it.  The
  * caller never clears it: the part that must start at zero (the read's
- * arrival counters) is zeroed by each call with a cudaMemsetAsync on
- * `stream`, and each call writes the rest before reading it.
+ * arrival counters) is zeroed by each call on `stream` with a small kernel
+ * of its own, and each call writes the rest before reading it.
  */
 #define NSV_NOALLOC_SCRATCH_BYTES (4u << 20)
 

@@ -20,8 +20,9 @@
 //
 // All calls on one device share the buffer.  Its first part holds the read's
 // arrival counters (one per row and KV-head group), which must be zero when
-// the kernel starts: nsv_paged_decode_ws clears them with a cudaMemsetAsync
-// on the caller's stream before every launch (no allocation).  Everything
+// the kernel starts: nsv_paged_decode_ws clears them on the caller's
+// stream before every launch, with a small kernel of its own (no
+// allocation).  Everything
 // else in it (the partial softmax states of rows cut between CTAs) each call
 // writes before it reads it.  So a caller never clears the buffer, whatever
 // an earlier call left there; but calls whose kernels overlap on the GPU

@@ -565,18 +565,20 @@ int decode_impl(const nsv_shape* s, const nsv_plan* plan_in, const void* q, cons
     }
   }
   // The arrival counters of cut rows start every call at zero: zeroed by
-  // the step's append launch, or by a memset.
-  if (append) {
-    append->zero_words = reinterpret_cast<int32_t*>(wsb);
-    append->zero_count = (int)(W.cnt_bytes / 4);
-    if (launch_kv_write(*append, stream) != cudaSuccess) return cuda_fail();
-  } else if (cudaMemsetAsync(wsb, 0, W.cnt_bytes, stream) != cudaSuccess) {
-    return cuda_fail();
+  // the step's append launch, or, for the read alone, by the same kernel
+  // with no rows to append.
+  KvWriteParams zero;
+  if (!append) {
+    memset(&zero, 0, sizeof zero);
+    append = &zero;
   }
-  // In the fused step the read may start while the append runs: it reads
-  // only the step's inputs until the append has completed.
+  append->zero_words = reinterpret_cast<int32_t*>(wsb);
+  append->zero_count = (int)(W.cnt_bytes / 4);
+  if (launch_kv_write(*append, stream) != cudaSuccess) return cuda_fail();
+  // The read may start while that kernel runs (programmatic dependent
+  // launch): it reads only the step's inputs until the kernel has completed.
   if (launch_decode(p, s->dtype, s->head_dim, plan.vectors_per_warp, plan.consumer, plan.grid,
-                    plan.threads, plan.smem_bytes, stream, append != nullptr) != cudaSuccess)
+                    plan.threads, plan.smem_bytes, stream, true) != cudaSuccess)
     return cuda_fail();
   return NSV_OK;
 }
