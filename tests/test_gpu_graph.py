@@ -10,7 +10,7 @@ batch of that shape written into the same buffers.
 import numpy as np
 import pytest
 
-from gpu_common import assert_parity, gpu_out_f64, oracle_step
+from gpu_common import assert_parity, gpu_out_f64, oracle_read, oracle_step
 from paged_kv_decode_nsv_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -84,6 +84,57 @@ def test_graph_recorded_on_padding_replays_real_steps(heads, kv_heads, consumer)
         st, _ = nsv.device_status(clear=True)
         assert st == 0
         assert_parity("bf16", gpu_out_f64(out), oracle_step(wl, host))
+
+
+@pytest.mark.parametrize("heads,kv_heads,consumer", [(8, 8, 1), (16, 4, 4)])
+def test_graph_of_the_read_alone_replays_real_batches(heads, kv_heads, consumer):
+    """The read alone on a caller workspace (nsv_paged_decode_ws) under
+    capture: its counter-zeroing kernel and the read launched dependent on it
+    are recorded over an all-padding batch and replayed over two real ones,
+    each checked against the oracle's read."""
+    import torch
+    from paged_kv_decode_nsv_gb300 import nsv
+    base, wa, wb = _batches(heads, kv_heads)
+    R, H, D = base["rows"], base["heads"], base["head_dim"]
+    dev = "cuda"
+    _, kp, vp, _, _ = W.device_values(wa, dev, value_seed=9)
+    q = torch.zeros((R, H, D), dtype=torch.bfloat16, device=dev)
+    tables = torch.full((R, base["max_blocks"]), -1, dtype=torch.int32, device=dev)
+    ctx = torch.zeros((R,), dtype=torch.int32, device=dev)                # all padding
+    out = torch.full((R, H, D), 3.0, dtype=torch.bfloat16, device=dev)
+    shape = nsv.shape_of(q, kp, tables)
+    plan = nsv.plan_split(shape) if consumer < 4 else nsv.plan_custom(shape, consumer=consumer)
+    assert plan.consumer == consumer
+    ws = nsv.workspace_for(plan)
+    scale = wa.scale
+
+    def read():
+        nsv.paged_decode_ws(q, kp, vp, tables, ctx, scale, out, workspace=ws, plan=plan)
+
+    read()                                     # first call on the device: set-up, uncaptured
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            read()
+    torch.cuda.current_stream().wait_stream(s)
+    out.fill_(3.0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out).item() == 0, "a warm batch reads nothing"
+    for wl, seed in ((wa, 201), (wb, 202)):
+        hq, _, _, _, _ = W.host_values(wl, value_seed=seed)
+        host = dict(q=hq, k_pool=W.to_numpy(kp), v_pool=W.to_numpy(vp))
+        q.copy_(torch.from_numpy(hq).view(torch.bfloat16))
+        tables.copy_(torch.from_numpy(wl.block_tables))
+        ctx.copy_(torch.from_numpy(wl.context_lens))
+        g.replay()
+        torch.cuda.synchronize()
+        st, _ = nsv.device_status(clear=True)
+        assert st == 0
+        assert_parity("bf16", gpu_out_f64(out), oracle_read(wl, host))
 
 
 def test_library_workspace_refuses_to_grow_under_capture():
