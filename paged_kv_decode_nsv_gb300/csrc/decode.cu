@@ -1085,8 +1085,10 @@ __device__ __forceinline__ bool tmem_mma_warp(const DecodeParams& p, unsigned ch
 // through shared memory, keeps the same running max and rescale decisions,
 // and splits the output columns for the rescale and the epilogue; each warp
 // keeps its own part of the running sum.  The query rows of a piece come
-// straight from global memory (the form keeps no q ring; the producer
-// prefetches them into L2 when it opens the piece).
+// straight from global memory into tensor memory (the form keeps no q ring;
+// the producer prefetches them into L2 when it opens the piece's first
+// stage, and the softmax warps stage them during the previous piece's
+// epilogue when that piece's last stage names it).
 template <int D>
 __device__ __forceinline__ void consume_tmem(const DecodeParams& p, unsigned char* smem,
                                              const SmemLayout& L, const int4* s_meta,
@@ -1916,8 +1918,7 @@ __global__ void __launch_bounds__(MMA == kMmaTmem ? (kTmemWarps + 3) * 32
     // stage and fills a stage in one pass: every lane issues the copies of
     // its own unit of the window, lane 0 arms the stage's full barrier once
     // with their bytes and publishes the stage (metadata, one arrival) when
-    // it is full or its segment ends.  Lane 0 keeps the open stage: its row,
-    // the flags of its first block, its blocks so far and their token masks.
+    // it is full or its segment ends.
     // The open stage's bookkeeping is warp-uniform (every lane keeps the
     // same copy, so a chunk of a window needs no broadcasts): whether a
     // stage is open, its blocks so far and their token masks, whether any
