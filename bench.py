@@ -273,6 +273,10 @@ def workload_config(wl):
 
 
 def run_nsv(args, wl):
+    # the library first: without it this arm stops here (ImportError), before
+    # any device work, and has no other path to take
+    from paged_kv_decode_nsv_gb300 import nsv
+    from paged_kv_decode_nsv_gb300 import workloads as W
     import torch
     import torch.distributed as dist
 
@@ -280,9 +284,6 @@ def run_nsv(args, wl):
     torch.cuda.set_device(local)
     if ws > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-
-    from paged_kv_decode_nsv_gb300 import nsv
-    from paged_kv_decode_nsv_gb300 import workloads as W
 
     # The oracle sample runs first, on the host, before the GPU work starts.
     cpu = cpu1 = None

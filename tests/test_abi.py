@@ -467,3 +467,22 @@ def test_plan_head_dim_64_tmem_rule(nsv, heads, kv_heads, qlen, consumer):
     p = nsv.plan_split(_shape(nsv, num_heads=heads, num_kv_heads=kv_heads, query_len=qlen,
                               head_dim=64), num_sms=152)
     assert p.consumer == consumer
+
+
+def test_binding_refuses_to_load_without_the_library(tmp_path):
+    """No fallback: a copy of the package without its built library cannot
+    be imported as a binding, and bench.py's GPU arm exits non-zero."""
+    import sys
+    pkg = tmp_path / "paged_kv_decode_nsv_gb300"
+    shutil.copytree(os.path.join(ROOT, "paged_kv_decode_nsv_gb300"), pkg,
+                    ignore=shutil.ignore_patterns("_lib", "_build", "__pycache__"))
+    r = subprocess.run([sys.executable, "-c", "import paged_kv_decode_nsv_gb300.nsv"],
+                       cwd=tmp_path, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "libnsv.so is not built" in r.stderr
+    shutil.copy(os.path.join(ROOT, "bench.py"), tmp_path / "bench.py")
+    r = subprocess.run([sys.executable, "bench.py", "--workload", "tiny_f32", "--steps", "1",
+                        "--warmup", "3", "--cpu-seconds", "0"],
+                       cwd=tmp_path, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0 and "libnsv.so is not built" in r.stderr
+    assert not [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
