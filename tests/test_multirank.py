@@ -1,4 +1,5 @@
-"""The benchmark's multi-rank logic on the CPU (gloo, world size 2).
+"""The benchmark's host-side logic on the CPU: its multi-rank timing (gloo,
+world size 2) and the roofline's recorded traffic.
 
 The decode read shards by rows with no exchange step, so N GPUs run N
 independent batches; the only cross-rank operations are the timing barrier
@@ -71,3 +72,19 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["unit"] == "GB/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_recorded_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from the committed ncu capture only while the
+    decode kernel's source is the one it was taken on: every consumer form
+    has an entry for the current source, and a changed source gives null."""
+    sys.path.insert(0, ROOT)
+    import bench
+    got = {c: bench.recorded_traffic(c, 1e9) for c in (1, 2, 3, 4)}
+    assert all(v is not None for v in got.values()), got
+    # the captured kernels read their unique bytes about once
+    assert all(0.9e9 < v < 1.1e9 for v in got.values()), got
+    changed = tmp_path / "decode.cu"
+    changed.write_bytes(open(bench.DECODE_SRC, "rb").read() + b"\n// changed\n")
+    monkeypatch.setattr(bench, "DECODE_SRC", str(changed))
+    assert all(bench.recorded_traffic(c, 1e9) is None for c in (1, 2, 3, 4))
